@@ -1,0 +1,399 @@
+"""Benchmark of the indexer backward on GB300: one step = score-grad + gemm
+stage (dQ, dW, dK) over one batch of seeded synthetic inputs of the anchor
+workload (B=1, H=64, D=128, S_k=4096, S_q=8192, topk=1024, causal top-k ids).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode atomic|det]
+                  [--workload anchor] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` is nominal gemm-stage TFLOP/s of the
+whole step (6*S_q*topk*H*D per step, all ranks), inputs resident in HBM;
+`e2e` is the same metric through the public API with pinned-host inputs and
+results copied inside the timed region; `roofline` covers the gemm-stage
+kernel; `cpu_baseline` times the fp64 oracle on a bounded row sample.
+`--impl reference` times the oracle itself as the reference arm.
+With N > 1 every rank runs an independent replica (weak scaling); the path
+has no exchange step between replicas.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "indexer-bwd kernel µs & TFLOP/s (frac of bf16 peak), H64 D128 Sq8192 topk1024"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="anchor", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--mode", default="atomic", choices=["atomic", "det"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]), "src": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "src": "fallback"}
+
+
+# ------------------------------------------------------------ distributed ---
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws, backend):
+    import torch.distributed as td
+    if ws > 1 and not td.is_initialized():
+        td.init_process_group(backend)
+    return td if ws > 1 else None
+
+
+# ------------------------------------------------------------ oracle legs ---
+
+def oracle_sample(wl: synth.Workload, x: dict, I: np.ndarray, rows: np.ndarray):
+    """Runs the oracle's score-grad and gemm stage on the given query rows
+    (B == 1 workloads).  Returns the nominal FLOPs of the sample."""
+    import oracle
+    q = x["q"][:, rows]
+    w = x["w"][:, rows]
+    if wl.dense:
+        raise ValueError("row samples of the dense workload are not supported")
+    idx = x["idx"][:, rows]
+    dI = oracle.score_grad_sparse(I[:, rows], x["attn"][:, rows], idx, wl.S_k)
+    # the scale 1/S_q of the full problem: score_grad_sparse divides by the
+    # sample's row count, so rescale to the workload's
+    dI *= len(rows) / wl.S_q
+    oracle.gemm_sparse(q, x["k"], w, dI, idx, wl.S_k)
+    return 6.0 * len(rows) * wl.topk * wl.H * wl.D
+
+
+def cpu_baseline(wl, x, I, seconds):
+    import oracle
+    cores = oracle.set_threads(0)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(wl.S_q)
+    flops = 0.0
+    done = 0
+    t0 = time.perf_counter()
+    chunk = 256
+    while done < wl.S_q and time.perf_counter() - t0 < seconds:
+        rows = np.sort(order[done:done + chunk])
+        flops += oracle_sample(wl, x, I, rows)
+        done += len(rows)
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {wl.S_q} query rows (random, full rows), score-grad + gemm stage, fp64, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    x = synth.make_inputs(wl)
+    # index_score = the forward logits, from the oracle's own forward (the
+    # reference arm runs nothing but the oracle)
+    rng = np.random.default_rng(1)
+    cores = oracle.set_threads(0)
+    # calibrate: seconds per row, then size each step's sample so that the
+    # whole run takes about a minute
+    cal = np.sort(rng.permutation(wl.S_q)[:32])
+    Ic = np.zeros((wl.B, wl.S_q, wl.topk), np.float32)
+    Ic[:, cal] = oracle.forward_sparse(x["q"][:, cal], x["k"], x["w"][:, cal], x["idx"][:, cal], wl.S_k)
+    t0 = time.perf_counter()
+    oracle_sample(wl, x, Ic, cal)
+    per_row = (time.perf_counter() - t0) / len(cal)
+    total_steps = args.steps + args.warmup
+    nrows = int(max(8, min(wl.S_q, 60.0 / max(total_steps, 1) / max(per_row, 1e-6))))
+    times, flops = [], 0.0
+    for s in range(total_steps):
+        rows = np.sort(rng.permutation(wl.S_q)[:nrows])
+        I = np.zeros((wl.B, wl.S_q, wl.topk), np.float32)
+        I[:, rows] = oracle.forward_sparse(x["q"][:, rows], x["k"], x["w"][:, rows], x["idx"][:, rows], wl.S_k)
+        t0 = time.perf_counter()
+        f = oracle_sample(wl, x, I, rows)
+        el = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(el)
+            flops += f
+    total = sum(times)
+    val = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(len(times), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: B={wl.B} H={wl.H} D={wl.D} S_q={wl.S_q} S_k={wl.S_k} topk={wl.topk}",
+                   "sample_rows_per_step": nrows},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{nrows} random full query rows per step of {wl.S_q}, "
+                                   "score-grad + gemm stage, fp64"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm ---
+
+def forward_logits(torch, q, k, w, idx, S_k, chunk=256):
+    """Input preparation: index_score = sum_h w relu(q.k_sel) per valid slot,
+    computed with plain torch ops in fp32 (not part of the timed path)."""
+    B, S_q, H, D = q.shape
+    out = torch.zeros(idx.shape, dtype=torch.float32, device=q.device)
+    for b in range(B):
+        for t0 in range(0, S_q, chunk):
+            ids = idx[b, t0:t0 + chunk].long()
+            valid = (ids >= 0) & (ids < S_k)
+            kg = k[b][ids.clamp(0, S_k - 1)].float()                # [c, topk, D]
+            z = torch.einsum("chd,ctd->cht", q[b, t0:t0 + chunk].float(), kg)
+            I = torch.einsum("ch,cht->ct", w[b, t0:t0 + chunk], torch.relu(z))
+            out[b, t0:t0 + chunk] = torch.where(valid, I, torch.zeros_like(I))
+    return out
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax = float(row[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args, wl):
+    import torch
+    import sparse_attention_indexer_bwd_gb300 as ibwd
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    td = dist_init(ws, "nccl")
+    if wl.dense:
+        raise SystemExit("the benchmark times the top-k workloads (the dense variant is a parity case)")
+    mode = ibwd.IBWD_DK_DETERMINISTIC if args.mode == "det" else ibwd.IBWD_DK_ATOMIC
+
+    # ---- inputs (seeded, synthetic; resident in HBM before timing)
+    x = synth.make_inputs(wl)
+    q = torch.from_numpy(x["q"].view(np.int16)).to(dev).view(torch.bfloat16)
+    k = torch.from_numpy(x["k"].view(np.int16)).to(dev).view(torch.bfloat16)
+    w = torch.from_numpy(x["w"]).to(dev)
+    idx = torch.from_numpy(x["idx"]).to(dev)
+    attn0 = torch.from_numpy(x["attn"]).to(dev)
+    I = forward_logits(torch, q, k, w, idx, wl.S_k)
+    B, S_q, H, D = q.shape
+    dq = torch.empty((B, S_q, H, D), dtype=torch.float32, device=dev)
+    dw = torch.empty((B, S_q, H), dtype=torch.float32, device=dev)
+    dk = torch.empty((B, wl.S_k, D), dtype=torch.float32, device=dev)
+    wsb = torch.empty(ibwd.indexer_bwd_gemm_workspace_size(B, S_q, wl.S_k, H, D, wl.topk, mode),
+                      dtype=torch.uint8, device=dev)
+    # score-grad overwrites attn_score with dI: every step gets its own copy
+    nbuf = args.steps + args.warmup
+    attn = [attn0.clone() for _ in range(nbuf)]
+    stream = torch.cuda.current_stream()
+    launches_per_step = 3 if mode == ibwd.IBWD_DK_ATOMIC else 8
+
+    def step(a, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ibwd.indexer_bwd_score_grad(I, a, idx, wl.S_k, 1.0, dk if mode == ibwd.IBWD_DK_ATOMIC else None, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ibwd.indexer_bwd_gemm(q, k, w, a, idx, dq, dw, dk, mode, wsb, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(attn[i])
+    st = ibwd.indexer_bwd_last_device_status(stream)
+    if st != ibwd.IBWD_OK:
+        raise SystemExit(f"device status after warm-up: {ibwd.status_string(st)}")
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                    if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    if td:
+        td.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(attn[args.warmup + i], evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if td:
+        td.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    sg_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    gm_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    st = ibwd.indexer_bwd_last_device_status(stream)
+    if st != ibwd.IBWD_OK:
+        raise SystemExit(f"device status after the timed region: {ibwd.status_string(st)}")
+    if td:
+        t = torch.tensor([total_ms], device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        total_ms = float(t.item())
+    del attn
+
+    flops = wl.flops()
+    ms_step = total_ms / args.steps
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    gm_avg = statistics.mean(gm_ms)
+    sg_avg = statistics.mean(sg_ms)
+    achieved = flops / (gm_avg * 1e-3) / 1e12
+    valid = float((x["idx"] >= 0).mean())
+    sg_bytes = 16.0 * wl.B * wl.S_q * wl.topk + (4.0 * wl.B * wl.S_k * wl.D if mode == ibwd.IBWD_DK_ATOMIC else 0.0)
+
+    # ---- end to end through the public API from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        h = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in
+             (("q", x["q"].view(np.int16)), ("k", x["k"].view(np.int16)), ("w", x["w"]), ("idx", x["idx"]),
+              ("attn", x["attn"]))}
+        h["I"] = I.cpu().pin_memory()
+        hq = torch.empty((B, S_q, H, D), dtype=torch.float32).pin_memory()
+        hw = torch.empty((B, S_q, H), dtype=torch.float32).pin_memory()
+        hk = torch.empty((B, wl.S_k, D), dtype=torch.float32).pin_memory()
+        dbuf = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in h.items()}
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = sum(t.numel() * t.element_size() for t in (hq, hw, hk))
+        ksteps = max(3, min(20, args.steps))
+
+        def e2e_step():
+            for n, t in h.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            ibwd.indexer_backward(dbuf["q"].view(torch.bfloat16), dbuf["k"].view(torch.bfloat16), dbuf["w"],
+                                  dbuf["I"], dbuf["attn"], dbuf["idx"], dk_mode=mode, workspace=wsb,
+                                  out=(dq, dw, dk), stream=stream)
+            hq.copy_(dq, non_blocking=True)
+            hw.copy_(dw, non_blocking=True)
+            hk.copy_(dk, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if td:
+            td.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ksteps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / ksteps
+        if td:
+            t = torch.tensor([e_ms], device=dev)
+            td.all_reduce(t, op=td.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": ws * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": ksteps}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, x, I.cpu().numpy(), args.cpu_seconds)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 tensor-core operands, fp32 accumulate (bf16 inputs)",
+        "data": "synthetic (seeded; index_score = forward logits of the seeded q, k, w)",
+        "config": {"workload": f"{wl.name}: B={wl.B} H={wl.H} D={wl.D} S_q={wl.S_q} S_k={wl.S_k} "
+                               f"topk={wl.topk}, causal top-k ids",
+                   "dk_mode": args.mode, "l2": "inputs larger than L2 (q alone is 134 MB); "
+                                               "a fresh attn_score copy per step",
+                   "valid_slot_fraction": round(valid, 4)},
+        "us_per_step": 1e3 * ms_step,
+        "kernels_us": {"score_grad": 1e3 * sg_avg, "gemm_stage": 1e3 * gm_avg},
+        "score_grad_gbs": sg_bytes / (sg_avg * 1e-3) / 1e9,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                     "note": f"gemm-stage call (fp16 copy of k + main kernel), nominal 6*S_q*topk*H*D FLOP; "
+                             f"peak = {pk['src']} dense bf16 burst (fp16 dense rate is the same)"},
+        "roofline_score_grad": {"bound": "hbm", "achieved": sg_bytes / (sg_avg * 1e-3) / 1e9,
+                                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                "frac": sg_bytes / (sg_avg * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,136 @@
+/*
+ * libindexer_bwd -- backward pass of the DeepSeek-sparse-attention lightning
+ * indexer on one GB300 (sm_103a).
+ *
+ * The forward being differentiated scores each selected key s of query row t
+ * as  I[t,s] = sum_h w[t,h] * relu(q[t,h,:] . k[s,:])  with one shared key
+ * head (cudnn-frontend #730 "optimize SM100 gradient kernels", benchmark
+ * harness fixture: q [B,S_q,H,D], k [B,S_k,D], w [B,S_q,H], top-k ids
+ * [B,S_q,topk]; #549 "restore range_constexpr in 8 kernel_gemm epilogue
+ * loops" names the two kernels kernel_score_grad and kernel_gemm).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are caller-owned, contiguous, row-major DEVICE memory on the
+ *    current CUDA device.  bf16 tensors are passed as uint16_t bit patterns.
+ *    Every pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All work is queued asynchronously on it; nothing blocks except
+ *    indexer_bwd_last_device_status.
+ *  - Every argument check (null pointers, alignment, device-resident memory,
+ *    shape limits, workspace size, an sm_103 device) happens before anything
+ *    is launched.  A failed check returns a nonzero ibwd_status and leaves all
+ *    memory untouched.  No exception or abort crosses this interface.
+ *  - A top-k id outside [0, S_k) is padding at every stage (-1 or any
+ *    positive out-of-range id); padding slots contribute nothing even when
+ *    index_score, attn_score or dI hold NaN there.  Ids are local to their
+ *    batch (id s of batch b addresses k[b, s]).
+ *  - Shape limits: B >= 1, S_q >= 1, S_k >= 1, topk >= 1, 1 <= H <= 64,
+ *    8 <= D <= 128 with D % 8 == 0, B*S_q*topk < 2^31.
+ *  - q and k entries must lie in fp16 range (|x| <= 65504): the gemm stage
+ *    feeds fp16 tensor-core operands converted exactly from bf16.
+ *  - The library allocates no memory on the compute path.  The deterministic
+ *    mode uses the caller's workspace.  One 4-byte device status word per
+ *    device is allocated on first use and kept until process exit.
+ */
+#ifndef INDEXER_BWD_H
+#define INDEXER_BWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define IBWD_API __attribute__((visibility("default")))
+#else
+#define IBWD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IBWD_OK = 0,
+  IBWD_ERR_INVALID_ARG = 1, /* null/misaligned/host pointer, bad shape */
+  IBWD_ERR_UNSUPPORTED = 2, /* not an sm_103 device, or a shape beyond the limits */
+  IBWD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  IBWD_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  IBWD_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (device status) */
+  IBWD_ERR_BAD_INDEX = 6    /* a device-side bounds check failed (device status) */
+} ibwd_status;
+
+typedef enum {
+  IBWD_DK_ATOMIC = 0,       /* dK += with fp32 red.global.add (run-to-run jitter ~1e-7) */
+  IBWD_DK_DETERMINISTIC = 1 /* dK = fixed-order segment sums by key (bitwise reproducible) */
+} ibwd_dk_mode;
+
+/*
+ * Kernel 1, score-grad (#730 walkthrough: kernel 1 writes the gradient signal
+ * over attn_score and leaves index_score intact; the dK zeroing is fused into
+ * the same launch).  For each row t over its valid slots j:
+ *   p_j = softmax_j(index_score[t,:]),  ahat_j = attn_score[t,j] / sum_valid attn_score,
+ *   dI[t,j] = grad_scale * (p_j - ahat_j) / S_q,   dI = 0 on padding slots
+ * (the gradient of grad_scale * mean_t KL(ahat_t || p_t); ahat = 0 if the row's
+ * target sums to 0; a row without valid slots is all zero).
+ *   index_score  fp32 [B,S_q,topk], read only
+ *   attn_score   fp32 [B,S_q,topk], read, then overwritten with dI
+ *   topk_idx     int32 [B,S_q,topk]
+ *   dk_to_zero   optional fp32 [B,S_k,D] set to 0 by the same launch (NULL: skipped)
+ */
+IBWD_API int indexer_bwd_score_grad(const float* index_score, float* attn_score, const int32_t* topk_idx,
+                           int B, int S_q, int S_k, int topk, float grad_scale, float* dk_to_zero,
+                           int D, void* stream);
+
+/* Bytes of device workspace indexer_bwd_gemm needs (always > 0: it holds an
+ * fp16 copy of k; the deterministic mode adds the per-slot dK rows, 4*D bytes
+ * per slot, and the key sort). */
+IBWD_API size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk,
+                                       int dk_mode);
+
+/*
+ * Kernel 2, gemm stage (#730 harness, ref_grads: the fp64 definition of the
+ * gemm_only semantics), for each valid slot (t, j), s = topk_idx[t,j]:
+ *   z[h] = q[t,h,:] . k[s,:];   dW[t,h] = sum_j dI[t,j] relu(z[h]);
+ *   dz[h] = dI[t,j] w[t,h] [z[h] > 0];   dQ[t,h,:] = sum_j dz[h] k[s,:];
+ *   dK[s,:] += sum_h dz[h] q[t,h,:]
+ *   q      bf16 [B,S_q,H,D];  k bf16 [B,S_k,D];  w fp32 [B,S_q,H]
+ *   dI     fp32 [B,S_q,topk]  (the attn_score buffer after kernel 1)
+ *   dq     fp32 [B,S_q,H,D], fully written;  dw fp32 [B,S_q,H], fully written
+ *   dk     fp32 [B,S_k,D]: IBWD_DK_ATOMIC accumulates into it (zero it first,
+ *          e.g. through indexer_bwd_score_grad's dk_to_zero);
+ *          IBWD_DK_DETERMINISTIC overwrites it.
+ *   workspace  device memory of at least indexer_bwd_gemm_workspace_size bytes
+ * dq and dw are bitwise reproducible run to run in both modes.
+ */
+IBWD_API int indexer_bwd_gemm(const uint16_t* q, const uint16_t* k, const float* w, const float* dI,
+                     const int32_t* topk_idx, float* dq, float* dw, float* dk, int B, int S_q,
+                     int S_k, int H, int D, int topk, int dk_mode, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * Dense variant (#549 tests: test_DSA_dense_indexer_backward; #730 touches
+ * dense_indexer_backward_sm100.py): every causal key s <= t is selected,
+ * S_q = S_k = S, and the scores are [B,S,S] (entry [t,s] for key s).  The
+ * formulas are those above with the valid set {s <= t}; dI above the
+ * diagonal is written as 0.
+ */
+IBWD_API int indexer_bwd_dense_score_grad(const float* index_score, float* attn_score, int B, int S,
+                                 float grad_scale, float* dk_to_zero, int D, void* stream);
+IBWD_API size_t indexer_bwd_dense_gemm_workspace_size(int B, int S, int H, int D, int dk_mode);
+IBWD_API int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const float* w, const float* dI,
+                           float* dq, float* dw, float* dk, int B, int S, int H, int D,
+                           int dk_mode, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronizes `stream`, then reads and clears this device's status word:
+ * IBWD_ERR_TIMEOUT if a kernel's bounded wait expired, IBWD_ERR_BAD_INDEX if a
+ * device bounds check failed, IBWD_ERR_CUDA if the stream reports an error,
+ * IBWD_OK otherwise. */
+IBWD_API int indexer_bwd_last_device_status(void* stream);
+
+/* Static English description of a status code. */
+IBWD_API const char* indexer_bwd_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INDEXER_BWD_H */

@@ -1,0 +1,211 @@
+// C-ABI of libindexer_bwd.so: argument checks, workspace sizing, launches.
+// The declarations, with their contracts and sources, are in indexer_bwd.h.
+#include <mutex>
+
+#include "indexer_bwd.h"
+#include "internal.h"
+
+namespace {
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  unsigned* status = nullptr;  // one device word, allocated once
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+// Current device's info; allocates its status word on first use.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return IBWD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return IBWD_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    if (d.supported) {
+      if (cudaMalloc(&d.status, sizeof(unsigned)) != cudaSuccess) return IBWD_ERR_CUDA;
+      if (cudaMemset(d.status, 0, sizeof(unsigned)) != cudaSuccess) return IBWD_ERR_CUDA;
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return IBWD_ERR_UNSUPPORTED;
+  *out = &d;
+  return IBWD_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Non-null, 16-byte aligned and addressable by the device.
+bool dev_ptr_ok(const void* p) {
+  if (!aligned16(p)) return false;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+bool shape_ok(int B, int S_q, int S_k, int H, int D, int L) {
+  if (B < 1 || S_q < 1 || S_k < 1 || L < 1) return false;
+  if (H < 1 || H > ibwd::kHP) return false;
+  if (D < 8 || D > ibwd::kDP || D % 8 != 0) return false;
+  const long long slots = (long long)B * S_q * L;
+  if (slots >= (1LL << 31)) return false;
+  return true;
+}
+
+// dense_or_idx: the sparse variant requires topk_idx (the dense one passes NULL).
+int score_grad_common(const float* I, float* A, const int32_t* idx, bool dense_or_idx, int B, int S_q, int S_k,
+                      int L, float grad_scale, float* dk, int D, void* stream) {
+  if (B < 1 || S_q < 1 || S_k < 1 || L < 1) return IBWD_ERR_INVALID_ARG;
+  if ((long long)B * S_q * L >= (1LL << 31)) return IBWD_ERR_UNSUPPORTED;
+  if (dk && (D < 1 || (long long)B * S_k * D >= (1LL << 40))) return IBWD_ERR_INVALID_ARG;
+  if (!aligned16(I) || !aligned16(A) || (dense_or_idx && !aligned16(idx)) || (dk && !aligned16(dk)))
+    return IBWD_ERR_INVALID_ARG;
+  DeviceInfo* dv = nullptr;
+  int rc = device_info(&dv);
+  if (rc) return rc;
+  if (!dev_ptr_ok(I) || !dev_ptr_ok(A)) return IBWD_ERR_INVALID_ARG;
+  if (idx && !dev_ptr_ok(idx)) return IBWD_ERR_INVALID_ARG;
+  if (dk && !dev_ptr_ok(dk)) return IBWD_ERR_INVALID_ARG;
+  if (static_cast<const void*>(I) == static_cast<const void*>(A)) return IBWD_ERR_INVALID_ARG;
+  ibwd::ScoreGradArgs a{};
+  a.index_score = I;
+  a.attn_score = A;
+  a.idx = idx;
+  a.rows = (long long)B * S_q;
+  a.L = L;
+  a.S_q = S_q;
+  a.S_k = S_k;
+  a.scale = grad_scale / (float)S_q;
+  a.dk_zero = dk;
+  a.dk_numel = dk ? (long long)B * S_k * D : 0;
+  cudaError_t e = ibwd::launch_score_grad(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
+}
+
+size_t workspace_common(int B, int S_q, int S_k, int H, int D, int L, int mode) {
+  if (!shape_ok(B, S_q, S_k, H, D, L) || (mode != IBWD_DK_ATOMIC && mode != IBWD_DK_DETERMINISTIC)) return 0;
+  return ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC).total;
+}
+
+// need_idx: the sparse variant requires topk_idx (the dense one passes NULL).
+int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const float* dI, const int32_t* idx,
+                bool need_idx, float* dq, float* dw, float* dk, int B, int S_q, int S_k, int H, int D, int L,
+                int mode, void* ws, size_t ws_bytes, void* stream) {
+  if (mode != IBWD_DK_ATOMIC && mode != IBWD_DK_DETERMINISTIC) return IBWD_ERR_INVALID_ARG;
+  if (B < 1 || S_q < 1 || S_k < 1 || L < 1 || H < 1 || D < 1) return IBWD_ERR_INVALID_ARG;
+  if (!shape_ok(B, S_q, S_k, H, D, L)) return IBWD_ERR_UNSUPPORTED;
+  // the sort keeps one counter per key of a batch in shared memory
+  if (mode == IBWD_DK_DETERMINISTIC && S_k > 49152) return IBWD_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, w, dI, dq, dw, dk};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return IBWD_ERR_INVALID_ARG;
+  if (need_idx && !aligned16(idx)) return IBWD_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return IBWD_ERR_WORKSPACE;
+  DeviceInfo* dv = nullptr;
+  int rc = device_info(&dv);
+  if (rc) return rc;
+  for (const void* p : ptrs)
+    if (!dev_ptr_ok(p)) return IBWD_ERR_INVALID_ARG;
+  if (idx && !dev_ptr_ok(idx)) return IBWD_ERR_INVALID_ARG;
+  const size_t need = ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC).total;
+  if (!ws || ws_bytes < need || !dev_ptr_ok(ws)) return IBWD_ERR_WORKSPACE;
+  ibwd::GemmArgs a{};
+  a.q = q;
+  a.k = k;
+  a.w = w;
+  a.dI = dI;
+  a.idx = idx;
+  a.dq = dq;
+  a.dw = dw;
+  a.dk = dk;
+  a.B = B;
+  a.S_q = S_q;
+  a.S_k = S_k;
+  a.H = H;
+  a.D = D;
+  a.L = L;
+  a.deterministic = mode == IBWD_DK_DETERMINISTIC;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  a.status = dv->status;
+  a.num_sms = dv->num_sms;
+  cudaError_t e = ibwd::launch_gemm(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int indexer_bwd_score_grad(const float* index_score, float* attn_score, const int32_t* topk_idx, int B,
+                           int S_q, int S_k, int topk, float grad_scale, float* dk_to_zero, int D,
+                           void* stream) {
+  return score_grad_common(index_score, attn_score, topk_idx, true, B, S_q, S_k, topk, grad_scale, dk_to_zero,
+                           D, stream);
+}
+
+size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk, int dk_mode) {
+  return workspace_common(B, S_q, S_k, H, D, topk, dk_mode);
+}
+
+int indexer_bwd_gemm(const uint16_t* q, const uint16_t* k, const float* w, const float* dI,
+                     const int32_t* topk_idx, float* dq, float* dw, float* dk, int B, int S_q, int S_k, int H,
+                     int D, int topk, int dk_mode, void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_common(q, k, w, dI, topk_idx, true, dq, dw, dk, B, S_q, S_k, H, D, topk, dk_mode, workspace,
+                     workspace_bytes, stream);
+}
+
+int indexer_bwd_dense_score_grad(const float* index_score, float* attn_score, int B, int S, float grad_scale,
+                                 float* dk_to_zero, int D, void* stream) {
+  return score_grad_common(index_score, attn_score, nullptr, false, B, S, S, S, grad_scale, dk_to_zero, D, stream);
+}
+
+size_t indexer_bwd_dense_gemm_workspace_size(int B, int S, int H, int D, int dk_mode) {
+  return workspace_common(B, S, S, H, D, S, dk_mode);
+}
+
+int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const float* w, const float* dI, float* dq,
+                           float* dw, float* dk, int B, int S, int H, int D, int dk_mode, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return gemm_common(q, k, w, dI, nullptr, false, dq, dw, dk, B, S, S, H, D, S, dk_mode, workspace,
+                     workspace_bytes, stream);
+}
+
+int indexer_bwd_last_device_status(void* stream) {
+  DeviceInfo* dv = nullptr;
+  int rc = device_info(&dv);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return IBWD_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dv->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return IBWD_ERR_CUDA;
+  if (word && cudaMemset(dv->status, 0, sizeof word) != cudaSuccess) return IBWD_ERR_CUDA;
+  if (word & 1u) return IBWD_ERR_TIMEOUT;
+  if (word & 2u) return IBWD_ERR_BAD_INDEX;
+  return IBWD_OK;
+}
+
+const char* indexer_bwd_status_string(int status) {
+  switch (status) {
+    case IBWD_OK: return "ok";
+    case IBWD_ERR_INVALID_ARG: return "invalid argument (null, misaligned or host pointer, or bad shape)";
+    case IBWD_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case IBWD_ERR_WORKSPACE: return "workspace missing or too small";
+    case IBWD_ERR_CUDA: return "CUDA runtime error";
+    case IBWD_ERR_TIMEOUT: return "a kernel wait timed out";
+    case IBWD_ERR_BAD_INDEX: return "a device bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

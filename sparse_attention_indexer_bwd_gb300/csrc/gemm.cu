@@ -1,0 +1,715 @@
+// Gemm stage of the lightning-indexer backward on sm_103a (kernel 2).
+//
+// Definition (cudnn-frontend #730 "optimize SM100 gradient kernels",
+// benchmark-harness comment, ref_grads; #549 names the kernel kernel_gemm and
+// its outputs d_index_q, d_weights, d_index_k), per query row t and selected
+// key s = idx[t,j] (padding ids, i.e. any id outside [0, S_k), are skipped):
+//   z[s,h]  = q[t,h,:] . k[s,:]                       (forward recompute)
+//   dW[t,h] = sum_s dI[t,s] relu(z[s,h])
+//   dz[s,h] = dI[t,s] w[t,h] [z[s,h] > 0]
+//   dQ[t,h] = sum_s dz[s,h] k[s,:]
+//   dK[s]  += sum_h dz[s,h] q[t,h,:]
+//
+// Design: one persistent CTA per SM walks its query rows (a low-discrepancy
+// permutation of all rows, so concurrently running rows are far apart and
+// local-window key sets rarely collide).  Each row's valid slots are
+// compacted into tiles of 128 keys, and the keys are the M = 128 dimension of
+// every tensor-core MMA:
+//   MMA1  Z^T[128 s, 64 h]   = Ksel[128 s, 128 d] . Q^T          (TMEM, fp32)
+//   MMA2  dK [128 s, 128 d]  = dz[128 s, 64 h] . Q[64 h, 128 d]  (TMEM, fp32)
+//   MMA3  dQ^T[128 d, 64 h] += Ksel^T[128 d, 128 s] . dz[128 s, 64 h]
+// Operands are fp16 in 128-byte-swizzled shared memory: k is converted once to
+// an fp16 copy (bf16 -> fp16 is exact in fp16 range), q is converted per row,
+// and dz is scaled by a per-row power of two 2^c so that it stays in the fp16
+// normal range (bf16 dz would cost ~1.6e-3 relative RMS, over the dK budget).
+// The scale is undone exactly in the fp32 epilogues.
+//
+// Warp roles (16 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
+//   0     producer: row scan (valid count, max|dI|, scale), compaction into
+//         tile metadata, cp.async gather of the selected fp16 k rows
+//   1     MMA issuer (one thread) and TMEM owner (512 columns)
+//   2-3   Q loader: q[t] bf16 -> fp16 swizzled tile, w[t] -> shared
+//   4-7   dz group for heads 0-31, 8-11 dz group for heads 32-63: Z from
+//         TMEM -> dW partial sums in registers, dz -> fp16 shared tile; at row
+//         end the dW reduction; one row later the dQ epilogue (TMEM -> fp32)
+//   12-15 dK group: dK tile from TMEM -> fp32 red.global.add.v4 into dk, or
+//         plain stores into the per-slot workspace in deterministic mode
+// Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
+// all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ibwd {
+namespace {
+
+constexpr int KST = 4;  // K-tile stages
+constexpr int MST = 4;  // tile-metadata ring
+constexpr int NTHREADS = 512;
+constexpr int W_PROD = 0, W_MMA = 1, W_Q0 = 2, W_DZ0 = 4, W_DK0 = 12;
+constexpr int NQT = 64;    // Q-loader threads
+constexpr int NDZT = 256;  // dz threads (two groups of 128)
+
+constexpr uint32_t KTILE_BYTES = kBM * kDP * 2;   // 32 KB
+constexpr uint32_t KHALF_BYTES = kBM * 64 * 2;    // one 64-column half of a K tile
+constexpr uint32_t QTILE_BYTES = kHP * kDP * 2;   // 16 KB
+constexpr uint32_t QHALF_BYTES = kHP * 64 * 2;
+constexpr uint32_t DZTILE_BYTES = kBM * kHP * 2;  // 16 KB
+
+// TMEM columns: Z double buffer, dK double buffer, dQ double buffer.
+constexpr uint32_t TM_Z = 0, TM_DK = 128, TM_DQ = 384, TM_COLS = 512;
+
+struct TileMeta {
+  int key[kBM];    // selected key (row of k within the batch)
+  int slot[kBM];   // slot j within the query row
+  float dis[kBM];  // dI[t, j] * 2^c
+  int r, count, c, flags;
+};
+enum { F_FIRST = 1, F_LAST = 2, F_END = 4 };
+
+struct Bars {
+  uint64_t kfull[KST], kempty[KST];
+  uint64_t mfull[MST], mempty[MST];
+  uint64_t qfull[2];
+  uint64_t zfull[2], zempty[2];
+  uint64_t dzfull[2], dzempty[2];
+  uint64_t dkfull[2], dkempty[2];
+  uint64_t dqfull[2], dqempty[2];
+  uint64_t dwred[2];
+  uint64_t drain;
+};
+
+constexpr uint32_t OFF_K = 0;
+constexpr uint32_t OFF_Q = OFF_K + KST * KTILE_BYTES;
+constexpr uint32_t OFF_DZ = OFF_Q + 2 * QTILE_BYTES;
+constexpr uint32_t OFF_META = OFF_DZ + 2 * DZTILE_BYTES;
+constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
+constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
+constexpr uint32_t OFF_BARS = OFF_RED + 2 * 4 * kHP * 4;  // [2][4 warps][64 heads]
+constexpr uint32_t OFF_MISC = OFF_BARS + sizeof(Bars);
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+static_assert(OFF_BARS % 8 == 0, "barrier alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+struct KParams {
+  const uint16_t* q;
+  const __half* k16;
+  const float* w;
+  const float* dI;
+  const int32_t* idx;
+  float* dq;
+  float* dw;
+  float* dk;
+  float* u;  // deterministic per-slot rows, or nullptr
+  unsigned* status;
+  long long rows;
+  unsigned long long perm_mul;
+  unsigned long long wait_ns;
+  int S_q, S_k, H, D, L, dense;
+};
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ long long row_of(long long u, const KParams& p) {
+  return (long long)(((unsigned long long)u * p.perm_mul) % (unsigned long long)p.rows);
+}
+
+struct Ctx {
+  uint32_t sbase;
+  uint8_t* smem;
+  TileMeta* meta;
+  float* w_s;
+  float* red_s;
+  Bars* bars;
+  volatile int* abort;
+  uint32_t tmem;
+  long long nq;
+};
+
+#define WAIT(bar, par) mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns)
+
+// ------------------------------------------------------------ Q loader ----
+__device__ void q_role(const KParams& p, const Ctx& cx) {
+  const int tid = threadIdx.x - W_Q0 * 32;  // 0..63
+  for (long long i = 0; i < cx.nq; ++i) {
+    const int qb = (int)(i & 1);
+    // buffer qb was last used by row i-2: all its MMAs and dz reads are done
+    // once that row's dQ accumulator is complete
+    if (i >= 2 && !WAIT(&cx.bars->dqfull[qb], (uint32_t)(((i - 2) >> 1) & 1))) return;
+    const long long r = row_of(blockIdx.x + i * gridDim.x, p);
+    const uint16_t* qr = p.q + r * p.H * p.D;
+    const uint32_t qs = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+    uint4 v[16];
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int x = tid + it * NQT;  // 16-byte chunk: head h, column chunk ch
+      const int h = x >> 4, ch = x & 15;
+      v[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (h < p.H && ch * 8 < p.D) v[it] = __ldg(reinterpret_cast<const uint4*>(qr + h * p.D + ch * 8));
+    }
+#pragma unroll
+    for (int it = 0; it < 16; ++it) {
+      const int x = tid + it * NQT;
+      const int h = x >> 4, ch = x & 15;
+      const uint32_t dst = qs + (ch >> 3) * QHALF_BYTES + h * 128 + (((ch & 7) ^ (h & 7)) << 4);
+      st_shared_v4(dst, bf16x2_to_half2(v[it].x), bf16x2_to_half2(v[it].y),
+                   bf16x2_to_half2(v[it].z), bf16x2_to_half2(v[it].w));
+    }
+    cx.w_s[qb * kHP + tid] = tid < p.H ? __ldg(p.w + r * p.H + tid) : 0.f;
+    fence_proxy_async_smem();
+    mbar_arrive(&cx.bars->qfull[qb]);
+  }
+}
+
+// ------------------------------------------------------------- producer ---
+__device__ void producer_role(const KParams& p, const Ctx& cx) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int g = 0;
+  bool pending = false;
+  for (long long i = 0; i < cx.nq; ++i) {
+    const long long r = row_of(blockIdx.x + i * gridDim.x, p);
+    const int b = (int)(r / p.S_q);
+    const int t = (int)(r % p.S_q);
+    const int32_t* idxr = p.dense ? nullptr : p.idx + r * p.L;
+    const float* dIr = p.dI + r * p.L;
+    const int Lr = p.dense ? min(p.L, t + 1) : p.L;
+    // pass 1: number of valid slots and max |dI| over them
+    int nv = 0;
+    float mx = 0.f;
+    for (int j0 = 0; j0 < Lr; j0 += 32) {
+      const int j = j0 + lane;
+      bool v = false;
+      if (j < Lr) v = p.dense ? true : ((unsigned)__ldg(idxr + j) < (unsigned)p.S_k);
+      if (v) mx = fmaxf(mx, fabsf(__ldg(dIr + j)));
+      nv += __popc(__ballot_sync(0xffffffffu, v));
+    }
+    mx = warp_max(mx);
+    float wm = 0.f;
+    for (int h = lane; h < p.H; h += 32) wm = fmaxf(wm, fabsf(__ldg(p.w + r * p.H + h)));
+    wm = warp_max(wm);
+    // per-row scale 2^c: max |dI w| 2^c lies in [2^13, 2^14), inside fp16 range
+    const float m = mx * wm;
+    int c = 0;
+    if (m > 0.f && m <= 3.0e38f) {
+      int e;
+      frexpf(m, &e);
+      c = max(-120, min(120, 14 - e));
+    }
+    const float sc = pow2f(c);
+    const int ntiles = max(1, (nv + kBM - 1) / kBM);
+    // pass 2: compact the valid slots into tiles of 128 and gather their keys
+    int jc = 0, skip = 0;
+    for (int tt = 0; tt < ntiles; ++tt, ++g) {
+      const int ms = g % MST;
+      if (!WAIT(&cx.bars->mempty[ms], (uint32_t)(((g / MST) & 1) ^ 1))) goto done;
+      TileMeta& M = cx.meta[ms];
+      int fill = 0;
+      while (fill < kBM && jc < Lr) {
+        const int j = jc + lane;
+        bool v = false;
+        int s = 0;
+        if (j < Lr) {
+          s = p.dense ? j : __ldg(idxr + j);
+          v = p.dense ? true : ((unsigned)s < (unsigned)p.S_k);
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, v);
+        const int tot = __popc(mask);
+        const int rank = __popc(mask & lt_mask);
+        const int room = kBM - fill;
+        if (v && rank >= skip && rank < skip + room) {
+          const int pos = fill + rank - skip;
+          M.key[pos] = s;
+          M.slot[pos] = j;
+          M.dis[pos] = __ldg(dIr + j) * sc;
+        }
+        const int taken = min(tot - skip, room);
+        fill += taken;
+        if (skip + taken < tot) {
+          skip += taken;
+        } else {
+          skip = 0;
+          jc += 32;
+        }
+      }
+      if (lane == 0) {
+        M.r = (int)r;
+        M.count = fill;
+        M.c = c;
+        M.flags = (tt == 0 ? F_FIRST : 0) | (tt == ntiles - 1 ? F_LAST : 0) |
+                  ((tt == ntiles - 1 && i == cx.nq - 1) ? F_END : 0);
+      }
+      __syncwarp();
+      const int st = g % KST;
+      if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) goto done;
+      const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES;
+      const __half* kb = p.k16 + (long long)b * p.S_k * kDP;
+#pragma unroll 4
+      for (int it = 0; it < kBM / 2; ++it) {
+        const int row = it * 2 + (lane >> 4);
+        const int ch = lane & 15;
+        const bool ok = row < fill;
+        const int key = ok ? M.key[row] : 0;
+        const uint32_t dst = kbase + (ch >> 3) * KHALF_BYTES + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+        cp_async16(dst, kb + (long long)key * kDP + ch * 8, ok ? 16u : 0u);
+      }
+      cp_async_commit();
+      mbar_arrive(&cx.bars->mfull[ms]);
+      if (pending) {
+        // the previous tile's copies have landed: publish them to the tensor core
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&cx.bars->kfull[(g - 1) % KST]);
+      }
+      pending = true;
+    }
+  }
+done:
+  cp_async_wait_all();
+  if (pending) {
+    fence_proxy_async_smem();
+    mbar_arrive(&cx.bars->kfull[(g - 1) % KST]);
+  }
+}
+
+// ------------------------------------------------------------------ MMA ---
+constexpr uint32_t ID_Z = idesc_f16_f32(128, 64, 0, 0);    // Z^T = K . Q^T
+constexpr uint32_t ID_DK = idesc_f16_f32(128, 128, 0, 1);  // dK = dz . Q   (Q as MN-major B)
+constexpr uint32_t ID_DQ = idesc_f16_f32(128, 64, 1, 1);   // dQ^T = K^T . dz (both MN-major)
+
+__device__ __forceinline__ void mma_z(const Ctx& cx, int g, int qb) {
+  const uint32_t ka = cx.sbase + OFF_K + (g % KST) * KTILE_BYTES;
+  const uint32_t qa = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+  const uint32_t d = cx.tmem + TM_Z + (g & 1) * 64;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // K = D = 128 in steps of 16
+    const uint64_t ad = sw128_desc(ka + (k >> 2) * KHALF_BYTES + (k & 3) * 32, 16, 1024);
+    const uint64_t bd = sw128_desc(qa + (k >> 2) * QHALF_BYTES + (k & 3) * 32, 16, 1024);
+    umma_f16(d, ad, bd, ID_Z, k > 0);
+  }
+}
+
+__device__ __forceinline__ void mma_dk(const Ctx& cx, int g, int qb) {
+  const uint32_t za = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES;
+  const uint32_t qa = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+  const uint32_t d = cx.tmem + TM_DK + (g & 1) * 128;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // K = H = 64 in steps of 16
+    const uint64_t ad = sw128_desc(za + k * 32, 16, 1024);
+    const uint64_t bd = sw128_desc(qa + k * 2048, QHALF_BYTES, 1024);
+    umma_f16(d, ad, bd, ID_DK, k > 0);
+  }
+}
+
+__device__ __forceinline__ void mma_dq(const Ctx& cx, int g, int qd, bool first) {
+  const uint32_t ka = cx.sbase + OFF_K + (g % KST) * KTILE_BYTES;
+  const uint32_t za = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES;
+  const uint32_t d = cx.tmem + TM_DQ + qd * 64;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {  // K = 128 keys in steps of 16
+    const uint64_t ad = sw128_desc(ka + k * 2048, KHALF_BYTES, 1024);
+    const uint64_t bd = sw128_desc(za + k * 2048, DZTILE_BYTES, 1024);
+    umma_f16(d, ad, bd, ID_DQ, (first && k == 0) ? 0u : 1u);
+  }
+}
+
+__device__ void mma_role(const KParams& p, const Ctx& cx) {
+  Bars* B = cx.bars;
+  int g = 0;
+  long long iq = 0;
+  if (!WAIT(&B->mfull[0], 0)) goto drain;
+  {
+    int flags = cx.meta[0].flags;
+    if (!WAIT(&B->qfull[0], 0) || !WAIT(&B->kfull[0], 0)) goto drain;
+    tc_fence_after();
+    mma_z(cx, 0, 0);
+    umma_commit(&B->zfull[0]);
+    for (;;) {
+      int nflags = 0;
+      long long niq = iq;
+      if (!(flags & F_END)) {
+        // look ahead: Z of tile g+1 overlaps the dz work of tile g
+        const int g1 = g + 1;
+        if (!WAIT(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) goto drain;
+        nflags = cx.meta[g1 % MST].flags;
+        if (nflags & F_FIRST) {
+          niq = iq + 1;
+          if (!WAIT(&B->qfull[niq & 1], (uint32_t)((niq >> 1) & 1))) goto drain;
+        }
+        if (!WAIT(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1))) goto drain;
+        if (!WAIT(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1))) goto drain;
+        tc_fence_after();
+        mma_z(cx, g1, (int)(niq & 1));
+        umma_commit(&B->zfull[g1 & 1]);
+      }
+      if (!WAIT(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
+      if (!WAIT(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
+      if ((flags & F_FIRST) && !WAIT(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
+      tc_fence_after();
+      mma_dk(cx, g, (int)(iq & 1));
+      umma_commit(&B->dkfull[g & 1]);
+      mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
+      umma_commit(&B->kempty[g % KST]);
+      umma_commit(&B->dzempty[g & 1]);
+      if (flags & F_LAST) umma_commit(&B->dqfull[iq & 1]);
+      if (flags & F_END) break;
+      ++g;
+      flags = nflags;
+      iq = niq;
+    }
+  }
+drain:
+  // every MMA issued so far completes before TMEM can be released; this wait
+  // ignores the abort flag (it must not return early) but is still bounded
+  umma_commit(&B->drain);
+  {
+    volatile int never = 0;
+    mbar_wait(&B->drain, 0, &never, p.status, p.wait_ns);
+  }
+}
+
+// ------------------------------------------------------------ dz group ----
+// Group `hg` (0 or 1) owns heads 32*hg .. 32*hg+31 of every tile row.
+__device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int hg, long long iq, int r,
+                                            int c) {
+  const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return;
+  tc_fence_after();
+  const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + hg * 32;
+  float v[32];
+  tmem_ld32(ta, v);
+  tmem_wait_ld();
+  tc_fence_before();
+  mbar_arrive(&cx.bars->dqempty[iq & 1]);
+  const float sc = pow2f(-c);
+  const int d = qw * 32 + lane;  // TMEM lane = column of dQ
+  if (d < p.D) {
+    float* dst = p.dq + (long long)r * p.H * p.D + d;
+#pragma unroll
+    for (int h = 0; h < 32; ++h)
+      if (hg * 32 + h < p.H) dst[(long long)(hg * 32 + h) * p.D] = v[h] * sc;
+  }
+}
+
+__device__ void dz_role(const KParams& p, const Ctx& cx) {
+  const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int s = qw * 32 + lane;  // tile row = TMEM lane
+  const int tdz = threadIdx.x - W_DZ0 * 32;  // 0..255
+  const int hg = tdz >> 7;                    // head group
+  float acc[32];
+#pragma unroll
+  for (int h = 0; h < 32; ++h) acc[h] = 0.f;
+  long long iq = -1, ep_iq = 0;
+  int ep_r = -1, ep_c = 0;
+  bool ok = true;
+  for (int g = 0;; ++g) {
+    const int ms = g % MST;
+    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) { ok = false; break; }
+    const TileMeta& M = cx.meta[ms];
+    const int flags = M.flags, count = M.count, c = M.c, r = M.r;
+    if (flags & F_FIRST) {
+      ++iq;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) acc[h] = 0.f;
+      if (!WAIT(&cx.bars->qfull[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
+    }
+    const float dis = s < count ? M.dis[s] : 0.f;
+    const float* wq = cx.w_s + (iq & 1) * kHP + hg * 32;
+    if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
+    if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
+    tc_fence_after();
+    const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
+    const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
+    float z[32];
+    tmem_ld32(za, z);
+    tmem_wait_ld();
+    tc_fence_before();
+    mbar_arrive(&cx.bars->zempty[g & 1]);
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h0 = c8 * 8 + e * 2;
+        const float z0 = z[h0], z1 = z[h0 + 1];
+        acc[h0] = fmaf(dis, fmaxf(z0, 0.f), acc[h0]);
+        acc[h0 + 1] = fmaf(dis, fmaxf(z1, 0.f), acc[h0 + 1]);
+        const float d0 = z0 > 0.f ? dis * wq[h0] : 0.f;
+        const float d1 = z1 > 0.f ? dis * wq[h0 + 1] : 0.f;
+        pk[e] = pack_half2(d0, d1);
+      }
+      const int chunk = hg * 4 + c8;  // 16-byte chunk of the 128-byte dz row
+      st_shared_v4(dzrow + ((chunk ^ (s & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&cx.bars->dzfull[g & 1]);
+    if ((flags & F_FIRST) && ep_r >= 0) {
+      dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
+      ep_r = -1;
+    }
+    if (flags & F_LAST) {
+      // dW[t,h] = 2^-c sum over the 128 tile rows of acc[h]: a butterfly
+      // leaves head 32*hg + lane summed over the warp, then the four warps'
+      // partials are added in a fixed order
+#pragma unroll
+      for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step, n = 16 >> step;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < n; ++k) {
+          const float send = upper ? acc[k] : acc[k + n];
+          const float keep = upper ? acc[k + n] : acc[k];
+          acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      float* red = cx.red_s + (iq & 1) * 4 * kHP;
+      red[qw * kHP + hg * 32 + lane] = acc[0];
+      mbar_arrive(&cx.bars->dwred[iq & 1]);
+      if (tdz < kHP) {
+        if (!WAIT(&cx.bars->dwred[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
+        if (tdz < p.H)
+          p.dw[(long long)r * p.H + tdz] =
+              (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
+      }
+      ep_r = r;
+      ep_c = c;
+      ep_iq = iq;
+    }
+    if (flags & F_END) break;
+  }
+  if (ok && ep_r >= 0) dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
+}
+
+// ------------------------------------------------------------ dK group ----
+__device__ void dk_role(const KParams& p, const Ctx& cx) {
+  const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int s = qw * 32 + lane;
+  for (int g = 0;; ++g) {
+    const int ms = g % MST;
+    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
+    const TileMeta& M = cx.meta[ms];
+    const int flags = M.flags, c = M.c, r = M.r;
+    const bool ok = s < M.count;
+    const int key = ok ? M.key[s] : 0;
+    const int slot = ok ? M.slot[s] : 0;
+    if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
+    tc_fence_after();
+    const float sc = pow2f(-c);
+    const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK + (uint32_t)(g & 1) * 128;
+    float* dst = p.u ? p.u + ((long long)r * p.L + slot) * p.D
+                     : p.dk + ((long long)(r / p.S_q) * p.S_k + key) * p.D;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      if (ch * 32 >= p.D) break;
+      float v[32];
+      tmem_ld32(ta + ch * 32, v);
+      tmem_wait_ld();
+      if (ok) {
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int d = ch * 32 + q4 * 4;
+          if (d < p.D) {
+            const float a0 = v[q4 * 4] * sc, a1 = v[q4 * 4 + 1] * sc;
+            const float a2 = v[q4 * 4 + 2] * sc, a3 = v[q4 * 4 + 3] * sc;
+            if (p.u)
+              *reinterpret_cast<float4*>(dst + d) = make_float4(a0, a1, a2, a3);
+            else
+              red_add_v4(dst + d, a0, a1, a2, a3);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&cx.bars->dkempty[g & 1]);
+    mbar_arrive(&cx.bars->mempty[ms]);
+    if (flags & F_END) return;
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctx cx;
+  cx.smem = smem;
+  cx.sbase = smem_u32(smem);
+  cx.meta = reinterpret_cast<TileMeta*>(smem + OFF_META);
+  cx.w_s = reinterpret_cast<float*>(smem + OFF_W);
+  cx.red_s = reinterpret_cast<float*>(smem + OFF_RED);
+  cx.bars = reinterpret_cast<Bars*>(smem + OFF_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  cx.abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  cx.nq = (p.rows - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    Bars* B = cx.bars;
+    for (int i = 0; i < KST; ++i) { mbar_init(&B->kfull[i], 32); mbar_init(&B->kempty[i], 1); }
+    for (int i = 0; i < MST; ++i) { mbar_init(&B->mfull[i], 32); mbar_init(&B->mempty[i], 128); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->qfull[i], NQT);
+      mbar_init(&B->zfull[i], 1);
+      mbar_init(&B->zempty[i], NDZT);
+      mbar_init(&B->dzfull[i], NDZT);
+      mbar_init(&B->dzempty[i], 1);
+      mbar_init(&B->dkfull[i], 1);
+      mbar_init(&B->dkempty[i], 128);
+      mbar_init(&B->dqfull[i], 1);
+      mbar_init(&B->dqempty[i], NDZT);
+      mbar_init(&B->dwred[i], NDZT);
+    }
+    mbar_init(&B->drain, 1);
+    *cx.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == W_MMA) {
+    tmem_alloc(tmem_slot, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cx.tmem = *tmem_slot;
+
+  if (warp == W_PROD) {
+    producer_role(p, cx);
+  } else if (warp == W_MMA) {
+    if ((threadIdx.x & 31) == 0) mma_role(p, cx);
+    __syncwarp();
+  } else if (warp < W_DZ0) {
+    q_role(p, cx);
+  } else if (warp < W_DK0) {
+    dz_role(p, cx);
+  } else {
+    dk_role(p, cx);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_MMA) tmem_dealloc(cx.tmem, TM_COLS);
+}
+
+// k (bf16, [rows, D]) -> fp16 [rows, 128], zero padded beyond D.
+__global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16,
+                                long long rows, int D) {
+  const long long n = rows * (kDP / 8);
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < n;
+       x += (long long)gridDim.x * blockDim.x) {
+    const long long row = x / (kDP / 8);
+    const int ch = (int)(x % (kDP / 8));
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (ch * 8 < D) v = __ldg(reinterpret_cast<const uint4*>(k + row * D + ch * 8));
+    uint4 o = make_uint4(bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z),
+                         bf16x2_to_half2(v.w));
+    *reinterpret_cast<uint4*>(k16 + row * kDP + ch * 8) = o;
+  }
+}
+
+unsigned long long gcd_u64(unsigned long long a, unsigned long long b) {
+  while (b) {
+    unsigned long long t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// Multiplier of the row permutation u -> u*A mod rows: the golden-ratio
+// point of rows, nudged to be coprime with rows (a bijection).
+unsigned long long row_permutation_multiplier(long long rows) {
+  if (rows <= 2) return 1;
+  unsigned long long a = (unsigned long long)((double)rows * 0.6180339887498949);
+  if (a < 1) a = 1;
+  while (gcd_u64(a, (unsigned long long)rows) != 1) ++a;
+  return a % (unsigned long long)rows;
+}
+
+}  // namespace
+
+cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
+cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
+
+WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic) {
+  (void)H;
+  WsLayout w{};
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off = 0;
+  w.k16 = off;
+  off = up(off + (size_t)B * S_k * kDP * 2);
+  w.nchunks = 0;
+  if (deterministic) {
+    const long long rows = (long long)B * S_q;
+    w.u = off;
+    off = up(off + (size_t)rows * L * D * 4);
+    w.nchunks = (long long)B * ((S_q + 15) / 16);
+    w.hist = off;
+    off = up(off + (size_t)w.nchunks * S_k * 4);
+    w.key_start = off;
+    off = up(off + ((size_t)B * S_k + 1) * 4);
+    w.perm = off;
+    off = up(off + (size_t)rows * L * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+  const WsLayout lay = gemm_workspace_layout(a.B, a.S_q, a.S_k, a.H, a.D, a.L, a.deterministic);
+  char* ws = static_cast<char*>(a.ws);
+  __half* k16 = reinterpret_cast<__half*>(ws + lay.k16);
+  const long long krows = (long long)a.B * a.S_k;
+  {
+    const long long n = krows * (kDP / 8);
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 4LL * a.num_sms);
+    k_to_f16_kernel<<<blocks, 256, 0, st>>>(a.k, k16, krows, a.D);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (a.deterministic) {
+    cudaError_t e = launch_det_sort(a, lay, st);
+    if (e != cudaSuccess) return e;
+  }
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  KParams p{};
+  p.q = a.q;
+  p.k16 = k16;
+  p.w = a.w;
+  p.dI = a.dI;
+  p.idx = a.idx;
+  p.dq = a.dq;
+  p.dw = a.dw;
+  p.dk = a.dk;
+  p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
+  p.status = a.status;
+  p.rows = (long long)a.B * a.S_q;
+  p.perm_mul = row_permutation_multiplier(p.rows);
+  p.wait_ns = 2000000000ull;
+  p.S_q = a.S_q;
+  p.S_k = a.S_k;
+  p.H = a.H;
+  p.D = a.D;
+  p.L = a.L;
+  p.dense = a.idx == nullptr;
+  const int grid = (int)std::min<long long>(a.num_sms, p.rows);
+  gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.deterministic) return launch_det_segsum(a, lay, st);
+  return cudaSuccess;
+}
+
+}  // namespace ibwd

@@ -1,0 +1,232 @@
+// Score-grad of the lightning-indexer backward (kernel 1).
+//
+// cudnn-frontend #730 "optimize SM100 gradient kernels" (walkthrough): kernel 1
+// turns the forward indexer logits (index_score, read only) and the target
+// distribution (attn_score) into the gradient signal dI, written in place over
+// attn_score; the same change fuses the zeroing of the fp32 dK accumulator
+// into this launch.  #549 names the kernel kernel_score_grad.  The pages give
+// no formula; the plain reading is the gradient of the row-mean KL divergence
+// KL(ahat || softmax(I)):
+//   p_j    = exp(I_j - m) / sum_valid exp(I - m)      (m = max over valid j)
+//   ahat_j = a_j / sum_valid a                        (0 when the sum is 0)
+//   dI_j   = grad_scale * (p_j - ahat_j) / S_q         (0 on padding slots)
+// A slot is valid iff its id lies in [0, S_k) (dense rows: iff j <= t).
+// Padding slots are selected out, never multiplied by a mask, so NaN or
+// garbage there never reaches dI.
+//
+// HBM-bound: 16 bytes per slot (read I, a, id; write dI).  A group of
+// 32*W threads owns a row and keeps it in registers (NV float4 per thread per
+// array), reductions are fixed-order butterflies (bitwise reproducible).
+#include <algorithm>
+
+#include "internal.h"
+
+namespace ibwd {
+namespace {
+
+constexpr int BLOCK = 256;
+
+template <int W>
+struct RowReduce {
+  // Sum/max over the row group (W warps) in a fixed order.
+  __device__ static float sum(float v, float* sh, int wig) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (W == 1) return v;
+    const int lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) sh[wig] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) t += sh[i];
+    return t;
+  }
+  __device__ static float max(float v, float* sh, int wig) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (W == 1) return v;
+    const int lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) sh[wig] = v;
+    __syncthreads();
+    float t = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < W; ++i) t = fmaxf(t, sh[i]);
+    return t;
+  }
+};
+
+// NV float4 per thread per array; W warps per row; BLOCK/(32W) rows per block.
+template <int NV, int W>
+__global__ void __launch_bounds__(BLOCK) score_grad_vec(ScoreGradArgs a, long long row_blocks) {
+  __shared__ float red[BLOCK / 32];
+  constexpr int G = 32 * W;                 // threads per row
+  constexpr int RPB = BLOCK / G;            // rows per block
+  if ((long long)blockIdx.x >= row_blocks) {
+    // trailing blocks zero the dK accumulator
+    if (a.dk_zero) {
+      const long long nb = gridDim.x - row_blocks;
+      const long long n4 = a.dk_numel / 4;
+      float4* d4 = reinterpret_cast<float4*>(a.dk_zero);
+      for (long long x = (blockIdx.x - row_blocks) * (long long)BLOCK + threadIdx.x; x < n4; x += nb * BLOCK)
+        d4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (long long x = n4 * 4 + (blockIdx.x - row_blocks) * (long long)BLOCK + threadIdx.x; x < a.dk_numel;
+           x += nb * BLOCK)
+        a.dk_zero[x] = 0.f;
+    }
+    return;
+  }
+  const int grp = threadIdx.x / G;          // row within the block
+  const int gt = threadIdx.x % G;           // thread within the row group
+  const int wig = gt / 32;                  // warp within the row group
+  float* sh = red + grp * W;
+  const long long r = (long long)blockIdx.x * RPB + grp;
+  const bool live = r < a.rows;             // uniform per row group
+  const long long rr = live ? r : 0;
+  const int L4 = a.L / 4;
+  const float4* I4 = reinterpret_cast<const float4*>(a.index_score + rr * a.L);
+  float4* A4 = reinterpret_cast<float4*>(a.attn_score + rr * a.L);
+  const int4* X4 = a.idx ? reinterpret_cast<const int4*>(a.idx + rr * a.L) : nullptr;
+  const int t = (int)(rr % a.S_q);
+  const int lim = a.idx ? a.L : min(a.L, t + 1);  // dense: slots beyond t are padding
+
+  float iv[NV][4], av[NV][4];
+  bool vv[NV][4];
+  float m = -INFINITY, sa = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v4 = gt + k * G;
+    const bool in = live && v4 < L4 && v4 * 4 < lim;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+    int4 id = make_int4(-1, -1, -1, -1);
+    if (in) {
+      x = __ldcs(I4 + v4);
+      y = __ldcs(A4 + v4);
+      if (X4) id = __ldcs(X4 + v4);
+    }
+    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+    const int ids[4] = {id.x, id.y, id.z, id.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = v4 * 4 + e;
+      const bool v = in && (X4 ? ((unsigned)ids[e] < (unsigned)a.S_k) : (j < lim));
+      vv[k][e] = v;
+      iv[k][e] = xs[e];
+      av[k][e] = ys[e];
+      if (v) {
+        m = fmaxf(m, xs[e]);
+        sa += ys[e];
+      }
+    }
+  }
+  m = RowReduce<W>::max(m, sh, wig);
+  sa = RowReduce<W>::sum(sa, sh, wig);
+  float z = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float ex = vv[k][e] ? expf(iv[k][e] - m) : 0.f;
+      iv[k][e] = ex;
+      z += ex;
+    }
+  z = RowReduce<W>::sum(z, sh, wig);
+  if (!live) return;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int v4 = gt + k * G;
+    if (v4 >= L4) continue;
+    float o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float ahat = sa != 0.f ? __fdiv_rn(av[k][e], sa) : 0.f;
+      o[e] = vv[k][e] ? a.scale * (__fdiv_rn(iv[k][e], z) - ahat) : 0.f;
+    }
+    __stcs(A4 + v4, make_float4(o[0], o[1], o[2], o[3]));
+  }
+}
+
+// Any row length: one block per row, three strided passes.
+__global__ void __launch_bounds__(BLOCK) score_grad_generic(ScoreGradArgs a, long long row_blocks) {
+  __shared__ float red[BLOCK / 32];
+  if ((long long)blockIdx.x >= row_blocks) {
+    if (a.dk_zero) {
+      const long long nb = gridDim.x - row_blocks;
+      for (long long x = (blockIdx.x - row_blocks) * (long long)BLOCK + threadIdx.x; x < a.dk_numel; x += nb * BLOCK)
+        a.dk_zero[x] = 0.f;
+    }
+    return;
+  }
+  const long long r = blockIdx.x;
+  const float* I = a.index_score + r * a.L;
+  float* A = a.attn_score + r * a.L;
+  const int32_t* X = a.idx ? a.idx + r * a.L : nullptr;
+  const int t = (int)(r % a.S_q);
+  const int lim = a.idx ? a.L : min(a.L, t + 1);
+  auto valid = [&](int j) { return X ? ((unsigned)X[j] < (unsigned)a.S_k) : (j < lim); };
+  auto block_reduce = [&](float v, bool is_max) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float u = __shfl_xor_sync(0xffffffffu, v, o);
+      v = is_max ? fmaxf(v, u) : v + u;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float t2 = is_max ? -INFINITY : 0.f;
+    for (int i = 0; i < BLOCK / 32; ++i) t2 = is_max ? fmaxf(t2, red[i]) : t2 + red[i];
+    return t2;
+  };
+  float m = -INFINITY, sa = 0.f;
+  for (int j = threadIdx.x; j < a.L; j += BLOCK)
+    if (valid(j)) {
+      m = fmaxf(m, I[j]);
+      sa += A[j];
+    }
+  m = block_reduce(m, true);
+  sa = block_reduce(sa, false);
+  float z = 0.f;
+  for (int j = threadIdx.x; j < a.L; j += BLOCK)
+    if (valid(j)) z += expf(I[j] - m);
+  z = block_reduce(z, false);
+  for (int j = threadIdx.x; j < a.L; j += BLOCK) {
+    float o = 0.f;
+    if (valid(j)) {
+      const float ahat = sa != 0.f ? __fdiv_rn(A[j], sa) : 0.f;
+      o = a.scale * (__fdiv_rn(expf(I[j] - m), z) - ahat);
+    }
+    A[j] = o;
+  }
+}
+
+template <int NV, int W>
+cudaError_t launch_vec(const ScoreGradArgs& a, int zero_blocks, cudaStream_t st) {
+  constexpr int RPB = BLOCK / (32 * W);
+  const long long row_blocks = (a.rows + RPB - 1) / RPB;
+  score_grad_vec<NV, W><<<(unsigned)(row_blocks + zero_blocks), BLOCK, 0, st>>>(a, row_blocks);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st) {
+  const int zero_blocks = a.dk_zero ? (int)std::min<long long>(256, (a.dk_numel / 4 + BLOCK - 1) / BLOCK + 1) : 0;
+  const bool aligned = (a.L % 4 == 0) && ((uintptr_t)a.index_score % 16 == 0) &&
+                       ((uintptr_t)a.attn_score % 16 == 0) && (!a.idx || (uintptr_t)a.idx % 16 == 0) &&
+                       (!a.dk_zero || (uintptr_t)a.dk_zero % 16 == 0);
+  if (aligned) {
+    const int L = a.L;
+    if (L <= 128) return launch_vec<1, 1>(a, zero_blocks, st);
+    if (L <= 256) return launch_vec<2, 1>(a, zero_blocks, st);
+    if (L <= 512) return launch_vec<4, 1>(a, zero_blocks, st);
+    if (L <= 1024) return launch_vec<8, 1>(a, zero_blocks, st);
+    if (L <= 2048) return launch_vec<8, 2>(a, zero_blocks, st);
+    if (L <= 4096) return launch_vec<8, 4>(a, zero_blocks, st);
+    if (L <= 8192) return launch_vec<8, 8>(a, zero_blocks, st);
+  }
+  score_grad_generic<<<(unsigned)(a.rows + zero_blocks), BLOCK, 0, st>>>(a, a.rows);
+  return cudaGetLastError();
+}
+
+}  // namespace ibwd

@@ -1,0 +1,78 @@
+"""Host-only checks of the C ABI (no GPU compute): the library builds, loads
+and exports every function include/*.h declares; host-side helpers answer."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import sparse_attention_indexer_bwd_gb300 as ibwd
+from sparse_attention_indexer_bwd_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ibwd.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names += re.findall(r"IBWD_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    assert sorted(names) == sorted(ibwd.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = ibwd.status_string(code)
+        assert isinstance(s, str) and s
+    assert ibwd.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(lib):
+    a = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_ATOMIC)
+    assert a == 4096 * 128 * 2                           # fp16 copy of k
+    d = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_DETERMINISTIC)
+    assert d >= a + 8192 * 1024 * 128 * 4 + 8192 * 1024 * 4
+    assert ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 0) == 4096 * 128 * 2
+    # unsupported shapes report 0
+    assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 65, 128, 4, 0) == 0
+    assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 4, 12, 4, 0) == 0
+    assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 4, 32, 4, 5) == 0
+
+
+def test_shape_errors_need_no_device(lib):
+    # invalid shapes are rejected before any CUDA call
+    assert lib.indexer_bwd_score_grad(None, None, None, 0, 1, 1, 1, 1.0, None, 0, None) == ibwd.IBWD_ERR_INVALID_ARG
+    assert lib.indexer_bwd_score_grad(None, None, None, 1, 1, 1, 1, 1.0, None, 0, None) == ibwd.IBWD_ERR_INVALID_ARG
+    assert lib.indexer_bwd_gemm(None, None, None, None, None, None, None, None, 1, 4, 4, 4, 32, 4, 3, None, 0,
+                                None) == ibwd.IBWD_ERR_INVALID_ARG
+    assert lib.indexer_bwd_gemm(None, None, None, None, None, None, None, None, 1, 4, 4, 100, 32, 4, 0, None, 0,
+                                None) == ibwd.IBWD_ERR_UNSUPPORTED
+    assert lib.indexer_bwd_dense_gemm(None, None, None, None, None, None, None, 1, 4, 4, 136, 0, None, 0,
+                                      None) == ibwd.IBWD_ERR_UNSUPPORTED
+
+
+def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
+    # the product path has no fallback: a missing library raises on load
+    monkeypatch.setattr(ibwd, "_lib", None)
+    monkeypatch.setattr(ibwd, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        ibwd.load()
