@@ -16,24 +16,33 @@
 // compacted into tiles of 128 keys, and the keys are the M = 128 dimension of
 // every tensor-core MMA:
 //   MMA1  Z^T[128 s, 64 h]   = Ksel[128 s, 128 d] . Q^T          (TMEM, fp32)
-//   MMA2  dK [128 s, 128 d]  = dz[128 s, 64 h] . Q[64 h, 128 d]  (TMEM, fp32)
+//   MMA2  dK^T[128 d, 128 s] = Q^T[128 d, 64 h] . dz^T[64 h, 128 s] (TMEM, fp32)
 //   MMA3  dQ^T[128 d, 64 h] += Ksel^T[128 d, 128 s] . dz[128 s, 64 h]
 // Operands are fp16 in 128-byte-swizzled shared memory: k is converted once to
-// an fp16 copy (bf16 -> fp16 is exact in fp16 range), q is converted per row,
-// and dz is scaled by a per-row power of two 2^c so that it stays in the fp16
-// normal range (bf16 dz would cost ~1.6e-3 relative RMS, over the dK budget).
-// The scale is undone exactly in the fp32 epilogues.
+// fp16 (bf16 -> fp16 is exact in fp16 range), q is converted per row, and dz
+// is scaled by a per-row power of two 2^c so that it stays in the fp16 normal
+// range (bf16 dz would cost ~1.6e-3 relative RMS, over the dK budget).  The
+// scale is undone exactly in the fp32 epilogues.
 //
-// Warp roles (16 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
-//   0     producer: row scan (valid count, max|dI|, scale), compaction into
-//         tile metadata, cp.async gather of the selected fp16 k rows
-//   1     MMA issuer (one thread) and TMEM owner (512 columns)
-//   2-3   Q loader: q[t] bf16 -> fp16 swizzled tile, w[t] -> shared
-//   4-7   dz group for heads 0-31, 8-11 dz group for heads 32-63: Z from
+// The selected key rows are gathered with 16-byte cp.async copies spread over
+// a warp group (16 lanes per 256-byte row, the swizzle applied in the
+// destination address); their completion arrives on the stage barrier.
+// dK is produced transposed (TMEM lane = column d), so that in the epilogue
+// each warp instruction reduces one whole 128-byte line of a dK row.
+//
+// Warp roles (20 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
+//   0-3   gather: 16 cp.async per thread per tile (selected fp16 key rows)
+//   4     scan: row idx/dI staged in shared memory by bulk copies (one row
+//         ahead); valid count, max|dI| and scale; compaction into tile
+//         metadata
+//   5     MMA issuer (one thread) and TMEM owner (512 columns)
+//   6-7   Q loader: q[t] bf16 -> fp16 swizzled tile, w[t] -> shared
+//   8-11  dz group for heads 0-31, 12-15 dz group for heads 32-63: Z from
 //         TMEM -> dW partial sums in registers, dz -> fp16 shared tile; at row
 //         end the dW reduction; one row later the dQ epilogue (TMEM -> fp32)
-//   12-15 dK group: dK tile from TMEM -> fp32 red.global.add.v4 into dk, or
-//         plain stores into the per-slot workspace in deterministic mode
+//   16-19 dK group: dK^T tile from TMEM -> fp32 red.global.add (one 128-byte
+//         line per warp instruction) into dk, or plain stores into the
+//         per-slot workspace in deterministic mode
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
 #include <algorithm>
@@ -44,12 +53,15 @@
 namespace ibwd {
 namespace {
 
-constexpr int KST = 4;  // K-tile stages
+constexpr int KST = 3;  // K-tile stages
 constexpr int MST = 4;  // tile-metadata ring
-constexpr int NTHREADS = 512;
-constexpr int W_PROD = 0, W_MMA = 1, W_Q0 = 2, W_DZ0 = 4, W_DK0 = 12;
-constexpr int NQT = 64;    // Q-loader threads
-constexpr int NDZT = 256;  // dz threads (two groups of 128)
+constexpr int NTHREADS = 640;
+constexpr int W_GATHER0 = 0, W_SCAN = 4, W_MMA = 5, W_Q0 = 6, W_DZ0 = 8, W_DK0 = 16;
+constexpr int NGT = 128;                  // gather threads
+constexpr int NQT = 64;                   // Q-loader threads
+constexpr int NDZT = 256;                 // dz threads (two groups of 128)
+constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI (sparse) or dI (dense)
+constexpr uint32_t ROW_DI_OFF = 8192;     // dI offset inside a staged sparse row
 
 constexpr uint32_t KTILE_BYTES = kBM * kDP * 2;   // 32 KB
 constexpr uint32_t KHALF_BYTES = kBM * 64 * 2;    // one 64-column half of a K tile
@@ -71,6 +83,7 @@ enum { F_FIRST = 1, F_LAST = 2, F_END = 4 };
 struct Bars {
   uint64_t kfull[KST], kempty[KST];
   uint64_t mfull[MST], mempty[MST];
+  uint64_t rowfull[2];
   uint64_t qfull[2];
   uint64_t zfull[2], zempty[2];
   uint64_t dzfull[2], dzempty[2];
@@ -83,18 +96,19 @@ struct Bars {
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = OFF_K + KST * KTILE_BYTES;
 constexpr uint32_t OFF_DZ = OFF_Q + 2 * QTILE_BYTES;
-constexpr uint32_t OFF_META = OFF_DZ + 2 * DZTILE_BYTES;
+constexpr uint32_t OFF_ROW = OFF_DZ + 2 * DZTILE_BYTES;
+constexpr uint32_t OFF_META = OFF_ROW + 2 * ROW_BYTES;
 constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
 constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
 constexpr uint32_t OFF_BARS = OFF_RED + 2 * 4 * kHP * 4;  // [2][4 warps][64 heads]
 constexpr uint32_t OFF_MISC = OFF_BARS + sizeof(Bars);
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-static_assert(OFF_BARS % 8 == 0, "barrier alignment");
+static_assert(OFF_BARS % 8 == 0 && OFF_ROW % 16 == 0, "alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct KParams {
   const uint16_t* q;
-  const __half* k16;
+  const __half* k16;   // [B][S_k + 1][128]; row S_k of each batch is zero
   const float* w;
   const float* dI;
   const int32_t* idx;
@@ -106,7 +120,8 @@ struct KParams {
   long long rows;
   unsigned long long perm_mul;
   unsigned long long wait_ns;
-  int S_q, S_k, H, D, L, dense;
+  int B, S_q, S_k, H, D, L, dense;
+  int staged;  // rows are staged in shared memory by bulk copies
 };
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
@@ -133,7 +148,33 @@ struct Ctx {
   long long nq;
 };
 
+// Optional per-tile timeline (clock64 stamps of each role's progress in the
+// first CTAs), compiled only with -DIBWD_TRACE for pipeline analysis.
+enum TraceEv {
+  EV_SCAN_PUB, EV_GATHER_ISSUED, EV_MMA_KFULL, EV_MMA_Z, EV_MMA_DZFULL, EV_MMA_DKEMPTY, EV_MMA_DKDQ,
+  EV_DZ_ZFULL, EV_DZ_DONE, EV_DK_FULL, EV_DK_DONE, EV_Q_READY, EV_COUNT
+};
+#ifdef IBWD_TRACE
+constexpr int TRACE_CTAS = 4, TRACE_TILES = 256;
+__device__ unsigned long long g_trace[TRACE_CTAS][EV_COUNT][TRACE_TILES];
+#define TRACE(ev, g)                                                                    \
+  do {                                                                                  \
+    if (blockIdx.x < TRACE_CTAS && (g) >= 0 && (g) < TRACE_TILES) g_trace[blockIdx.x][ev][g] = clock64(); \
+  } while (0)
+#else
+#define TRACE(ev, g) \
+  do {               \
+  } while (0)
+#endif
+
 #define WAIT(bar, par) mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns)
+
+// A bounded wait that ignores the abort flag: used only to drain work that
+// was already issued before the kernel may exit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const KParams& p) {
+  volatile int never = 0;
+  mbar_wait(bar, parity, &never, p.status, p.wait_ns);
+}
 
 // ------------------------------------------------------------ Q loader ----
 __device__ void q_role(const KParams& p, const Ctx& cx) {
@@ -146,142 +187,209 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
     const long long r = row_of(blockIdx.x + i * gridDim.x, p);
     const uint16_t* qr = p.q + r * p.H * p.D;
     const uint32_t qs = cx.sbase + OFF_Q + qb * QTILE_BYTES;
-    uint4 v[16];
 #pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int x = tid + it * NQT;  // 16-byte chunk: head h, column chunk ch
-      const int h = x >> 4, ch = x & 15;
-      v[it] = make_uint4(0u, 0u, 0u, 0u);
-      if (h < p.H && ch * 8 < p.D) v[it] = __ldg(reinterpret_cast<const uint4*>(qr + h * p.D + ch * 8));
-    }
+    for (int half = 0; half < 2; ++half) {
+      uint4 v[8];
 #pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int x = tid + it * NQT;
-      const int h = x >> 4, ch = x & 15;
-      const uint32_t dst = qs + (ch >> 3) * QHALF_BYTES + h * 128 + (((ch & 7) ^ (h & 7)) << 4);
-      st_shared_v4(dst, bf16x2_to_half2(v[it].x), bf16x2_to_half2(v[it].y),
-                   bf16x2_to_half2(v[it].z), bf16x2_to_half2(v[it].w));
+      for (int it = 0; it < 8; ++it) {
+        const int x = tid + (half * 8 + it) * NQT;  // 16-byte chunk: head h, column chunk ch
+        const int h = x >> 4, ch = x & 15;
+        v[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (h < p.H && ch * 8 < p.D) v[it] = __ldg(reinterpret_cast<const uint4*>(qr + h * p.D + ch * 8));
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int x = tid + (half * 8 + it) * NQT;
+        const int h = x >> 4, ch = x & 15;
+        const uint32_t dst = qs + (ch >> 3) * QHALF_BYTES + h * 128 + (((ch & 7) ^ (h & 7)) << 4);
+        st_shared_v4(dst, bf16x2_to_half2(v[it].x), bf16x2_to_half2(v[it].y), bf16x2_to_half2(v[it].z),
+                     bf16x2_to_half2(v[it].w));
+      }
     }
     cx.w_s[qb * kHP + tid] = tid < p.H ? __ldg(p.w + r * p.H + tid) : 0.f;
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->qfull[qb]);
+    if (tid == 0) TRACE(EV_Q_READY, (int)i);
   }
 }
 
-// ------------------------------------------------------------- producer ---
-__device__ void producer_role(const KParams& p, const Ctx& cx) {
+// ----------------------------------------------------------------- scan ---
+// Slot source of one query row: the staged copy in shared memory or global.
+struct RowSrc {
+  const int32_t* idx;  // nullptr for dense rows
+  const float* dI;
+  int Lr;              // slots to look at
+  int S_k;
+  __device__ __forceinline__ bool key(int j, int& s) const {
+    if (!idx) {
+      s = j;
+      return true;
+    }
+    s = idx[j];
+    return (unsigned)s < (unsigned)S_k;
+  }
+};
+
+__device__ void scan_role(const KParams& p, const Ctx& cx) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  uint8_t* rowbuf = cx.smem + OFF_ROW;
+  long long staged_wait = -1;  // last row whose bulk copy was issued but not yet waited for
+  auto issue_row = [&](long long i) {
+    const long long r = row_of(blockIdx.x + i * gridDim.x, p);
+    const int t = (int)(r % p.S_q);
+    const int buf = (int)(i & 1);
+    if (lane == 0) {
+      // this thread's earlier generic reads of the buffer precede the async writes
+      fence_proxy_async_smem();
+      const uint32_t dst = smem_u32(rowbuf + buf * ROW_BYTES);
+      if (p.dense) {
+        const uint32_t bytes = (uint32_t)(((min(p.L, t + 1) * 4) + 15) & ~15);
+        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], bytes);
+        bulk_g2s(dst, p.dI + r * p.L, bytes, &cx.bars->rowfull[buf]);
+      } else {
+        const uint32_t bytes = (uint32_t)p.L * 4;
+        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], 2 * bytes);
+        bulk_g2s(dst, p.idx + r * p.L, bytes, &cx.bars->rowfull[buf]);
+        bulk_g2s(dst + ROW_DI_OFF, p.dI + r * p.L, bytes, &cx.bars->rowfull[buf]);
+      }
+    }
+    staged_wait = i;
+  };
+
   int g = 0;
-  bool pending = false;
+  if (p.staged) issue_row(0);
   for (long long i = 0; i < cx.nq; ++i) {
     const long long r = row_of(blockIdx.x + i * gridDim.x, p);
-    const int b = (int)(r / p.S_q);
     const int t = (int)(r % p.S_q);
-    const int32_t* idxr = p.dense ? nullptr : p.idx + r * p.L;
-    const float* dIr = p.dI + r * p.L;
-    const int Lr = p.dense ? min(p.L, t + 1) : p.L;
-    // pass 1: number of valid slots and max |dI| over them
-    int nv = 0;
-    float mx = 0.f;
-    for (int j0 = 0; j0 < Lr; j0 += 32) {
-      const int j = j0 + lane;
-      bool v = false;
-      if (j < Lr) v = p.dense ? true : ((unsigned)__ldg(idxr + j) < (unsigned)p.S_k);
-      if (v) mx = fmaxf(mx, fabsf(__ldg(dIr + j)));
-      nv += __popc(__ballot_sync(0xffffffffu, v));
-    }
-    mx = warp_max(mx);
-    float wm = 0.f;
-    for (int h = lane; h < p.H; h += 32) wm = fmaxf(wm, fabsf(__ldg(p.w + r * p.H + h)));
-    wm = warp_max(wm);
-    // per-row scale 2^c: max |dI w| 2^c lies in [2^13, 2^14), inside fp16 range
-    const float m = mx * wm;
-    int c = 0;
-    if (m > 0.f && m <= 3.0e38f) {
-      int e;
-      frexpf(m, &e);
-      c = max(-120, min(120, 14 - e));
-    }
-    const float sc = pow2f(c);
-    const int ntiles = max(1, (nv + kBM - 1) / kBM);
-    // pass 2: compact the valid slots into tiles of 128 and gather their keys
-    int jc = 0, skip = 0;
-    for (int tt = 0; tt < ntiles; ++tt, ++g) {
-      const int ms = g % MST;
-      if (!WAIT(&cx.bars->mempty[ms], (uint32_t)(((g / MST) & 1) ^ 1))) goto done;
-      TileMeta& M = cx.meta[ms];
-      int fill = 0;
-      while (fill < kBM && jc < Lr) {
-        const int j = jc + lane;
-        bool v = false;
-        int s = 0;
-        if (j < Lr) {
-          s = p.dense ? j : __ldg(idxr + j);
-          v = p.dense ? true : ((unsigned)s < (unsigned)p.S_k);
-        }
-        const unsigned mask = __ballot_sync(0xffffffffu, v);
-        const int tot = __popc(mask);
-        const int rank = __popc(mask & lt_mask);
-        const int room = kBM - fill;
-        if (v && rank >= skip && rank < skip + room) {
-          const int pos = fill + rank - skip;
-          M.key[pos] = s;
-          M.slot[pos] = j;
-          M.dis[pos] = __ldg(dIr + j) * sc;
-        }
-        const int taken = min(tot - skip, room);
-        fill += taken;
-        if (skip + taken < tot) {
-          skip += taken;
-        } else {
-          skip = 0;
-          jc += 32;
-        }
-      }
-      if (lane == 0) {
-        M.r = (int)r;
-        M.count = fill;
-        M.c = c;
-        M.flags = (tt == 0 ? F_FIRST : 0) | (tt == ntiles - 1 ? F_LAST : 0) |
-                  ((tt == ntiles - 1 && i == cx.nq - 1) ? F_END : 0);
-      }
+    RowSrc src;
+    src.S_k = p.S_k;
+    src.Lr = p.dense ? min(p.L, t + 1) : p.L;
+    if (p.staged) {
+      const int buf = (int)(i & 1);
+      if (!WAIT(&cx.bars->rowfull[buf], (uint32_t)((i >> 1) & 1))) goto done;
+      staged_wait = -1;
       __syncwarp();
-      const int st = g % KST;
-      if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) goto done;
-      const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES;
-      const __half* kb = p.k16 + (long long)b * p.S_k * kDP;
-#pragma unroll 4
-      for (int it = 0; it < kBM / 2; ++it) {
-        const int row = it * 2 + (lane >> 4);
-        const int ch = lane & 15;
-        const bool ok = row < fill;
-        const int key = ok ? M.key[row] : 0;
-        const uint32_t dst = kbase + (ch >> 3) * KHALF_BYTES + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
-        cp_async16(dst, kb + (long long)key * kDP + ch * 8, ok ? 16u : 0u);
-      }
-      cp_async_commit();
-      mbar_arrive(&cx.bars->mfull[ms]);
-      if (pending) {
-        // the previous tile's copies have landed: publish them to the tensor core
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        mbar_arrive(&cx.bars->kfull[(g - 1) % KST]);
-      }
-      pending = true;
+      if (i + 1 < cx.nq) issue_row(i + 1);
+      const uint8_t* rb = rowbuf + buf * ROW_BYTES;
+      src.idx = p.dense ? nullptr : reinterpret_cast<const int32_t*>(rb);
+      src.dI = reinterpret_cast<const float*>(rb + (p.dense ? 0 : ROW_DI_OFF));
+    } else {
+      src.idx = p.dense ? nullptr : p.idx + r * p.L;
+      src.dI = p.dI + r * p.L;
     }
+    {
+      // pass 1: number of valid slots and max |dI| over them
+      int nv = 0;
+      float mx = 0.f;
+      for (int j0 = 0; j0 < src.Lr; j0 += 32) {
+        const int j = j0 + lane;
+        int s;
+        const bool v = j < src.Lr && src.key(j, s);
+        if (v) mx = fmaxf(mx, fabsf(src.dI[j]));
+        nv += __popc(__ballot_sync(0xffffffffu, v));
+      }
+      mx = warp_max(mx);
+      // per-row scale 2^c: max |dI w| 2^c lies in [2^13, 2^14), inside fp16 range
+      float wm = 0.f;
+      for (int h = lane; h < p.H; h += 32) wm = fmaxf(wm, fabsf(__ldg(p.w + r * p.H + h)));
+      wm = warp_max(wm);
+      const float m = mx * wm;
+      int c = 0;
+      if (m > 0.f && m <= 3.0e38f) {
+        int e;
+        frexpf(m, &e);
+        c = max(-120, min(120, 14 - e));
+      }
+      const float sc = pow2f(c);
+      const int ntiles = max(1, (nv + kBM - 1) / kBM);
+      // pass 2: compact the valid slots, in slot order, into tiles of 128
+      int jc = 0, skip = 0;
+      for (int tt = 0; tt < ntiles; ++tt, ++g) {
+        const int ms = g % MST;
+        if (!WAIT(&cx.bars->mempty[ms], (uint32_t)(((g / MST) & 1) ^ 1))) goto done;
+        TileMeta& M = cx.meta[ms];
+        int fill = 0;
+        while (fill < kBM && jc < src.Lr) {
+          const int j = jc + lane;
+          int s = 0;
+          const bool v = j < src.Lr && src.key(j, s);
+          const unsigned mask = __ballot_sync(0xffffffffu, v);
+          const int tot = __popc(mask);
+          const int rank = __popc(mask & lt_mask);
+          const int room = kBM - fill;
+          if (v && rank >= skip && rank < skip + room) {
+            const int pos = fill + rank - skip;
+            M.key[pos] = s;
+            M.slot[pos] = j;
+            M.dis[pos] = src.dI[j] * sc;
+          }
+          const int taken = min(tot - skip, room);
+          fill += taken;
+          if (skip + taken < tot) {
+            skip += taken;
+          } else {
+            skip = 0;
+            jc += 32;
+          }
+        }
+        if (lane == 0) {
+          M.r = (int)r;
+          M.count = fill;
+          M.c = c;
+          M.flags = (tt == 0 ? F_FIRST : 0) | (tt == ntiles - 1 ? F_LAST : 0) |
+                    ((tt == ntiles - 1 && i == cx.nq - 1) ? F_END : 0);
+        }
+        __syncwarp();
+        mbar_arrive(&cx.bars->mfull[ms]);
+        if (lane == 0) TRACE(EV_SCAN_PUB, g);
+      }
+    }
+    __syncwarp();
   }
 done:
-  cp_async_wait_all();
-  if (pending) {
-    fence_proxy_async_smem();
-    mbar_arrive(&cx.bars->kfull[(g - 1) % KST]);
+  // a row copy still in flight must land before the CTA can exit
+  if (staged_wait >= 0) drain_wait(&cx.bars->rowfull[staged_wait & 1], (uint32_t)((staged_wait >> 1) & 1), p);
+}
+
+// --------------------------------------------------------------- gather ---
+// Thread x copies chunk (x % 16) of rows (x / 16) + 8i, i = 0..15: every warp
+// instruction moves two whole 256-byte key rows.  Row r of the tile lands in
+// the 128-byte-swizzle layout: half (chunk / 8), XOR (chunk % 8) ^ (r % 8).
+// Each thread's copies arrive on the stage barrier when they land.
+__device__ void gather_role(const KParams& p, const Ctx& cx) {
+  const int x = threadIdx.x - W_GATHER0 * 32;  // 0..127
+  const int rsub = x >> 4, ch = x & 15;
+  const uint32_t dst_off = (ch >> 3) * KHALF_BYTES + rsub * 128 + (((ch & 7) ^ rsub) << 4);
+  for (int g = 0;; ++g) {
+    const int ms = g % MST;
+    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) break;
+    const TileMeta& M = cx.meta[ms];
+    const int count = M.count, flags = M.flags;
+    const long long b = M.r / p.S_q;
+    const int st = g % KST;
+    if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) break;
+    const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES + dst_off;
+    const __half* kb = p.k16 + b * (p.S_k + 1) * kDP + ch * 8;
+    int key[kBM / 8];
+#pragma unroll
+    for (int i = 0; i < kBM / 8; ++i) {
+      const int row = rsub + 8 * i;
+      key[i] = row < count ? M.key[row] : p.S_k;  // padding rows copy the zero row
+    }
+#pragma unroll
+    for (int i = 0; i < kBM / 8; ++i) cp_async16(kbase + i * 1024, kb + (long long)key[i] * kDP, 16);
+    cp_async_mbar_arrive_noinc(&cx.bars->kfull[st]);
+    if (x == 0) TRACE(EV_GATHER_ISSUED, g);
+    if (flags & F_END) break;
   }
+  // copies in flight must land before the CTA can exit
+  cp_async_wait_all();
 }
 
 // ------------------------------------------------------------------ MMA ---
 constexpr uint32_t ID_Z = idesc_f16_f32(128, 64, 0, 0);    // Z^T = K . Q^T
-constexpr uint32_t ID_DK = idesc_f16_f32(128, 128, 0, 1);  // dK = dz . Q   (Q as MN-major B)
+constexpr uint32_t ID_DKT = idesc_f16_f32(128, 128, 1, 0);  // dK^T = Q^T . dz^T (Q as MN-major A)
 constexpr uint32_t ID_DQ = idesc_f16_f32(128, 64, 1, 1);   // dQ^T = K^T . dz (both MN-major)
 
 __device__ __forceinline__ void mma_z(const Ctx& cx, int g, int qb) {
@@ -302,9 +410,9 @@ __device__ __forceinline__ void mma_dk(const Ctx& cx, int g, int qb) {
   const uint32_t d = cx.tmem + TM_DK + (g & 1) * 128;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {  // K = H = 64 in steps of 16
-    const uint64_t ad = sw128_desc(za + k * 32, 16, 1024);
-    const uint64_t bd = sw128_desc(qa + k * 2048, QHALF_BYTES, 1024);
-    umma_f16(d, ad, bd, ID_DK, k > 0);
+    const uint64_t ad = sw128_desc(qa + k * 2048, QHALF_BYTES, 1024);  // Q^T: M = d, MN-major
+    const uint64_t bd = sw128_desc(za + k * 32, 16, 1024);             // dz^T: N = s, K-major
+    umma_f16(d, ad, bd, ID_DKT, k > 0);
   }
 }
 
@@ -328,6 +436,9 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
   {
     int flags = cx.meta[0].flags;
     if (!WAIT(&B->qfull[0], 0) || !WAIT(&B->kfull[0], 0)) goto drain;
+    // the key tile was written by cp.async (generic proxy): order it before
+    // the tensor core's reads
+    fence_proxy_async_smem();
     tc_fence_after();
     mma_z(cx, 0, 0);
     umma_commit(&B->zfull[0]);
@@ -344,13 +455,18 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
           if (!WAIT(&B->qfull[niq & 1], (uint32_t)((niq >> 1) & 1))) goto drain;
         }
         if (!WAIT(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1))) goto drain;
+        TRACE(EV_MMA_KFULL, g1);
         if (!WAIT(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1))) goto drain;
+        fence_proxy_async_smem();
         tc_fence_after();
         mma_z(cx, g1, (int)(niq & 1));
+        TRACE(EV_MMA_Z, g1);
         umma_commit(&B->zfull[g1 & 1]);
       }
       if (!WAIT(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
+      TRACE(EV_MMA_DZFULL, g);
       if (!WAIT(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
+      TRACE(EV_MMA_DKEMPTY, g);
       if ((flags & F_FIRST) && !WAIT(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
       tc_fence_after();
       mma_dk(cx, g, (int)(iq & 1));
@@ -359,6 +475,7 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
       umma_commit(&B->kempty[g % KST]);
       umma_commit(&B->dzempty[g & 1]);
       if (flags & F_LAST) umma_commit(&B->dqfull[iq & 1]);
+      TRACE(EV_MMA_DKDQ, g);
       if (flags & F_END) break;
       ++g;
       flags = nflags;
@@ -366,13 +483,9 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
     }
   }
 drain:
-  // every MMA issued so far completes before TMEM can be released; this wait
-  // ignores the abort flag (it must not return early) but is still bounded
+  // every MMA issued so far completes before TMEM can be released
   umma_commit(&B->drain);
-  {
-    volatile int never = 0;
-    mbar_wait(&B->drain, 0, &never, p.status, p.wait_ns);
-  }
+  drain_wait(&B->drain, 0, p);
 }
 
 // ------------------------------------------------------------ dz group ----
@@ -421,8 +534,11 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
       if (!WAIT(&cx.bars->qfull[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
     }
     const float dis = s < count ? M.dis[s] : 0.f;
-    const float* wq = cx.w_s + (iq & 1) * kHP + hg * 32;
+    // dI 2^c w for this row's 32 heads, as fp32 pairs
+    const uint64_t* w2 = reinterpret_cast<const uint64_t*>(cx.w_s + (iq & 1) * kHP + hg * 32);
+    const uint64_t dis2 = pack2(__float_as_uint(dis), __float_as_uint(dis));
     if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
+    if (tdz == 0) TRACE(EV_DZ_ZFULL, g);
     if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
     tc_fence_after();
     const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
@@ -439,10 +555,12 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
       for (int e = 0; e < 4; ++e) {
         const int h0 = c8 * 8 + e * 2;
         const float z0 = z[h0], z1 = z[h0 + 1];
-        acc[h0] = fmaf(dis, fmaxf(z0, 0.f), acc[h0]);
-        acc[h0 + 1] = fmaf(dis, fmaxf(z1, 0.f), acc[h0 + 1]);
-        const float d0 = z0 > 0.f ? dis * wq[h0] : 0.f;
-        const float d1 = z1 > 0.f ? dis * wq[h0 + 1] : 0.f;
+        const uint64_t dw = mul_f32x2(dis2, w2[h0 >> 1]);
+        const bool p0 = z0 > 0.f, p1 = z1 > 0.f;
+        if (p0) acc[h0] = fmaf(dis, z0, acc[h0]);
+        if (p1) acc[h0 + 1] = fmaf(dis, z1, acc[h0 + 1]);
+        const float d0 = p0 ? __uint_as_float((uint32_t)dw) : 0.f;
+        const float d1 = p1 ? __uint_as_float((uint32_t)(dw >> 32)) : 0.f;
         pk[e] = pack_half2(d0, d1);
       }
       const int chunk = hg * 4 + c8;  // 16-byte chunk of the 128-byte dz row
@@ -450,6 +568,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     }
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
+    if (tdz == 0) TRACE(EV_DZ_DONE, g);
     if ((flags & F_FIRST) && ep_r >= 0) {
       dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
       ep_r = -1;
@@ -488,40 +607,46 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------ dK group ----
+// TMEM holds dK^T: lane = column d, TMEM column = tile row.  Thread d of the
+// group reduces element d of every valid row, so each warp instruction covers
+// 32 consecutive floats (one 128-byte line) of one dK row.
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-  const int s = qw * 32 + lane;
+  const int d = qw * 32 + lane;
+  const bool don = d < p.D;
   for (int g = 0;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
     const TileMeta& M = cx.meta[ms];
-    const int flags = M.flags, c = M.c, r = M.r;
-    const bool ok = s < M.count;
-    const int key = ok ? M.key[s] : 0;
-    const int slot = ok ? M.slot[s] : 0;
+    const int flags = M.flags, c = M.c, r = M.r, count = M.count;
+    float* base = p.u ? p.u + (long long)r * p.L * p.D + d
+                      : p.dk + (long long)(r / p.S_q) * p.S_k * p.D + d;
+    const int* ids = p.u ? M.slot : M.key;
     if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
+    if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, g);
     tc_fence_after();
     const float sc = pow2f(-c);
     const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK + (uint32_t)(g & 1) * 128;
-    float* dst = p.u ? p.u + ((long long)r * p.L + slot) * p.D
-                     : p.dk + ((long long)(r / p.S_q) * p.S_k + key) * p.D;
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
-      if (ch * 32 >= p.D) break;
+      if (ch * 32 >= count) break;  // uniform: the remaining rows are padding
       float v[32];
       tmem_ld32(ta + ch * 32, v);
       tmem_wait_ld();
-      if (ok) {
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const int d = ch * 32 + q4 * 4;
-          if (d < p.D) {
-            const float a0 = v[q4 * 4] * sc, a1 = v[q4 * 4 + 1] * sc;
-            const float a2 = v[q4 * 4 + 2] * sc, a3 = v[q4 * 4 + 3] * sc;
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const int4 id4 = *reinterpret_cast<const int4*>(ids + ch * 32 + j4 * 4);
+        const int idv[4] = {id4.x, id4.y, id4.z, id4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = ch * 32 + j4 * 4 + e;
+          if (row < count && don) {
+            float* dst = base + (long long)idv[e] * p.D;
+            const float val = v[j4 * 4 + e] * sc;
             if (p.u)
-              *reinterpret_cast<float4*>(dst + d) = make_float4(a0, a1, a2, a3);
+              *dst = val;
             else
-              red_add_v4(dst + d, a0, a1, a2, a3);
+              asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(val) : "memory");
           }
         }
       }
@@ -529,6 +654,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
     tc_fence_before();
     mbar_arrive(&cx.bars->dkempty[g & 1]);
     mbar_arrive(&cx.bars->mempty[ms]);
+    if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_DONE, g);
     if (flags & F_END) return;
   }
 }
@@ -550,9 +676,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
 
   if (threadIdx.x == 0) {
     Bars* B = cx.bars;
-    for (int i = 0; i < KST; ++i) { mbar_init(&B->kfull[i], 32); mbar_init(&B->kempty[i], 1); }
-    for (int i = 0; i < MST; ++i) { mbar_init(&B->mfull[i], 32); mbar_init(&B->mempty[i], 128); }
+    for (int i = 0; i < KST; ++i) {
+      mbar_init(&B->kfull[i], NGT);
+      mbar_init(&B->kempty[i], 1);
+    }
+    for (int i = 0; i < MST; ++i) {
+      mbar_init(&B->mfull[i], 32);
+      mbar_init(&B->mempty[i], 128);
+    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->rowfull[i], 1);
       mbar_init(&B->qfull[i], NQT);
       mbar_init(&B->zfull[i], 1);
       mbar_init(&B->zempty[i], NDZT);
@@ -577,8 +710,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   tc_fence_after();
   cx.tmem = *tmem_slot;
 
-  if (warp == W_PROD) {
-    producer_role(p, cx);
+  if (warp < W_SCAN) {
+    gather_role(p, cx);
+  } else if (warp == W_SCAN) {
+    scan_role(p, cx);
   } else if (warp == W_MMA) {
     if ((threadIdx.x & 31) == 0) mma_role(p, cx);
     __syncwarp();
@@ -596,19 +731,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   if (warp == W_MMA) tmem_dealloc(cx.tmem, TM_COLS);
 }
 
-// k (bf16, [rows, D]) -> fp16 [rows, 128], zero padded beyond D.
-__global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16,
-                                long long rows, int D) {
+// k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
+// row S_k of each batch zero (padding rows of a tile copy it).
+__global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16, int B, int S_k, int D) {
+  const long long rows = (long long)B * (S_k + 1);
   const long long n = rows * (kDP / 8);
   for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < n;
        x += (long long)gridDim.x * blockDim.x) {
-    const long long row = x / (kDP / 8);
     const int ch = (int)(x % (kDP / 8));
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (ch * 8 < D) v = __ldg(reinterpret_cast<const uint4*>(k + row * D + ch * 8));
-    uint4 o = make_uint4(bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z),
-                         bf16x2_to_half2(v.w));
-    *reinterpret_cast<uint4*>(k16 + row * kDP + ch * 8) = o;
+    const long long row = x / (kDP / 8);
+    const int b = (int)(row / (S_k + 1));
+    const int s = (int)(row % (S_k + 1));
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (s < S_k && ch * 8 < D) val = __ldg(reinterpret_cast<const uint4*>(k + ((long long)b * S_k + s) * D + ch * 8));
+    *reinterpret_cast<uint4*>(k16 + row * kDP + ch * 8) =
+        make_uint4(bf16x2_to_half2(val.x), bf16x2_to_half2(val.y), bf16x2_to_half2(val.z), bf16x2_to_half2(val.w));
   }
 }
 
@@ -642,7 +779,7 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   w.k16 = off;
-  off = up(off + (size_t)B * S_k * kDP * 2);
+  off = up(off + (size_t)B * (S_k + 1) * kDP * 2);
   w.nchunks = 0;
   if (deterministic) {
     const long long rows = (long long)B * S_q;
@@ -664,11 +801,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const WsLayout lay = gemm_workspace_layout(a.B, a.S_q, a.S_k, a.H, a.D, a.L, a.deterministic);
   char* ws = static_cast<char*>(a.ws);
   __half* k16 = reinterpret_cast<__half*>(ws + lay.k16);
-  const long long krows = (long long)a.B * a.S_k;
   {
-    const long long n = krows * (kDP / 8);
-    const int blocks = (int)std::min<long long>((n + 255) / 256, 4LL * a.num_sms);
-    k_to_f16_kernel<<<blocks, 256, 0, st>>>(a.k, k16, krows, a.D);
+    const long long n = (long long)a.B * (a.S_k + 1) * (kDP / 8);
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * a.num_sms);
+    k_to_f16_kernel<<<blocks, 256, 0, st>>>(a.k, k16, a.B, a.S_k, a.D);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -698,12 +834,17 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.rows = (long long)a.B * a.S_q;
   p.perm_mul = row_permutation_multiplier(p.rows);
   p.wait_ns = 2000000000ull;
+  p.B = a.B;
   p.S_q = a.S_q;
   p.S_k = a.S_k;
   p.H = a.H;
   p.D = a.D;
   p.L = a.L;
   p.dense = a.idx == nullptr;
+  // rows are staged in shared memory when they fit and are 16-byte aligned
+  const bool fits = p.dense ? (size_t)a.L * 4 <= ROW_BYTES : (size_t)a.L * 4 <= ROW_DI_OFF;
+  const bool al = (a.L % 4 == 0) && ((uintptr_t)a.dI % 16 == 0) && (p.dense || (uintptr_t)a.idx % 16 == 0);
+  p.staged = fits && al;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
   gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -711,5 +852,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (a.deterministic) return launch_det_segsum(a, lay, st);
   return cudaSuccess;
 }
+
+#ifdef IBWD_TRACE
+extern "C" __attribute__((visibility("default"))) int ibwd_trace_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+#endif
 
 }  // namespace ibwd
