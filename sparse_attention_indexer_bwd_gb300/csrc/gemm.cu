@@ -152,7 +152,8 @@ struct Ctx {
 // first CTAs), compiled only with -DIBWD_TRACE for pipeline analysis.
 enum TraceEv {
   EV_SCAN_PUB, EV_GATHER_ISSUED, EV_MMA_KFULL, EV_MMA_Z, EV_MMA_DZFULL, EV_MMA_DKEMPTY, EV_MMA_DKDQ,
-  EV_DZ_ZFULL, EV_DZ_DONE, EV_DK_FULL, EV_DK_DONE, EV_Q_READY, EV_COUNT
+  EV_DZ_ZFULL, EV_DZ_DONE, EV_DK_FULL, EV_DK_DONE, EV_Q_READY, EV_MMA_MFULL, EV_MMA_QFULL, EV_GATHER_KEMPTY,
+  EV_DZ_DZEMPTY, EV_DZW0, EV_COUNT = EV_DZW0 + 8
 };
 #ifdef IBWD_TRACE
 constexpr int TRACE_CTAS = 4, TRACE_TILES = 256;
@@ -168,6 +169,8 @@ __device__ unsigned long long g_trace[TRACE_CTAS][EV_COUNT][TRACE_TILES];
 #endif
 
 #define WAIT(bar, par) mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns)
+// Warp-uniform form for the MMA warp, which must stay converged (elect.sync).
+#define WAITW(bar, par) __all_sync(0xffffffffu, WAIT(bar, par))
 
 // A bounded wait that ignores the abort flag: used only to drain work that
 // was already issued before the kernel may exit.
@@ -369,6 +372,7 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
     const long long b = M.r / p.S_q;
     const int st = g % KST;
     if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) break;
+    if (x == 0) TRACE(EV_GATHER_KEMPTY, g);
     const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES + dst_off;
     const __half* kb = p.k16 + b * (p.S_k + 1) * kDP + ch * 8;
     int key[kBM / 8];
@@ -388,93 +392,93 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------ MMA ---
+// The MMA warp runs its loop with all 32 lanes (waits and descriptor math are
+// warp-uniform, so operands stay in uniform registers); an elected lane issues
+// each tcgen05.mma and commit.
 constexpr uint32_t ID_Z = idesc_f16_f32(128, 64, 0, 0);    // Z^T = K . Q^T
 constexpr uint32_t ID_DKT = idesc_f16_f32(128, 128, 1, 0);  // dK^T = Q^T . dz^T (Q as MN-major A)
 constexpr uint32_t ID_DQ = idesc_f16_f32(128, 64, 1, 1);   // dQ^T = K^T . dz (both MN-major)
 
+// Descriptors are built once per operand buffer; a k-step advances the start
+// address field (address >> 4, 14 bits: shared memory stays below 256 KB, so
+// the addition never carries out of the field).
 __device__ __forceinline__ void mma_z(const Ctx& cx, int g, int qb) {
-  const uint32_t ka = cx.sbase + OFF_K + (g % KST) * KTILE_BYTES;
-  const uint32_t qa = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+  const uint64_t a0 = sw128_desc(cx.sbase + OFF_K + (g % KST) * KTILE_BYTES, 16, 1024);
+  const uint64_t b0 = sw128_desc(cx.sbase + OFF_Q + qb * QTILE_BYTES, 16, 1024);
   const uint32_t d = cx.tmem + TM_Z + (g & 1) * 64;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // K = D = 128 in steps of 16
-    const uint64_t ad = sw128_desc(ka + (k >> 2) * KHALF_BYTES + (k & 3) * 32, 16, 1024);
-    const uint64_t bd = sw128_desc(qa + (k >> 2) * QHALF_BYTES + (k & 3) * 32, 16, 1024);
-    umma_f16(d, ad, bd, ID_Z, k > 0);
-  }
+  for (int k = 0; k < 8; ++k)  // K = D = 128 in steps of 16
+    umma_f16_elect(d, a0 + (((k >> 2) * KHALF_BYTES + (k & 3) * 32) >> 4),
+                   b0 + (((k >> 2) * QHALF_BYTES + (k & 3) * 32) >> 4), ID_Z, k > 0);
 }
 
 __device__ __forceinline__ void mma_dk(const Ctx& cx, int g, int qb) {
-  const uint32_t za = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES;
-  const uint32_t qa = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+  const uint64_t a0 = sw128_desc(cx.sbase + OFF_Q + qb * QTILE_BYTES, QHALF_BYTES, 1024);  // Q^T: M = d, MN-major
+  const uint64_t b0 = sw128_desc(cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES, 16, 1024);    // dz^T: N = s, K-major
   const uint32_t d = cx.tmem + TM_DK + (g & 1) * 128;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {  // K = H = 64 in steps of 16
-    const uint64_t ad = sw128_desc(qa + k * 2048, QHALF_BYTES, 1024);  // Q^T: M = d, MN-major
-    const uint64_t bd = sw128_desc(za + k * 32, 16, 1024);             // dz^T: N = s, K-major
-    umma_f16(d, ad, bd, ID_DKT, k > 0);
-  }
+  for (int k = 0; k < 4; ++k)  // K = H = 64 in steps of 16
+    umma_f16_elect(d, a0 + ((k * 2048) >> 4), b0 + ((k * 32) >> 4), ID_DKT, k > 0);
 }
 
 __device__ __forceinline__ void mma_dq(const Ctx& cx, int g, int qd, bool first) {
-  const uint32_t ka = cx.sbase + OFF_K + (g % KST) * KTILE_BYTES;
-  const uint32_t za = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES;
+  const uint64_t a0 = sw128_desc(cx.sbase + OFF_K + (g % KST) * KTILE_BYTES, KHALF_BYTES, 1024);
+  const uint64_t b0 = sw128_desc(cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES, DZTILE_BYTES, 1024);
   const uint32_t d = cx.tmem + TM_DQ + qd * 64;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {  // K = 128 keys in steps of 16
-    const uint64_t ad = sw128_desc(ka + k * 2048, KHALF_BYTES, 1024);
-    const uint64_t bd = sw128_desc(za + k * 2048, DZTILE_BYTES, 1024);
-    umma_f16(d, ad, bd, ID_DQ, (first && k == 0) ? 0u : 1u);
-  }
+  for (int k = 0; k < 8; ++k)  // K = 128 keys in steps of 16
+    umma_f16_elect(d, a0 + ((k * 2048) >> 4), b0 + ((k * 2048) >> 4), ID_DQ, (first && k == 0) ? 0u : 1u);
 }
 
 __device__ void mma_role(const KParams& p, const Ctx& cx) {
   Bars* B = cx.bars;
   int g = 0;
   long long iq = 0;
-  if (!WAIT(&B->mfull[0], 0)) goto drain;
+  if (!WAITW(&B->mfull[0], 0)) goto drain;
   {
     int flags = cx.meta[0].flags;
-    if (!WAIT(&B->qfull[0], 0) || !WAIT(&B->kfull[0], 0)) goto drain;
+    if (!WAITW(&B->qfull[0], 0) || !WAITW(&B->kfull[0], 0)) goto drain;
     // the key tile was written by cp.async (generic proxy): order it before
     // the tensor core's reads
     fence_proxy_async_smem();
     tc_fence_after();
     mma_z(cx, 0, 0);
-    umma_commit(&B->zfull[0]);
+    umma_commit_elect(&B->zfull[0]);
     for (;;) {
       int nflags = 0;
       long long niq = iq;
       if (!(flags & F_END)) {
         // look ahead: Z of tile g+1 overlaps the dz work of tile g
         const int g1 = g + 1;
-        if (!WAIT(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) goto drain;
+        if (!WAITW(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) goto drain;
+        TRACE(EV_MMA_MFULL, g1);
         nflags = cx.meta[g1 % MST].flags;
         if (nflags & F_FIRST) {
           niq = iq + 1;
-          if (!WAIT(&B->qfull[niq & 1], (uint32_t)((niq >> 1) & 1))) goto drain;
+          if (!WAITW(&B->qfull[niq & 1], (uint32_t)((niq >> 1) & 1))) goto drain;
+          TRACE(EV_MMA_QFULL, g1);
         }
-        if (!WAIT(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1))) goto drain;
+        if (!WAITW(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1))) goto drain;
         TRACE(EV_MMA_KFULL, g1);
-        if (!WAIT(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1))) goto drain;
+        if (!WAITW(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1))) goto drain;
         fence_proxy_async_smem();
         tc_fence_after();
         mma_z(cx, g1, (int)(niq & 1));
         TRACE(EV_MMA_Z, g1);
-        umma_commit(&B->zfull[g1 & 1]);
+        umma_commit_elect(&B->zfull[g1 & 1]);
       }
-      if (!WAIT(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
+      if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
       TRACE(EV_MMA_DZFULL, g);
-      if (!WAIT(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
+      if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
       TRACE(EV_MMA_DKEMPTY, g);
-      if ((flags & F_FIRST) && !WAIT(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
+      if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
       tc_fence_after();
       mma_dk(cx, g, (int)(iq & 1));
-      umma_commit(&B->dkfull[g & 1]);
+      umma_commit_elect(&B->dkfull[g & 1]);
       mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
-      umma_commit(&B->kempty[g % KST]);
-      umma_commit(&B->dzempty[g & 1]);
-      if (flags & F_LAST) umma_commit(&B->dqfull[iq & 1]);
+      umma_commit_elect(&B->kempty[g % KST]);
+      umma_commit_elect(&B->dzempty[g & 1]);
+      if (flags & F_LAST) umma_commit_elect(&B->dqfull[iq & 1]);
       TRACE(EV_MMA_DKDQ, g);
       if (flags & F_END) break;
       ++g;
@@ -484,7 +488,8 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
   }
 drain:
   // every MMA issued so far completes before TMEM can be released
-  umma_commit(&B->drain);
+  __syncwarp();
+  umma_commit_elect(&B->drain);
   drain_wait(&B->drain, 0, p);
 }
 
@@ -540,6 +545,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
     if (tdz == 0) TRACE(EV_DZ_ZFULL, g);
     if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
+    if (tdz == 0) TRACE(EV_DZ_DZEMPTY, g);
     tc_fence_after();
     const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
     const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
@@ -569,6 +575,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
     if (tdz == 0) TRACE(EV_DZ_DONE, g);
+    if ((tdz & 31) == 0) TRACE(EV_DZW0 + (tdz >> 5), g);
     if ((flags & F_FIRST) && ep_r >= 0) {
       dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
       ep_r = -1;
@@ -715,8 +722,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   } else if (warp == W_SCAN) {
     scan_role(p, cx);
   } else if (warp == W_MMA) {
-    if ((threadIdx.x & 31) == 0) mma_role(p, cx);
-    __syncwarp();
+    mma_role(p, cx);  // the whole warp runs the loop; one elected lane issues
   } else if (warp < W_DZ0) {
     q_role(p, cx);
   } else if (warp < W_DK0) {
