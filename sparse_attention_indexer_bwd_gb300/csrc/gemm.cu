@@ -503,7 +503,7 @@ __device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int
   const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + hg * 32;
   float v[32];
   tmem_ld32(ta, v);
-  tmem_wait_ld();
+  tmem_wait_ld_dep(v);
   tc_fence_before();
   mbar_arrive(&cx.bars->dqempty[iq & 1]);
   const float sc = pow2f(-c);
@@ -551,7 +551,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
     float z[32];
     tmem_ld32(za, z);
-    tmem_wait_ld();
+    tmem_wait_ld_dep(z);
     tc_fence_before();
     mbar_arrive(&cx.bars->zempty[g & 1]);
 #pragma unroll
@@ -639,7 +639,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
       if (ch * 32 >= count) break;  // uniform: the remaining rows are padding
       float v[32];
       tmem_ld32(ta + ch * 32, v);
-      tmem_wait_ld();
+      tmem_wait_ld_dep(v);
 #pragma unroll
       for (int j4 = 0; j4 < 8; ++j4) {
         const int4 id4 = *reinterpret_cast<const int4*>(ids + ch * 32 + j4 * 4);
