@@ -121,6 +121,31 @@ IBWD_API int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const 
                            float* dq, float* dw, float* dk, int B, int S, int H, int D,
                            int dk_mode, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Gemm stage without any allocation (the pages have no counterpart: this is a
+ * service of this library).  Same computation, arguments and outputs as
+ * indexer_bwd_gemm in IBWD_DK_ATOMIC mode (dk accumulates; zero it first),
+ * but it takes no workspace and never calls cudaMalloc, cudaFree or any other
+ * allocating routine.  It is meant for callers that cannot allocate device
+ * memory where they run the backward: code running inside a memory
+ * allocator or pool callback, runtimes that hand out all device memory up
+ * front, and launch paths that must not synchronize the device.
+ *  - Its scratch (the fp16 copy of k) is a fixed 8 MiB array inside the
+ *    library, held by every GPU that loads it until the process exits, so
+ *    B * (S_k + 1) <= 32768; larger shapes return IBWD_ERR_UNSUPPORTED before
+ *    anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the one array: calls that overlap on the GPU (two
+ *    streams, or two host threads) race and corrupt each other's results.
+ *    Each call rewrites the array before reading it.
+ *  - A kernel wait that times out is recorded in a status word of this entry
+ *    point, not in the one indexer_bwd_last_device_status reports.
+ */
+IBWD_API int indexer_bwd_gemm_noalloc(const uint16_t* q, const uint16_t* k, const float* w, const float* dI,
+                             const int32_t* topk_idx, float* dq, float* dw, float* dk, int B, int S_q,
+                             int S_k, int H, int D, int topk, void* stream);
+
 /* Synchronizes `stream`, then reads and clears this device's status word:
  * IBWD_ERR_TIMEOUT if a kernel's bounded wait expired, IBWD_ERR_BAD_INDEX if a
  * device bounds check failed, IBWD_ERR_CUDA if the stream reports an error,

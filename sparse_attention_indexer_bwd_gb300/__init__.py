@@ -38,6 +38,7 @@ EXPORTS = (
     "indexer_bwd_dense_gemm",
     "indexer_bwd_last_device_status",
     "indexer_bwd_status_string",
+    "indexer_bwd_gemm_noalloc",
 )
 
 
