@@ -30,7 +30,7 @@
 // dK is produced transposed (TMEM lane = column d), so that in the epilogue
 // each warp instruction reduces one whole 128-byte line of a dK row.
 //
-// Warp roles (20 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
+// Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
 //   0-3   gather: 16 cp.async per thread per tile (selected fp16 key rows)
 //   4     scan: row idx/dI staged in shared memory by bulk copies (one row
 //         ahead); valid count, max|dI| and scale; compaction into tile
@@ -40,9 +40,10 @@
 //   8-11  dz group for heads 0-31, 12-15 dz group for heads 32-63: Z from
 //         TMEM -> dW partial sums in registers, dz -> fp16 shared tile; at row
 //         end the dW reduction; one row later the dQ epilogue (TMEM -> fp32)
-//   16-19 dK group: dK^T tile from TMEM -> fp32 red.global.add (one 128-byte
-//         line per warp instruction) into dk, or plain stores into the
-//         per-slot workspace in deterministic mode
+//   16-19 dK group for tile rows 0-63, 20-23 dK group for rows 64-127: dK^T
+//         tile from TMEM -> fp32 red.global.add (one 128-byte line per warp
+//         instruction) into dk, or plain stores into the per-slot workspace in
+//         deterministic mode
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
 #include <algorithm>
@@ -55,11 +56,12 @@ namespace {
 
 constexpr int KST = 3;  // K-tile stages
 constexpr int MST = 4;  // tile-metadata ring
-constexpr int NTHREADS = 640;
+constexpr int NTHREADS = 768;
 constexpr int W_GATHER0 = 0, W_SCAN = 4, W_MMA = 5, W_Q0 = 6, W_DZ0 = 8, W_DK0 = 16;
 constexpr int NGT = 128;                  // gather threads
 constexpr int NQT = 64;                   // Q-loader threads
 constexpr int NDZT = 256;                 // dz threads (two groups of 128)
+constexpr int NDKT = 256;                 // dK threads (two groups of 128)
 constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI (sparse) or dI (dense)
 constexpr uint32_t ROW_DI_OFF = 8192;     // dI offset inside a staged sparse row
 
@@ -501,18 +503,25 @@ __device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int
   if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return;
   tc_fence_after();
   const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + hg * 32;
-  float v[32];
-  tmem_ld32(ta, v);
-  tmem_wait_ld_dep(v);
-  tc_fence_before();
-  mbar_arrive(&cx.bars->dqempty[iq & 1]);
   const float sc = pow2f(-c);
   const int d = qw * 32 + lane;  // TMEM lane = column of dQ
-  if (d < p.D) {
-    float* dst = p.dq + (long long)r * p.H * p.D + d;
+  float* dst = p.dq + (long long)r * p.H * p.D + d;
 #pragma unroll
-    for (int h = 0; h < 32; ++h)
-      if (hg * 32 + h < p.H) dst[(long long)(hg * 32 + h) * p.D] = v[h] * sc;
+  for (int half = 0; half < 2; ++half) {
+    float v[16];
+    tmem_ld16(ta + half * 16, v);
+    tmem_wait_ld_dep16(v);
+    if (half == 1) {
+      tc_fence_before();
+      mbar_arrive(&cx.bars->dqempty[iq & 1]);
+    }
+    if (d < p.D) {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const int hh = hg * 32 + half * 16 + h;
+        if (hh < p.H) dst[(long long)hh * p.D] = v[h] * sc;
+      }
+    }
   }
 }
 
@@ -549,18 +558,22 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     tc_fence_after();
     const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
     const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
-    float z[32];
-    tmem_ld32(za, z);
-    tmem_wait_ld_dep(z);
-    tc_fence_before();
-    mbar_arrive(&cx.bars->zempty[g & 1]);
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
+    for (int zh = 0; zh < 2; ++zh) {
+    float z[16];
+    tmem_ld16(za + zh * 16, z);
+    tmem_wait_ld_dep16(z);
+    if (zh == 1) {
+      tc_fence_before();
+      mbar_arrive(&cx.bars->zempty[g & 1]);
+    }
+#pragma unroll
+    for (int c8 = zh * 2; c8 < zh * 2 + 2; ++c8) {
       uint32_t pk[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int h0 = c8 * 8 + e * 2;
-        const float z0 = z[h0], z1 = z[h0 + 1];
+        const float z0 = z[h0 - zh * 16], z1 = z[h0 + 1 - zh * 16];
         const uint64_t dw = mul_f32x2(dis2, w2[h0 >> 1]);
         const bool p0 = z0 > 0.f, p1 = z1 > 0.f;
         if (p0) acc[h0] = fmaf(dis, z0, acc[h0]);
@@ -571,6 +584,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
       }
       const int chunk = hg * 4 + c8;  // 16-byte chunk of the 128-byte dz row
       st_shared_v4(dzrow + ((chunk ^ (s & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+    }
     }
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
@@ -619,6 +633,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
 // 32 consecutive floats (one 128-byte line) of one dK row.
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int kg = (threadIdx.x - W_DK0 * 32) >> 7;  // group: tile rows 64*kg .. 64*kg+63
   const int d = qw * 32 + lane;
   const bool don = d < p.D;
   for (int g = 0;; ++g) {
@@ -635,7 +650,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
     const float sc = pow2f(-c);
     const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK + (uint32_t)(g & 1) * 128;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = kg * 2; ch < kg * 2 + 2; ++ch) {
       if (ch * 32 >= count) break;  // uniform: the remaining rows are padding
       float v[32];
       tmem_ld32(ta + ch * 32, v);
@@ -689,7 +704,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
     }
     for (int i = 0; i < MST; ++i) {
       mbar_init(&B->mfull[i], 32);
-      mbar_init(&B->mempty[i], 128);
+      mbar_init(&B->mempty[i], NDKT);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->rowfull[i], 1);
@@ -699,7 +714,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
       mbar_init(&B->dzfull[i], NDZT);
       mbar_init(&B->dzempty[i], 1);
       mbar_init(&B->dkfull[i], 1);
-      mbar_init(&B->dkempty[i], 128);
+      mbar_init(&B->dkempty[i], NDKT);
       mbar_init(&B->dqfull[i], 1);
       mbar_init(&B->dqempty[i], NDZT);
       mbar_init(&B->dwred[i], NDZT);

@@ -148,6 +148,15 @@ __device__ __forceinline__ void tmem_wait_ld_dep(float (&v)[32]) {
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_wait_ld_dep16(float (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]),
+                 "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
+                 "+f"(v[15])
+               :
+               : "memory");
+}
+
 // 32 lanes x 32 bit, 16 consecutive columns: thread i gets lane (base + i).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
