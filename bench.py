@@ -35,6 +35,35 @@ import synth  # noqa: E402
 
 METRIC = "indexer-bwd kernel µs & TFLOP/s (frac of bf16 peak), H64 D128 Sq8192 topk1024"
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the anchor workload in atomic mode, kept with the hash of the
+# kernel sources it was taken on; any change to those sources makes it stale
+# and the benchmark then reports null.  The capture and its command are
+# summarised under profiles/.
+PROFILED_SOURCES = "9eab5226006acaa5c38fa62e7a91901bb7d9842f08f051a37765383719038860"
+PROFILED_TRAFFIC = {
+    ("anchor", "atomic"): {"gemm_stage": 206.737408e6 + 222.362112e6 + 1.058560e6,  # gemm_kernel + k_to_f16
+                           "score_grad": 100.711936e6 + 4.698112e6},
+}
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "sparse_attention_indexer_bwd_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str, mode: str) -> dict:
+    if kernel_sources_hash() != PROFILED_SOURCES:
+        return {}
+    return PROFILED_TRAFFIC.get((workload, mode), {})
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -358,6 +387,7 @@ def run_ours(args, wl):
 
     if rank != 0:
         return
+    traffic = profiled_traffic(wl.name, args.mode)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -372,12 +402,13 @@ def run_ours(args, wl):
         "kernels_us": {"score_grad": 1e3 * sg_avg, "gemm_stage": 1e3 * gm_avg},
         "score_grad_gbs": sg_bytes / (sg_avg * 1e-3) / 1e9,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                     "frac": achieved / pk["bf16_tflops"], "traffic": traffic.get("gemm_stage"),
                      "note": f"gemm-stage call (fp16 copy of k + main kernel), nominal 6*S_q*topk*H*D FLOP; "
                              f"peak = {pk['src']} dense bf16 burst (fp16 dense rate is the same)"},
         "roofline_score_grad": {"bound": "hbm", "achieved": sg_bytes / (sg_avg * 1e-3) / 1e9,
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                "frac": sg_bytes / (sg_avg * 1e-3) / 1e9 / pk["hbm_gbs"], "traffic": None},
+                                "frac": sg_bytes / (sg_avg * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                "traffic": traffic.get("score_grad"), "algorithmic_bytes": sg_bytes},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,
