@@ -55,7 +55,7 @@ namespace ibwd {
 namespace {
 
 constexpr int KST = 3;  // K-tile stages
-constexpr int MST = 4;  // tile-metadata ring
+constexpr int MST = 8;  // tile-metadata ring (deep enough to hide the per-row scan)
 constexpr int NTHREADS = 768;
 constexpr int W_GATHER0 = 0, W_SCAN = 4, W_MMA = 5, W_Q0 = 6, W_DZ0 = 8, W_DK0 = 16;
 constexpr int NGT = 128;                  // gather threads
@@ -155,17 +155,39 @@ struct Ctx {
 enum TraceEv {
   EV_SCAN_PUB, EV_GATHER_ISSUED, EV_MMA_KFULL, EV_MMA_Z, EV_MMA_DZFULL, EV_MMA_DKEMPTY, EV_MMA_DKDQ,
   EV_DZ_ZFULL, EV_DZ_DONE, EV_DK_FULL, EV_DK_DONE, EV_Q_READY, EV_MMA_MFULL, EV_MMA_QFULL, EV_GATHER_KEMPTY,
-  EV_DZ_DZEMPTY, EV_DZW0, EV_COUNT = EV_DZW0 + 8
+  EV_DZ_DZEMPTY, EV_DZW0, EV_DK_LD = EV_DZW0 + 8, EV_COUNT
 };
 #ifdef IBWD_TRACE
 constexpr int TRACE_CTAS = 4, TRACE_TILES = 256;
 __device__ unsigned long long g_trace[TRACE_CTAS][EV_COUNT][TRACE_TILES];
+// per CTA (first 1024): clock64 and %globaltimer at the start and at the
+// end, %smid, tiles processed
+constexpr int TRACE_ALL = 1024;
+__device__ unsigned long long g_trace_cta[TRACE_ALL][6];
+__device__ __forceinline__ unsigned long long trace_gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+#define TRACE_CTA(i)                                                   \
+  do {                                                                 \
+    if (blockIdx.x < TRACE_ALL && threadIdx.x == 0) {                  \
+      g_trace_cta[blockIdx.x][(i)*2] = clock64();                      \
+      g_trace_cta[blockIdx.x][(i)*2 + 1] = trace_gtime();              \
+      unsigned smid;                                                   \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));                \
+      g_trace_cta[blockIdx.x][4] = smid;                               \
+    }                                                                  \
+  } while (0)
 #define TRACE(ev, g)                                                                    \
   do {                                                                                  \
     if (blockIdx.x < TRACE_CTAS && (g) >= 0 && (g) < TRACE_TILES) g_trace[blockIdx.x][ev][g] = clock64(); \
   } while (0)
 #else
 #define TRACE(ev, g) \
+  do {               \
+  } while (0)
+#define TRACE_CTA(i) \
   do {               \
   } while (0)
 #endif
@@ -487,6 +509,9 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
       flags = nflags;
       iq = niq;
     }
+#ifdef IBWD_TRACE
+    if (blockIdx.x < TRACE_ALL && (threadIdx.x & 31) == 0) g_trace_cta[blockIdx.x][5] = (unsigned long long)g + 1;
+#endif
   }
 drain:
   // every MMA issued so far completes before TMEM can be released
@@ -631,6 +656,38 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
 // TMEM holds dK^T: lane = column d, TMEM column = tile row.  Thread d of the
 // group reduces element d of every valid row, so each warp instruction covers
 // 32 consecutive floats (one 128-byte line) of one dK row.
+// One 32-row chunk of the transposed dK tile: v holds column d of the chunk's
+// rows.  Ids are read 16 at a time into registers and the mode is fixed at
+// compile time, so the reductions (or stores) issue back to back with no
+// load or branch between them.
+template <bool RED>
+__device__ __forceinline__ void dk_chunk(float* base, const int* ids, const float (&v)[32], int nrow, float sc,
+                                         int D) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    int idv[16];
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const int4 t = *reinterpret_cast<const int4*>(ids + hf * 16 + j4 * 4);
+      idv[j4 * 4] = t.x;
+      idv[j4 * 4 + 1] = t.y;
+      idv[j4 * 4 + 2] = t.z;
+      idv[j4 * 4 + 3] = t.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      if (hf * 16 + e < nrow) {
+        float* dst = base + (long long)idv[e] * D;
+        const float val = v[hf * 16 + e] * sc;
+        if (RED)
+          asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(val));
+        else
+          *dst = val;
+      }
+    }
+  }
+}
+
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int kg = (threadIdx.x - W_DK0 * 32) >> 7;  // group: tile rows 64*kg .. 64*kg+63
@@ -655,22 +712,13 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
       float v[32];
       tmem_ld32(ta + ch * 32, v);
       tmem_wait_ld_dep(v);
-#pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
-        const int4 id4 = *reinterpret_cast<const int4*>(ids + ch * 32 + j4 * 4);
-        const int idv[4] = {id4.x, id4.y, id4.z, id4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = ch * 32 + j4 * 4 + e;
-          if (row < count && don) {
-            float* dst = base + (long long)idv[e] * p.D;
-            const float val = v[j4 * 4 + e] * sc;
-            if (p.u)
-              *dst = val;
-            else
-              asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(val) : "memory");
-          }
-        }
+      if (threadIdx.x == W_DK0 * 32 && ch == 0) TRACE(EV_DK_LD, g);
+      const int nrow = min(32, count - ch * 32);
+      if (don) {
+        if (p.u)
+          dk_chunk<false>(base, ids + ch * 32, v, nrow, sc, p.D);
+        else
+          dk_chunk<true>(base, ids + ch * 32, v, nrow, sc, p.D);
       }
     }
     tc_fence_before();
@@ -731,6 +779,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   __syncthreads();
   tc_fence_after();
   cx.tmem = *tmem_slot;
+  TRACE_CTA(0);
 
   if (warp < W_SCAN) {
     gather_role(p, cx);
@@ -750,6 +799,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   __syncthreads();
   tc_fence_after();
   if (warp == W_MMA) tmem_dealloc(cx.tmem, TM_COLS);
+  TRACE_CTA(1);
 }
 
 // k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
@@ -877,6 +927,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
 #ifdef IBWD_TRACE
 extern "C" __attribute__((visibility("default"))) int ibwd_trace_read(void* host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+extern "C" __attribute__((visibility("default"))) int ibwd_trace_cta_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_trace_cta, bytes < sizeof(g_trace_cta) ? bytes : sizeof(g_trace_cta));
 }
 #endif
 
