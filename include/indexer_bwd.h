@@ -80,10 +80,12 @@ IBWD_API int indexer_bwd_score_grad(const float* index_score, float* attn_score,
                            int B, int S_q, int S_k, int topk, float grad_scale, float* dk_to_zero,
                            int D, void* stream);
 
-/* Bytes of device workspace indexer_bwd_gemm needs (always > 0: it holds an
- * fp16 copy of k, 256 bytes per key row plus one zero row per batch; the
- * deterministic mode adds the per-slot dK rows, 4*D bytes per slot, and the
- * key sort).  0 for unsupported arguments. */
+/* Bytes of device workspace indexer_bwd_gemm needs (always > 0: a 256-byte
+ * block for the kernel's row counter and an fp16 copy of k, 256 bytes per key
+ * row plus one zero row per batch; the deterministic mode adds the per-slot
+ * dK rows, 4*D bytes per slot, and the key sort).  The workspace is rewritten
+ * by every call: calls that may overlap on the GPU need separate workspaces.
+ * 0 for unsupported arguments. */
 IBWD_API size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk,
                                        int dk_mode);
 

@@ -56,6 +56,7 @@ namespace {
 
 constexpr int KST = 3;  // K-tile stages
 constexpr int MST = 8;  // tile-metadata ring (deep enough to hide the per-row scan)
+constexpr int RQ = 16;  // row-order ring: the scan runs at most ~MST + 2 rows ahead of the Q loader
 constexpr int NTHREADS = 768;
 constexpr int W_GATHER0 = 0, W_SCAN = 4, W_MMA = 5, W_Q0 = 6, W_DZ0 = 8, W_DK0 = 16;
 constexpr int NGT = 128;                  // gather threads
@@ -92,6 +93,7 @@ struct Bars {
   uint64_t dkfull[2], dkempty[2];
   uint64_t dqfull[2], dqempty[2];
   uint64_t dwred[2];
+  uint64_t rowid[RQ];
   uint64_t drain;
 };
 
@@ -103,7 +105,8 @@ constexpr uint32_t OFF_META = OFF_ROW + 2 * ROW_BYTES;
 constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
 constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
 constexpr uint32_t OFF_BARS = OFF_RED + 2 * 4 * kHP * 4;  // [2][4 warps][64 heads]
-constexpr uint32_t OFF_MISC = OFF_BARS + sizeof(Bars);
+constexpr uint32_t OFF_ROWQ = OFF_BARS + sizeof(Bars);  // int[RQ]: rows in this CTA's order, -1 = end
+constexpr uint32_t OFF_MISC = OFF_ROWQ + RQ * 4;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(OFF_BARS % 8 == 0 && OFF_ROW % 16 == 0, "alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -118,6 +121,7 @@ struct KParams {
   float* dw;
   float* dk;
   float* u;  // deterministic per-slot rows, or nullptr
+  unsigned* sched;  // row counter in the workspace, zeroed by k_to_f16_kernel
   unsigned* status;
   long long rows;
   unsigned long long perm_mul;
@@ -147,7 +151,7 @@ struct Ctx {
   Bars* bars;
   volatile int* abort;
   uint32_t tmem;
-  long long nq;
+  int* rowq;
 };
 
 // Optional per-tile timeline (clock64 stamps of each role's progress in the
@@ -206,12 +210,15 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
 // ------------------------------------------------------------ Q loader ----
 __device__ void q_role(const KParams& p, const Ctx& cx) {
   const int tid = threadIdx.x - W_Q0 * 32;  // 0..63
-  for (long long i = 0; i < cx.nq; ++i) {
+  for (long long i = 0;; ++i) {
     const int qb = (int)(i & 1);
+    // the scan publishes the CTA's rows in order; -1 ends the list
+    if (!WAIT(&cx.bars->rowid[i % RQ], (uint32_t)((i / RQ) & 1))) return;
+    const long long r = cx.rowq[i % RQ];
+    if (r < 0) return;
     // buffer qb was last used by row i-2: all its MMAs and dz reads are done
     // once that row's dQ accumulator is complete
     if (i >= 2 && !WAIT(&cx.bars->dqfull[qb], (uint32_t)(((i - 2) >> 1) & 1))) return;
-    const long long r = row_of(blockIdx.x + i * gridDim.x, p);
     const uint16_t* qr = p.q + r * p.H * p.D;
     const uint32_t qs = cx.sbase + OFF_Q + qb * QTILE_BYTES;
 #pragma unroll
@@ -262,8 +269,23 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
   const uint32_t lt_mask = (1u << lane) - 1u;
   uint8_t* rowbuf = cx.smem + OFF_ROW;
   long long staged_wait = -1;  // last row whose bulk copy was issued but not yet waited for
-  auto issue_row = [&](long long i) {
-    const long long r = row_of(blockIdx.x + i * gridDim.x, p);
+  // The CTA's first row is blockIdx.x (the grid never exceeds the row
+  // count); later rows are claimed from the shared counter, so CTAs that run
+  // faster take more rows.  Row numbers go through the permutation.
+  auto claim = [&]() -> long long {
+    unsigned v = 0;
+    if (lane == 0) v = atomicAdd(p.sched, 1u);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    const long long u = (long long)gridDim.x + v;
+    return u < p.rows ? row_of(u, p) : -1;
+  };
+  auto publish_row = [&](long long i, long long r) {
+    if (lane == 0) {
+      cx.rowq[i % RQ] = (int)r;
+      mbar_arrive(&cx.bars->rowid[i % RQ]);
+    }
+  };
+  auto issue_row = [&](long long i, long long r) {
     const int t = (int)(r % p.S_q);
     const int buf = (int)(i & 1);
     if (lane == 0) {
@@ -285,10 +307,15 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
   };
 
   int g = 0;
-  if (p.staged) issue_row(0);
-  for (long long i = 0; i < cx.nq; ++i) {
-    const long long r = row_of(blockIdx.x + i * gridDim.x, p);
+  long long r_next = row_of(blockIdx.x, p);
+  publish_row(0, r_next);
+  if (p.staged) issue_row(0, r_next);
+  for (long long i = 0;; ++i) {
+    const long long r = r_next;
     const int t = (int)(r % p.S_q);
+    r_next = claim();
+    publish_row(i + 1, r_next);
+    const bool last = r_next < 0;
     RowSrc src;
     src.S_k = p.S_k;
     src.Lr = p.dense ? min(p.L, t + 1) : p.L;
@@ -297,7 +324,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       if (!WAIT(&cx.bars->rowfull[buf], (uint32_t)((i >> 1) & 1))) goto done;
       staged_wait = -1;
       __syncwarp();
-      if (i + 1 < cx.nq) issue_row(i + 1);
+      if (!last) issue_row(i + 1, r_next);
       const uint8_t* rb = rowbuf + buf * ROW_BYTES;
       src.idx = p.dense ? nullptr : reinterpret_cast<const int32_t*>(rb);
       src.dI = reinterpret_cast<const float*>(rb + (p.dense ? 0 : ROW_DI_OFF));
@@ -365,7 +392,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
           M.count = fill;
           M.c = c;
           M.flags = (tt == 0 ? F_FIRST : 0) | (tt == ntiles - 1 ? F_LAST : 0) |
-                    ((tt == ntiles - 1 && i == cx.nq - 1) ? F_END : 0);
+                    ((tt == ntiles - 1 && last) ? F_END : 0);
         }
         __syncwarp();
         mbar_arrive(&cx.bars->mfull[ms]);
@@ -373,6 +400,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       }
     }
     __syncwarp();
+    if (last) break;
   }
 done:
   // a row copy still in flight must land before the CTA can exit
@@ -741,7 +769,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   cx.bars = reinterpret_cast<Bars*>(smem + OFF_BARS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   cx.abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  cx.nq = (p.rows - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x;
+  cx.rowq = reinterpret_cast<int*>(smem + OFF_ROWQ);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -767,6 +795,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
       mbar_init(&B->dqempty[i], NDZT);
       mbar_init(&B->dwred[i], NDZT);
     }
+    for (int i = 0; i < RQ; ++i) mbar_init(&B->rowid[i], 1);
     mbar_init(&B->drain, 1);
     *cx.abort = 0;
     fence_barrier_init();
@@ -804,7 +833,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
 
 // k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
 // row S_k of each batch zero (padding rows of a tile copy it).
-__global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16, int B, int S_k, int D) {
+__global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16, int B, int S_k, int D,
+                                unsigned* __restrict__ sched) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the gemm kernel's row counter
   const long long rows = (long long)B * (S_k + 1);
   const long long n = rows * (kDP / 8);
   for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < n;
@@ -849,6 +880,8 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
   WsLayout w{};
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
+  w.sched = off;
+  off = up(off + 4);
   w.k16 = off;
   off = up(off + (size_t)B * (S_k + 1) * kDP * 2);
   w.nchunks = 0;
@@ -872,10 +905,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const WsLayout lay = gemm_workspace_layout(a.B, a.S_q, a.S_k, a.H, a.D, a.L, a.deterministic);
   char* ws = static_cast<char*>(a.ws);
   __half* k16 = reinterpret_cast<__half*>(ws + lay.k16);
+  unsigned* sched = reinterpret_cast<unsigned*>(ws + lay.sched);
   {
     const long long n = (long long)a.B * (a.S_k + 1) * (kDP / 8);
     const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * a.num_sms);
-    k_to_f16_kernel<<<blocks, 256, 0, st>>>(a.k, k16, a.B, a.S_k, a.D);
+    k_to_f16_kernel<<<blocks, 256, 0, st>>>(a.k, k16, a.B, a.S_k, a.D, sched);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -901,6 +935,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.dw = a.dw;
   p.dk = a.dk;
   p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
+  p.sched = sched;
   p.status = a.status;
   p.rows = (long long)a.B * a.S_q;
   p.perm_mul = row_permutation_multiplier(p.rows);

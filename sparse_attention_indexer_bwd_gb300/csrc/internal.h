@@ -43,7 +43,8 @@ struct GemmArgs {
 };
 
 struct WsLayout {
-  size_t k16;        // fp16 copy of k, [B, S_k, 128]
+  size_t sched;      // the gemm kernel's row counter (one 256-byte block)
+  size_t k16;        // fp16 copy of k, [B, S_k + 1, 128]
   size_t u;          // deterministic: per-slot dK rows [rows*L, D] fp32
   size_t hist;       // deterministic: per-chunk key counts [nchunks, S_k] int32
   size_t key_start;  // deterministic: CSR offsets [B*S_k + 1] int32

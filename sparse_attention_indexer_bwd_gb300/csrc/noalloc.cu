@@ -17,9 +17,10 @@
 
 namespace {
 
-// Scratch for the fp16 copy of k: 256 bytes per key row plus one zero row per
-// batch, so B * (S_k + 1) <= 32768.
-constexpr size_t kScratchBytes = size_t(8) << 20;
+// Scratch for the gemm kernel's row counter (256 bytes) and the fp16 copy of
+// k (256 bytes per key row plus one zero row per batch), so
+// B * (S_k + 1) <= 32768.
+constexpr size_t kScratchBytes = (size_t(8) << 20) + 256;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 // Device status word of these calls (a wait that timed out sets a bit).
 static __device__ __align__(256) unsigned g_status;

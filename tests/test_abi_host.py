@@ -48,10 +48,10 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     a = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_ATOMIC)
-    assert a == 4097 * 128 * 2                           # fp16 copy of k (+ a zero row)
+    assert a == 256 + 4097 * 128 * 2                     # row counter + fp16 copy of k (+ a zero row)
     d = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_DETERMINISTIC)
     assert d >= a + 8192 * 1024 * 128 * 4 + 8192 * 1024 * 4
-    assert ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 0) == 4097 * 128 * 2
+    assert ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 0) == 256 + 4097 * 128 * 2
     # unsupported shapes report 0
     assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 65, 128, 4, 0) == 0
     assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 4, 12, 4, 0) == 0
