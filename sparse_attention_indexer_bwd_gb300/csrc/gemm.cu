@@ -106,7 +106,8 @@ constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
 constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
 constexpr uint32_t OFF_BARS = OFF_RED + 2 * 4 * kHP * 4;  // [2][4 warps][64 heads]
 constexpr uint32_t OFF_ROWQ = OFF_BARS + sizeof(Bars);  // int[RQ]: rows in this CTA's order, -1 = end
-constexpr uint32_t OFF_MISC = OFF_ROWQ + RQ * 4;
+constexpr uint32_t OFF_DKST = (OFF_ROWQ + RQ * 4 + 15) & ~15u;  // dK transpose stages, 2 KB per dK warp
+constexpr uint32_t OFF_MISC = OFF_DKST + (NDKT / 32) * 16 * 32 * 4;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(OFF_BARS % 8 == 0 && OFF_ROW % 16 == 0, "alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -681,53 +682,54 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------ dK group ----
-// TMEM holds dK^T: lane = column d, TMEM column = tile row.  Thread d of the
-// group reduces element d of every valid row, so each warp instruction covers
-// 32 consecutive floats (one 128-byte line) of one dK row.
-// One 32-row chunk of the transposed dK tile: v holds column d of the chunk's
-// rows.  Ids are read 16 at a time into registers and the mode is fixed at
-// compile time, so the reductions (or stores) issue back to back with no
-// load or branch between them.
+// TMEM holds dK^T: lane = column d, TMEM column = tile row.  A warp holds 32
+// columns (its lane quarter) of 32 tile rows per chunk.  It passes each half
+// chunk through its own 2 KB of shared memory (row-major, 16 rows x 32
+// floats) and reads it back four rows per instruction, so one 16-byte vector
+// reduction per lane covers four 128-byte lines of four dK rows (a quarter of
+// the instructions of one line per row).
 template <bool RED>
 __device__ __forceinline__ void dk_chunk(float* base, const int* ids, const float (&v)[32], int nrow, float sc,
-                                         int D) {
+                                         int D, int dblk, float* stage) {
+  const int lane = threadIdx.x & 31;
+  const int rsub = lane >> 3, c4 = (lane & 7) * 4;  // this lane's row in a group of four, column offset
+  const bool con = dblk + c4 < D;                    // D % 8 == 0: the whole float4 is in range
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
-    int idv[16];
+    if (hf * 16 >= nrow) break;  // uniform
+    int idv[4];
 #pragma unroll
-    for (int j4 = 0; j4 < 4; ++j4) {
-      const int4 t = *reinterpret_cast<const int4*>(ids + hf * 16 + j4 * 4);
-      idv[j4 * 4] = t.x;
-      idv[j4 * 4 + 1] = t.y;
-      idv[j4 * 4 + 2] = t.z;
-      idv[j4 * 4 + 3] = t.w;
-    }
+    for (int k = 0; k < 4; ++k) idv[k] = ids[hf * 16 + rsub + 4 * k];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      if (hf * 16 + e < nrow) {
-        float* dst = base + (long long)idv[e] * D;
-        const float val = v[hf * 16 + e] * sc;
+    for (int e = 0; e < 16; ++e) stage[e * 32 + lane] = v[hf * 16 + e] * sc;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = rsub + 4 * k;
+      if (hf * 16 + e < nrow && con) {
+        const float4 x = *reinterpret_cast<const float4*>(stage + e * 32 + c4);
+        float* dst = base + (long long)idv[k] * D + dblk + c4;
         if (RED)
-          asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(val));
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x), "f"(x.y), "f"(x.z),
+                       "f"(x.w));
         else
-          *dst = val;
+          *reinterpret_cast<float4*>(dst) = x;
       }
     }
+    __syncwarp();  // the stage is rewritten by the next half
   }
 }
 
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
-  const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int qw = (threadIdx.x >> 5) & 3;
   const int kg = (threadIdx.x - W_DK0 * 32) >> 7;  // group: tile rows 64*kg .. 64*kg+63
-  const int d = qw * 32 + lane;
-  const bool don = d < p.D;
+  float* stage = reinterpret_cast<float*>(cx.smem + OFF_DKST) + ((threadIdx.x >> 5) - W_DK0) * (16 * 32);
   for (int g = 0;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
     const TileMeta& M = cx.meta[ms];
     const int flags = M.flags, c = M.c, r = M.r, count = M.count;
-    float* base = p.u ? p.u + (long long)r * p.L * p.D + d
-                      : p.dk + (long long)(r / p.S_q) * p.S_k * p.D + d;
+    float* base = p.u ? p.u + (long long)r * p.L * p.D : p.dk + (long long)(r / p.S_q) * p.S_k * p.D;
     const int* ids = p.u ? M.slot : M.key;
     if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
     if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, g);
@@ -742,12 +744,10 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
       tmem_wait_ld_dep(v);
       if (threadIdx.x == W_DK0 * 32 && ch == 0) TRACE(EV_DK_LD, g);
       const int nrow = min(32, count - ch * 32);
-      if (don) {
-        if (p.u)
-          dk_chunk<false>(base, ids + ch * 32, v, nrow, sc, p.D);
-        else
-          dk_chunk<true>(base, ids + ch * 32, v, nrow, sc, p.D);
-      }
+      if (p.u)
+        dk_chunk<false>(base, ids + ch * 32, v, nrow, sc, p.D, qw * 32, stage);
+      else
+        dk_chunk<true>(base, ids + ch * 32, v, nrow, sc, p.D, qw * 32, stage);
     }
     tc_fence_before();
     mbar_arrive(&cx.bars->dkempty[g & 1]);
