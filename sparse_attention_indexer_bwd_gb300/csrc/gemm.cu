@@ -273,12 +273,19 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
   // The CTA's first row is blockIdx.x (the grid never exceeds the row
   // count); later rows are claimed from the shared counter, so CTAs that run
   // faster take more rows.  Row numbers go through the permutation.
-  auto claim = [&]() -> long long {
-    unsigned v = 0;
-    if (lane == 0) v = atomicAdd(p.sched, 1u);
-    v = __shfl_sync(0xffffffffu, v, 0);
+  // A claim is issued at the start of a row and resolved after that row's
+  // first pass, so the atomic's round trip overlaps the pass.
+  auto claim_issue = [&]() -> unsigned { return lane == 0 ? atomicAdd(p.sched, 1u) : 0u; };
+  auto claim_resolve = [&](unsigned pend) -> long long {
+    const unsigned v = __shfl_sync(0xffffffffu, pend, 0);
     const long long u = (long long)gridDim.x + v;
     return u < p.rows ? row_of(u, p) : -1;
+  };
+  // |w| of a row, loaded early (two heads per lane, H <= 64) and reduced
+  // when the row is scanned
+  auto w_load = [&](long long r, float& w0, float& w1) {
+    w0 = lane < p.H ? __ldg(p.w + r * p.H + lane) : 0.f;
+    w1 = lane + 32 < p.H ? __ldg(p.w + r * p.H + lane + 32) : 0.f;
   };
   auto publish_row = [&](long long i, long long r) {
     if (lane == 0) {
@@ -311,12 +318,14 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
   long long r_next = row_of(blockIdx.x, p);
   publish_row(0, r_next);
   if (p.staged) issue_row(0, r_next);
+  float wn0, wn1;
+  w_load(r_next, wn0, wn1);
   for (long long i = 0;; ++i) {
     const long long r = r_next;
     const int t = (int)(r % p.S_q);
-    r_next = claim();
-    publish_row(i + 1, r_next);
-    const bool last = r_next < 0;
+    const unsigned pend = claim_issue();
+    const float w0 = wn0, w1 = wn1;
+    bool last = false;
     RowSrc src;
     src.S_k = p.S_k;
     src.Lr = p.dense ? min(p.L, t + 1) : p.L;
@@ -325,7 +334,6 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       if (!WAIT(&cx.bars->rowfull[buf], (uint32_t)((i >> 1) & 1))) goto done;
       staged_wait = -1;
       __syncwarp();
-      if (!last) issue_row(i + 1, r_next);
       const uint8_t* rb = rowbuf + buf * ROW_BYTES;
       src.idx = p.dense ? nullptr : reinterpret_cast<const int32_t*>(rb);
       src.dI = reinterpret_cast<const float*>(rb + (p.dense ? 0 : ROW_DI_OFF));
@@ -337,18 +345,49 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       // pass 1: number of valid slots and max |dI| over them
       int nv = 0;
       float mx = 0.f;
-      for (int j0 = 0; j0 < src.Lr; j0 += 32) {
-        const int j = j0 + lane;
-        int s;
-        const bool v = j < src.Lr && src.key(j, s);
-        if (v) mx = fmaxf(mx, fabsf(src.dI[j]));
-        nv += __popc(__ballot_sync(0xffffffffu, v));
+      if (p.staged) {
+        // 16-byte reads of the staged row, four slots per lane (the staged
+        // length is a multiple of 4; dense rows are masked at Lr)
+        const int nq4 = (src.Lr + 3) >> 2;
+        for (int q = lane; q < nq4; q += 32) {
+          const float4 dv = reinterpret_cast<const float4*>(src.dI)[q];
+          int4 id = make_int4(0, 0, 0, 0);
+          if (src.idx) id = reinterpret_cast<const int4*>(src.idx)[q];
+          const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
+          const int ii[4] = {id.x, id.y, id.z, id.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int j = 4 * q + k;
+            const bool v = src.idx ? (unsigned)ii[k] < (unsigned)src.S_k : j < src.Lr;
+            if (v) {
+              ++nv;
+              mx = fmaxf(mx, fabsf(dd[k]));
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+      } else {
+        for (int j0 = 0; j0 < src.Lr; j0 += 32) {
+          const int j = j0 + lane;
+          int s;
+          const bool v = j < src.Lr && src.key(j, s);
+          if (v) mx = fmaxf(mx, fabsf(src.dI[j]));
+          nv += __popc(__ballot_sync(0xffffffffu, v));
+        }
       }
       mx = warp_max(mx);
+      // the next row: resolve its claim, publish it, start its staging copy
+      // and its w loads
+      r_next = claim_resolve(pend);
+      publish_row(i + 1, r_next);
+      last = r_next < 0;
+      if (!last) {
+        if (p.staged) issue_row(i + 1, r_next);
+        w_load(r_next, wn0, wn1);
+      }
       // per-row scale 2^c: max |dI w| 2^c lies in [2^13, 2^14), inside fp16 range
-      float wm = 0.f;
-      for (int h = lane; h < p.H; h += 32) wm = fmaxf(wm, fabsf(__ldg(p.w + r * p.H + h)));
-      wm = warp_max(wm);
+      const float wm = warp_max(fmaxf(fabsf(w0), fabsf(w1)));
       const float m = mx * wm;
       int c = 0;
       if (m > 0.f && m <= 3.0e38f) {
