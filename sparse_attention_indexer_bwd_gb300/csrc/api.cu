@@ -89,6 +89,8 @@ int score_grad_common(const float* I, float* A, const int32_t* idx, bool dense_o
   a.scale = grad_scale / (float)S_q;
   a.dk_zero = dk;
   a.dk_numel = dk ? (long long)B * S_k * D : 0;
+  a.status = dv->status;
+  a.num_sms = dv->num_sms;
   cudaError_t e = ibwd::launch_score_grad(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
 }

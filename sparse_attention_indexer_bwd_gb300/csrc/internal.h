@@ -22,6 +22,8 @@ struct ScoreGradArgs {
   float scale;               // grad_scale / S_q
   float* dk_zero;            // optional buffer zeroed by the same launch
   long long dk_numel;
+  unsigned* status;          // device status word (a bounded wait that gave up)
+  int num_sms;
 };
 cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st);
 

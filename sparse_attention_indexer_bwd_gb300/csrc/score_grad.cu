@@ -14,9 +14,11 @@
 // Padding slots are selected out, never multiplied by a mask, so NaN or
 // garbage there never reaches dI.
 //
-// HBM-bound: 16 bytes per slot (read I, a, id; write dI).  A group of
-// 32*W threads owns a row and keeps it in registers (NV float4 per thread per
-// array), reductions are fixed-order butterflies (bitwise reproducible).
+// HBM-bound: 16 bytes per slot (read I, a, id; write dI).  Sparse rows of
+// 128..2048 slots go to a persistent kernel that streams rows through a
+// three-deep shared-memory ring of bulk copies; other shapes use a group of
+// 32*W threads per row that keeps the row in registers (NV float4 per thread
+// per array).  All reductions are fixed-order (bitwise reproducible).
 #include <algorithm>
 
 #include "internal.h"
@@ -200,6 +202,169 @@ __global__ void __launch_bounds__(BLOCK) score_grad_generic(ScoreGradArgs a, lon
   }
 }
 
+// ------------------------------------------------------- staged rows ---
+// Persistent variant for sparse rows: a CTA of L/4 threads (rounded up to a
+// warp) owns one row at a time, one float4 of each array per thread.  Thread
+// 0 keeps up to NSTG rows in flight in shared memory (bulk copies of the
+// row's index_score, attn_score and ids, 12 bytes per slot), so HBM streams
+// while the block reduces; dI goes out with 16-byte streaming stores.
+constexpr int NSTG = 3;
+
+__device__ __forceinline__ uint32_t sg_smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void sg_bulk(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(sg_smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool sg_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sg_smem_u32(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+// bounded (2 s of %globaltimer) wait for a stage
+__device__ __forceinline__ bool sg_wait(uint64_t* bar, uint32_t parity) {
+  if (sg_try(bar, parity)) return true;
+  uint64_t t0, t1;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    if (sg_try(bar, parity)) return true;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+    if (t1 - t0 > 2000000000ull) return false;
+  }
+}
+
+__global__ void score_grad_staged(ScoreGradArgs a) {
+  extern __shared__ __align__(16) uint8_t sg_smem[];
+  __shared__ uint64_t full[NSTG];
+  __shared__ float red[32];
+  const int L = a.L, L4 = L / 4;
+  const uint32_t row_bytes = (uint32_t)L * 4;
+  const uint32_t stage_bytes = 3 * row_bytes;  // I | attn | ids
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  // zero this CTA's share of dK first
+  if (a.dk_zero) {
+    const long long n4 = a.dk_numel / 4;
+    float4* d4 = reinterpret_cast<float4*>(a.dk_zero);
+    for (long long x = (long long)blockIdx.x * blockDim.x + tid; x < n4; x += (long long)gridDim.x * blockDim.x)
+      d4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long x = n4 * 4 + (long long)blockIdx.x * blockDim.x + tid; x < a.dk_numel;
+         x += (long long)gridDim.x * blockDim.x)
+      a.dk_zero[x] = 0.f;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < NSTG; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sg_smem_u32(&full[s])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const long long G = gridDim.x;
+  auto issue = [&](long long i) {  // row blockIdx.x + i*G into stage i % NSTG (thread 0)
+    const long long r = blockIdx.x + i * G;
+    const int s = (int)(i % NSTG);
+    const uint32_t dst = sg_smem_u32(sg_smem + s * stage_bytes);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sg_smem_u32(&full[s])),
+                 "r"(stage_bytes)
+                 : "memory");
+    sg_bulk(dst, a.index_score + r * L, row_bytes, &full[s]);
+    sg_bulk(dst + row_bytes, a.attn_score + r * L, row_bytes, &full[s]);
+    sg_bulk(dst + 2 * row_bytes, a.idx + r * L, row_bytes, &full[s]);
+  };
+  const long long nrows = (a.rows - blockIdx.x + G - 1) / G;
+  if (tid == 0)
+    for (long long i = 0; i < nrows && i < NSTG; ++i) issue(i);
+  long long issued = nrows < NSTG ? nrows : NSTG;
+  auto block_sum = [&](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int k = 0; k < nw; ++k) t += red[k];
+    __syncthreads();
+    return t;
+  };
+  auto block_max = [&](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    float t = -INFINITY;
+    for (int k = 0; k < nw; ++k) t = fmaxf(t, red[k]);
+    __syncthreads();
+    return t;
+  };
+  bool aborted = false;
+  for (long long i = 0; i < nrows; ++i) {
+    const int s = (int)(i % NSTG);
+    const bool ok = sg_wait(&full[s], (uint32_t)((i / NSTG) & 1));
+    if (!__syncthreads_and(ok)) {
+      aborted = true;
+      break;
+    }
+    const long long r = blockIdx.x + i * G;
+    const uint8_t* st = sg_smem + s * stage_bytes;
+    const bool in = tid < L4;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+    int4 id = make_int4(-1, -1, -1, -1);
+    if (in) {
+      x = reinterpret_cast<const float4*>(st)[tid];
+      y = reinterpret_cast<const float4*>(st + row_bytes)[tid];
+      id = reinterpret_cast<const int4*>(st + 2 * row_bytes)[tid];
+    }
+    __syncthreads();  // the stage is free: refill it with row i + NSTG
+    if (tid == 0 && issued < nrows) {
+      // the block's generic reads of the stage precede the async-proxy writes
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(issued);
+      ++issued;
+    }
+    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+    const int ids[4] = {id.x, id.y, id.z, id.w};
+    bool vv[4];
+    float m = -INFINITY, sa = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      vv[e] = in && (unsigned)ids[e] < (unsigned)a.S_k;
+      if (vv[e]) {
+        m = fmaxf(m, xs[e]);
+        sa += ys[e];
+      }
+    }
+    m = block_max(m);
+    sa = block_sum(sa);
+    float ex[4], z = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ex[e] = vv[e] ? expf(xs[e] - m) : 0.f;
+      z += ex[e];
+    }
+    z = block_sum(z);
+    if (in) {
+      float o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float ahat = sa != 0.f ? __fdiv_rn(ys[e], sa) : 0.f;
+        o[e] = vv[e] ? a.scale * (__fdiv_rn(ex[e], z) - ahat) : 0.f;
+      }
+      __stcs(reinterpret_cast<float4*>(a.attn_score + r * L) + tid, make_float4(o[0], o[1], o[2], o[3]));
+    }
+  }
+  if (aborted) {
+    if (tid == 0) atomicOr(a.status, 1u);
+    // copies still in flight land before the CTA exits (bounded)
+    __syncthreads();
+    if (tid == 0)
+      for (long long i = 0; i < issued; ++i) (void)sg_wait(&full[i % NSTG], (uint32_t)((i / NSTG) & 1));
+  }
+}
+
 template <int NV, int W>
 cudaError_t launch_vec(const ScoreGradArgs& a, int zero_blocks, cudaStream_t st) {
   constexpr int RPB = BLOCK / (32 * W);
@@ -215,6 +380,27 @@ cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st) {
   const bool aligned = (a.L % 4 == 0) && ((uintptr_t)a.index_score % 16 == 0) &&
                        ((uintptr_t)a.attn_score % 16 == 0) && (!a.idx || (uintptr_t)a.idx % 16 == 0) &&
                        (!a.dk_zero || (uintptr_t)a.dk_zero % 16 == 0);
+  // sparse rows of 128..2048 slots (a multiple of 128): the staged kernel
+  if (aligned && a.idx && a.L % 128 == 0 && a.L >= 128 && a.L <= 2048 && a.status && a.num_sms > 0) {
+    const int threads = a.L / 4;
+    const size_t smem = (size_t)NSTG * 12 * a.L;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(score_grad_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           NSTG * 12 * 2048);
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = true;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const long long grid = std::min<long long>(a.rows, (long long)a.num_sms * per_sm);
+    score_grad_staged<<<(unsigned)grid, threads, smem, st>>>(a);
+    return cudaGetLastError();
+  }
   if (aligned) {
     const int L = a.L;
     if (L <= 128) return launch_vec<1, 1>(a, zero_blocks, st);
