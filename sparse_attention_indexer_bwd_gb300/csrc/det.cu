@@ -4,11 +4,14 @@
 // fp32 atomics make d_index_k run-to-run nondeterministic (cudnn-frontend #549
 // "restore range_constexpr ...", numerics: dK uses fp32 atomicAdd and differs
 // between reruns by ~1e-7; #707 makes the same point for red.global.add).
-// Here the gemm kernel stores each slot's dK row u[r*L + j] instead, and
+// Here the slots are first sorted by key:
 //   sort:    for every key s, the slots (r, j) selecting it, in ascending
 //            (r, j) order, from per-chunk histograms and a scan (no position
-//            atomics, so the order is fixed);
-//   segsum:  dK[s] = sum over that list, in that order, of u rows.
+//            atomics, so the order is fixed); the result is each valid
+//            slot's position in that order;
+// then the gemm kernel stores each slot's dK row u at its position, so every
+// key's rows are contiguous, and
+//   segsum:  dK[s] = sum of the key's u rows, in position order.
 // The result is bitwise identical run to run and overwrites dK.
 #include <algorithm>
 
@@ -51,20 +54,46 @@ __global__ void __launch_bounds__(256) hist_kernel(const GemmArgs a, int* __rest
 }
 
 // For each (batch, key): exclusive prefix of the counts over the batch's
-// chunks (in place), and the key's total into key_start.
-__global__ void colscan_kernel(const GemmArgs a, int* __restrict__ hist, int* __restrict__ key_start) {
-  const long long gk = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (gk >= (long long)a.B * a.S_k) return;
-  const int b = (int)(gk / a.S_k), s = (int)(gk % a.S_k);
+// chunks (in place), and the key's total into key_start.  A block takes 32
+// keys; its 32 warps split the batch's chunks into 32 contiguous segments
+// (lane = key, so every access is a coalesced 128-byte row piece): segment
+// sums, a scan over the segments, then the prefixes within each segment.
+__global__ void __launch_bounds__(1024) colscan_kernel(const GemmArgs a, int* __restrict__ hist,
+                                                      int* __restrict__ key_start) {
+  __shared__ int seg[32][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int kpb = (a.S_k + 31) / 32;  // key blocks per batch
+  const int b = (int)(blockIdx.x / kpb);
+  const int s = (int)(blockIdx.x % kpb) * 32 + lane;
+  const bool on = s < a.S_k;
   const int cpb = (a.S_q + RB - 1) / RB;
-  int run = 0;
-  for (int c = 0; c < cpb; ++c) {
-    int* h = hist + ((long long)b * cpb + c) * a.S_k + s;
-    const int v = *h;
-    *h = run;
-    run += v;
+  const int per = (cpb + 31) / 32;
+  const int c0 = min(cpb, w * per), c1 = min(cpb, c0 + per);
+  int* col = hist + (long long)b * cpb * a.S_k + s;
+  int sum = 0;
+  if (on)
+    for (int c = c0; c < c1; ++c) sum += col[(long long)c * a.S_k];
+  seg[w][lane] = sum;
+  __syncthreads();
+  if (w == 0) {
+    int run = 0;
+    for (int k = 0; k < 32; ++k) {
+      const int v = seg[k][lane];
+      seg[k][lane] = run;
+      run += v;
+    }
+    if (on) key_start[(long long)b * a.S_k + s] = run;
   }
-  key_start[gk] = run;
+  __syncthreads();
+  if (on) {
+    int run = seg[w][lane];
+    for (int c = c0; c < c1; ++c) {
+      int* h = col + (long long)c * a.S_k;
+      const int v = *h;
+      *h = run;
+      run += v;
+    }
+  }
 }
 
 // Exclusive scan of the per-key totals into CSR offsets (one block).
@@ -93,75 +122,136 @@ __global__ void __launch_bounds__(1024) keyscan_kernel(int* __restrict__ key_sta
   if (threadIdx.x == 0) key_start[n] = carry;
 }
 
-// One warp per chunk places its slots in ascending (r, j) order: lanes that
+// One warp per chunk ranks its slots in ascending (r, j) order: lanes that
 // hold the same key in one 32-slot step take consecutive positions by lane.
+// Each row's ids are read 256 slots at a time into registers, one block
+// ahead.  A step first tests for equal keys among its lanes (each lane tags
+// its key in shared memory and reads the tag back): without duplicates every
+// lane takes the key's cursor directly; with them the lanes rank themselves
+// with a match.
 __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* __restrict__ hist,
-                                                   const int* __restrict__ key_start, int* __restrict__ perm) {
-  extern __shared__ int cursor[];
+                                                   const int* __restrict__ key_start, int* __restrict__ pos) {
+  extern __shared__ int cursor[];  // [S_k] cursors, then [S_k] tags
+  int* tag = cursor + a.S_k;
   const int cpb = (a.S_q + RB - 1) / RB;
   const long long chunk = blockIdx.x;
   const int b = (int)(chunk / cpb);
   const int t0 = (int)(chunk % cpb) * RB;
   const int lane = threadIdx.x;
-  for (int s = lane; s < a.S_k; s += 32)
-    cursor[s] = key_start[(long long)b * a.S_k + s] + hist[chunk * a.S_k + s];
+  {
+    const int* ks = key_start + (long long)b * a.S_k;
+    const int* hs = hist + chunk * a.S_k;
+    int s = lane;
+    for (; s + 7 * 32 < a.S_k; s += 8 * 32) {
+      int x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = __ldg(ks + s + k * 32) + __ldg(hs + s + k * 32);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) cursor[s + k * 32] = x[k];
+    }
+    for (; s < a.S_k; s += 32) cursor[s] = __ldg(ks + s) + __ldg(hs + s);
+  }
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
   const int t1 = min(a.S_q, t0 + RB);
+  constexpr int NB = 8;  // 32-slot steps per register block
+  // key of slot j of row r, or -1 when the slot is padding
+  auto load_key = [&](long long r, int t, int j) -> int {
+    const int lim = a.idx ? a.L : min(a.L, t + 1);
+    if (j >= lim) return -1;
+    if (!a.idx) return j;
+    const int k = __ldg(a.idx + r * a.L + j);
+    return (unsigned)k < (unsigned)a.S_k ? k : -1;
+  };
   for (int t = t0; t < t1; ++t) {
     const long long r = (long long)b * a.S_q + t;
     const int lim = a.idx ? a.L : min(a.L, t + 1);
-    for (int j0 = 0; j0 < lim; j0 += 32) {
-      const int j = j0 + lane;
-      int key = 0;
-      const bool v = j < lim && slot_key(a, r, j, key);
-      const unsigned grp = __match_any_sync(0xffffffffu, v ? key : -1 - lane);
-      int base = 0;
-      if (v) base = cursor[key];
-      __syncwarp();
-      if (v) {
-        perm[base + __popc(grp & lt)] = (int)(r * a.L + j);
-        if ((grp & lt) == 0) cursor[key] = base + __popc(grp);
+    int cur[NB], nxt[NB];
+#pragma unroll
+    for (int k = 0; k < NB; ++k) cur[k] = load_key(r, t, k * 32 + lane);
+    for (int j0 = 0; j0 < lim; j0 += NB * 32) {
+#pragma unroll
+      for (int k = 0; k < NB; ++k) nxt[k] = load_key(r, t, j0 + NB * 32 + k * 32 + lane);
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        const int key = cur[k];
+        const bool v = key >= 0;
+        const int slot = (int)(r * a.L + j0 + k * 32 + lane);
+        if (v) tag[key] = lane;
+        __syncwarp();
+        const bool dup = __any_sync(0xffffffffu, v && tag[key] != lane);
+        if (!dup) {
+          if (v) {
+            const int base = cursor[key];
+            pos[slot] = base;
+            cursor[key] = base + 1;
+          }
+        } else {
+          const unsigned grp = __match_any_sync(0xffffffffu, v ? key : -1 - lane);
+          int base = 0;
+          if (v) base = cursor[key];
+          __syncwarp();
+          if (v) {
+            pos[slot] = base + __popc(grp & lt);
+            if ((grp & lt) == 0) cursor[key] = base + __popc(grp);
+          }
+        }
+        __syncwarp();
       }
-      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < NB; ++k) cur[k] = nxt[k];
     }
   }
 }
 
-// One warp per key: dK[key] = sum of u rows over the key's CSR segment, in
-// segment order.
-__global__ void __launch_bounds__(256) segsum_kernel(const GemmArgs a, const float* __restrict__ u,
-                                                     const int* __restrict__ key_start,
-                                                     const int* __restrict__ perm) {
-  const long long gk = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (gk >= (long long)a.B * a.S_k) return;
+// One block of eight warps per key: dK[key] = sum of the key's u rows, which
+// the gemm kernel stored contiguously in position order.  Warp w sums rows
+// w, w + 8, w + 16, ... of the segment in order (the block reads eight
+// consecutive rows per step, four steps in flight), then the eight partial
+// sums are added in warp order: a fixed order, so dK is bitwise reproducible.
+constexpr int SEG_WARPS = 8;
+__global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const GemmArgs a, const float* __restrict__ u,
+                                                               const int* __restrict__ key_start) {
+  __shared__ float4 part[SEG_WARPS][32];
+  const long long gk = blockIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int beg = key_start[gk], end = key_start[gk + 1];
   const int d = lane * 4;
   const bool on = d < a.D;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int p = beg;
-  for (; p + 4 <= end; p += 4) {
-    const int i0 = __ldg(perm + p), i1 = __ldg(perm + p + 1), i2 = __ldg(perm + p + 2), i3 = __ldg(perm + p + 3);
-    if (on) {
-      const float4 v0 = __ldcs(reinterpret_cast<const float4*>(u + (long long)i0 * a.D + d));
-      const float4 v1 = __ldcs(reinterpret_cast<const float4*>(u + (long long)i1 * a.D + d));
-      const float4 v2 = __ldcs(reinterpret_cast<const float4*>(u + (long long)i2 * a.D + d));
-      const float4 v3 = __ldcs(reinterpret_cast<const float4*>(u + (long long)i3 * a.D + d));
-      acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
-      acc.x += v1.x; acc.y += v1.y; acc.z += v1.z; acc.w += v1.w;
-      acc.x += v2.x; acc.y += v2.y; acc.z += v2.z; acc.w += v2.w;
-      acc.x += v3.x; acc.y += v3.y; acc.z += v3.z; acc.w += v3.w;
+  constexpr int NF = 4;  // steps in flight per warp
+  for (int p0 = beg + w; p0 < end; p0 += NF * SEG_WARPS) {
+    float4 v[NF];
+#pragma unroll
+    for (int k = 0; k < NF; ++k) {
+      const int pr = p0 + k * SEG_WARPS;
+      v[k] = (on && pr < end) ? __ldcs(reinterpret_cast<const float4*>(u + (long long)pr * a.D + d))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < NF; ++k) {
+      if (p0 + k * SEG_WARPS < end) {
+        acc.x += v[k].x;
+        acc.y += v[k].y;
+        acc.z += v[k].z;
+        acc.w += v[k].w;
+      }
     }
   }
-  for (; p < end; ++p) {
-    const int i0 = __ldg(perm + p);
-    if (on) {
-      const float4 v0 = __ldcs(reinterpret_cast<const float4*>(u + (long long)i0 * a.D + d));
-      acc.x += v0.x; acc.y += v0.y; acc.z += v0.z; acc.w += v0.w;
+  part[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && on) {
+    float4 t = part[0][lane];
+#pragma unroll
+    for (int k = 1; k < SEG_WARPS; ++k) {
+      const float4 x = part[k][lane];
+      t.x += x.x;
+      t.y += x.y;
+      t.z += x.z;
+      t.w += x.w;
     }
+    *reinterpret_cast<float4*>(a.dk + gk * a.D + d) = t;
   }
-  if (on) *reinterpret_cast<float4*>(a.dk + gk * a.D + d) = acc;
 }
 
 }  // namespace
@@ -170,12 +260,13 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   char* ws = static_cast<char*>(a.ws);
   int* hist = reinterpret_cast<int*>(ws + lay.hist);
   int* key_start = reinterpret_cast<int*>(ws + lay.key_start);
-  int* perm = reinterpret_cast<int*>(ws + lay.perm);
-  const size_t sh = (size_t)a.S_k * sizeof(int);
+  int* pos = reinterpret_cast<int*>(ws + lay.pos);
+  const size_t sh = (size_t)a.S_k * sizeof(int);       // histogram counters
+  const size_t sh_place = 2 * sh;                          // cursors and tags
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (sh > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (sh_place > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -184,9 +275,9 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   }
   hist_kernel<<<(unsigned)lay.nchunks, 256, sh, st>>>(a, hist);
   const long long nk = (long long)a.B * a.S_k;
-  colscan_kernel<<<(unsigned)((nk + 255) / 256), 256, 0, st>>>(a, hist, key_start);
+  colscan_kernel<<<(unsigned)(a.B * ((a.S_k + 31) / 32)), 1024, 0, st>>>(a, hist, key_start);
   keyscan_kernel<<<1, 1024, 0, st>>>(key_start, nk);
-  place_kernel<<<(unsigned)lay.nchunks, 32, sh, st>>>(a, hist, key_start, perm);
+  place_kernel<<<(unsigned)lay.nchunks, 32, sh_place, st>>>(a, hist, key_start, pos);
   return cudaGetLastError();
 }
 
@@ -194,9 +285,8 @@ cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream
   char* ws = static_cast<char*>(a.ws);
   const float* u = reinterpret_cast<const float*>(ws + lay.u);
   const int* key_start = reinterpret_cast<const int*>(ws + lay.key_start);
-  const int* perm = reinterpret_cast<const int*>(ws + lay.perm);
   const long long nk = (long long)a.B * a.S_k;
-  segsum_kernel<<<(unsigned)((nk * 32 + 255) / 256), 256, 0, st>>>(a, u, key_start, perm);
+  segsum_kernel<<<(unsigned)nk, SEG_WARPS * 32, 0, st>>>(a, u, key_start);
   return cudaGetLastError();
 }
 

@@ -63,8 +63,7 @@ constexpr int NGT = 128;                  // gather threads
 constexpr int NQT = 64;                   // Q-loader threads
 constexpr int NDZT = 256;                 // dz threads (two groups of 128)
 constexpr int NDKT = 256;                 // dK threads (two groups of 128)
-constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI (sparse) or dI (dense)
-constexpr uint32_t ROW_DI_OFF = 8192;     // dI offset inside a staged sparse row
+constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI [| pos] (sparse), dI [| pos] (dense)
 
 constexpr uint32_t KTILE_BYTES = kBM * kDP * 2;   // 32 KB
 constexpr uint32_t KHALF_BYTES = kBM * 64 * 2;    // one 64-column half of a K tile
@@ -77,7 +76,7 @@ constexpr uint32_t TM_Z = 0, TM_DK = 128, TM_DQ = 384, TM_COLS = 512;
 
 struct TileMeta {
   int key[kBM];    // selected key (row of k within the batch)
-  int slot[kBM];   // slot j within the query row
+  int slot[kBM];   // deterministic mode: the slot's row in u (its position in key order)
   float dis[kBM];  // dI[t, j] * 2^c
   int r, count, c, flags;
 };
@@ -121,7 +120,8 @@ struct KParams {
   float* dq;
   float* dw;
   float* dk;
-  float* u;  // deterministic per-slot rows, or nullptr
+  float* u;         // deterministic: per-slot dK rows in key order, or nullptr
+  const int* pos;   // deterministic: each slot's row in u
   unsigned* sched;  // row counter in the workspace, zeroed by k_to_f16_kernel
   unsigned* status;
   long long rows;
@@ -253,6 +253,7 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
 struct RowSrc {
   const int32_t* idx;  // nullptr for dense rows
   const float* dI;
+  const int* pos;      // deterministic: the slots' rows in u (else nullptr)
   int Lr;              // slots to look at
   int S_k;
   __device__ __forceinline__ bool key(int j, int& s) const {
@@ -300,15 +301,18 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       // this thread's earlier generic reads of the buffer precede the async writes
       fence_proxy_async_smem();
       const uint32_t dst = smem_u32(rowbuf + buf * ROW_BYTES);
+      // packed: [idx (sparse)] dI [pos (deterministic)], L*4 bytes apart
+      const uint32_t stride = (uint32_t)p.L * 4;
       if (p.dense) {
         const uint32_t bytes = (uint32_t)(((min(p.L, t + 1) * 4) + 15) & ~15);
-        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], bytes);
+        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], p.pos ? 2 * bytes : bytes);
         bulk_g2s(dst, p.dI + r * p.L, bytes, &cx.bars->rowfull[buf]);
+        if (p.pos) bulk_g2s(dst + stride, p.pos + r * p.L, bytes, &cx.bars->rowfull[buf]);
       } else {
-        const uint32_t bytes = (uint32_t)p.L * 4;
-        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], 2 * bytes);
-        bulk_g2s(dst, p.idx + r * p.L, bytes, &cx.bars->rowfull[buf]);
-        bulk_g2s(dst + ROW_DI_OFF, p.dI + r * p.L, bytes, &cx.bars->rowfull[buf]);
+        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], p.pos ? 3 * stride : 2 * stride);
+        bulk_g2s(dst, p.idx + r * p.L, stride, &cx.bars->rowfull[buf]);
+        bulk_g2s(dst + stride, p.dI + r * p.L, stride, &cx.bars->rowfull[buf]);
+        if (p.pos) bulk_g2s(dst + 2 * stride, p.pos + r * p.L, stride, &cx.bars->rowfull[buf]);
       }
     }
     staged_wait = i;
@@ -335,11 +339,14 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       staged_wait = -1;
       __syncwarp();
       const uint8_t* rb = rowbuf + buf * ROW_BYTES;
+      const uint32_t stride = (uint32_t)p.L * 4;
       src.idx = p.dense ? nullptr : reinterpret_cast<const int32_t*>(rb);
-      src.dI = reinterpret_cast<const float*>(rb + (p.dense ? 0 : ROW_DI_OFF));
+      src.dI = reinterpret_cast<const float*>(rb + (p.dense ? 0 : stride));
+      src.pos = p.pos ? reinterpret_cast<const int*>(rb + (p.dense ? 1 : 2) * stride) : nullptr;
     } else {
       src.idx = p.dense ? nullptr : p.idx + r * p.L;
       src.dI = p.dI + r * p.L;
+      src.pos = p.pos ? p.pos + r * p.L : nullptr;
     }
     {
       // pass 1: number of valid slots and max |dI| over them
@@ -415,7 +422,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
           if (v && rank >= skip && rank < skip + room) {
             const int pos = fill + rank - skip;
             M.key[pos] = s;
-            M.slot[pos] = j;
+            M.slot[pos] = src.pos ? src.pos[j] : j;
             M.dis[pos] = src.dI[j] * sc;
           }
           const int taken = min(tot - skip, room);
@@ -768,7 +775,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
     const TileMeta& M = cx.meta[ms];
     const int flags = M.flags, c = M.c, r = M.r, count = M.count;
-    float* base = p.u ? p.u + (long long)r * p.L * p.D : p.dk + (long long)(r / p.S_q) * p.S_k * p.D;
+    float* base = p.u ? p.u : p.dk + (long long)(r / p.S_q) * p.S_k * p.D;
     const int* ids = p.u ? M.slot : M.key;
     if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
     if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, g);
@@ -933,7 +940,7 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
     off = up(off + (size_t)w.nchunks * S_k * 4);
     w.key_start = off;
     off = up(off + ((size_t)B * S_k + 1) * 4);
-    w.perm = off;
+    w.pos = off;
     off = up(off + (size_t)rows * L * 4);
   }
   w.total = off;
@@ -974,6 +981,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.dw = a.dw;
   p.dk = a.dk;
   p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
+  p.pos = a.deterministic ? reinterpret_cast<const int*>(ws + lay.pos) : nullptr;
   p.sched = sched;
   p.status = a.status;
   p.rows = (long long)a.B * a.S_q;
@@ -987,7 +995,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.L = a.L;
   p.dense = a.idx == nullptr;
   // rows are staged in shared memory when they fit and are 16-byte aligned
-  const bool fits = p.dense ? (size_t)a.L * 4 <= ROW_BYTES : (size_t)a.L * 4 <= ROW_DI_OFF;
+  const size_t arrays = (p.dense ? 1 : 2) + (a.deterministic ? 1 : 0);
+  const bool fits = arrays * a.L * 4 <= ROW_BYTES;
   const bool al = (a.L % 4 == 0) && ((uintptr_t)a.dI % 16 == 0) && (p.dense || (uintptr_t)a.idx % 16 == 0);
   p.staged = fits && al;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);

@@ -50,7 +50,7 @@ struct WsLayout {
   size_t u;          // deterministic: per-slot dK rows [rows*L, D] fp32
   size_t hist;       // deterministic: per-chunk key counts [nchunks, S_k] int32
   size_t key_start;  // deterministic: CSR offsets [B*S_k + 1] int32
-  size_t perm;       // deterministic: slot ids r*L + j sorted by key [rows*L] int32
+  size_t pos;        // deterministic: sorted position of each valid slot r*L + j [rows*L] int32
   size_t total;
   long long nchunks;
 };
