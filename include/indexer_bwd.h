@@ -26,7 +26,7 @@
  *    batch (id s of batch b addresses k[b, s]).
  *  - Shape limits: B >= 1, S_q >= 1, S_k >= 1, topk >= 1, 1 <= H <= 64,
  *    8 <= D <= 128 with D % 8 == 0, B*S_q*topk < 2^31; the deterministic
- *    dK mode also needs S_k <= 24576 (its key sort keeps per-key state in
+ *    dK mode also needs S_k <= 40960 (its key sort keeps per-key state in
  *    shared memory).
  *  - q and k entries must lie in fp16 range (|x| <= 65504): the gemm stage
  *    feeds fp16 tensor-core operands converted exactly from bf16.

@@ -108,7 +108,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   if (B < 1 || S_q < 1 || S_k < 1 || L < 1 || H < 1 || D < 1) return IBWD_ERR_INVALID_ARG;
   if (!shape_ok(B, S_q, S_k, H, D, L)) return IBWD_ERR_UNSUPPORTED;
   // the sort keeps a cursor and a tag per key of a batch in shared memory
-  if (mode == IBWD_DK_DETERMINISTIC && S_k > 24576) return IBWD_ERR_UNSUPPORTED;
+  if (mode == IBWD_DK_DETERMINISTIC && S_k > 40960) return IBWD_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k, w, dI, dq, dw, dk};
   for (const void* p : ptrs)
     if (!aligned16(p)) return IBWD_ERR_INVALID_ARG;

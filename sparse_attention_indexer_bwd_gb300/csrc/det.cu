@@ -21,7 +21,7 @@
 namespace ibwd {
 namespace {
 
-constexpr int RB = 16;  // query rows per sort chunk (chunks never straddle a batch)
+constexpr int RB = kSortRows;  // query rows per sort chunk (chunks never straddle a batch)
 
 __device__ __forceinline__ bool slot_key(const GemmArgs& a, long long r, int j, int& key) {
   if (a.idx) {
@@ -131,8 +131,8 @@ __global__ void __launch_bounds__(1024) keyscan_kernel(int* __restrict__ key_sta
 // with a match.
 __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* __restrict__ hist,
                                                    const int* __restrict__ key_start, int* __restrict__ pos) {
-  extern __shared__ int cursor[];  // [S_k] cursors, then [S_k] tags
-  int* tag = cursor + a.S_k;
+  extern __shared__ int cursor[];  // [S_k] cursors, then [S_k] one-byte tags
+  unsigned char* tag = reinterpret_cast<unsigned char*>(cursor + a.S_k);
   const int cpb = (a.S_q + RB - 1) / RB;
   const long long chunk = blockIdx.x;
   const int b = (int)(chunk / cpb);
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* 
         const int key = cur[k];
         const bool v = key >= 0;
         const int slot = (int)(r * a.L + j0 + k * 32 + lane);
-        if (v) tag[key] = lane;
+        if (v) tag[key] = (unsigned char)lane;
         __syncwarp();
         const bool dup = __any_sync(0xffffffffu, v && tag[key] != lane);
         if (!dup) {
@@ -262,7 +262,7 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   int* key_start = reinterpret_cast<int*>(ws + lay.key_start);
   int* pos = reinterpret_cast<int*>(ws + lay.pos);
   const size_t sh = (size_t)a.S_k * sizeof(int);       // histogram counters
-  const size_t sh_place = 2 * sh;                          // cursors and tags
+  const size_t sh_place = sh + (size_t)a.S_k;              // cursors and one-byte tags
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

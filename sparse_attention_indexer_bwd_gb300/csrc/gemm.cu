@@ -935,7 +935,7 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
     const long long rows = (long long)B * S_q;
     w.u = off;
     off = up(off + (size_t)rows * L * D * 4);
-    w.nchunks = (long long)B * ((S_q + 15) / 16);
+    w.nchunks = (long long)B * ((S_q + kSortRows - 1) / kSortRows);
     w.hist = off;
     off = up(off + (size_t)w.nchunks * S_k * 4);
     w.key_start = off;

@@ -11,6 +11,7 @@ namespace ibwd {
 constexpr int kBM = 128;  // keys per tile (the MMA M dimension for Z and dK)
 constexpr int kDP = 128;  // head dim padded to 128 (the MMA M dimension for dQ)
 constexpr int kHP = 64;   // indexer heads padded to 64 (the MMA N dimension for Z and dQ)
+constexpr int kSortRows = 4;  // query rows per chunk of the deterministic mode's key sort
 
 struct ScoreGradArgs {
   const float* index_score;  // [rows, L]
