@@ -40,10 +40,10 @@ METRIC = "indexer-bwd kernel µs & TFLOP/s (frac of bf16 peak), H64 D128 Sq8192 
 # kernel sources it was taken on; any change to those sources makes it stale
 # and the benchmark then reports null.  The capture and its command are
 # summarised under profiles/.
-PROFILED_SOURCES = "9eab5226006acaa5c38fa62e7a91901bb7d9842f08f051a37765383719038860"
+PROFILED_SOURCES = "3b8e2613a6cf6b44e2c098c3f87fa402ffc102b0c341bfa7eab2ce804b0eddce"
 PROFILED_TRAFFIC = {
-    ("anchor", "atomic"): {"gemm_stage": 206.737408e6 + 222.362112e6 + 1.058560e6,  # gemm_kernel + k_to_f16
-                           "score_grad": 100.711936e6 + 4.698112e6},
+    ("anchor", "atomic"): {"gemm_stage": 206.738944e6 + 222.515968e6 + 1.058560e6,  # gemm_kernel + k_to_f16
+                           "score_grad": 100.696064e6 + 4.952832e6},
 }
 
 
@@ -208,6 +208,22 @@ def forward_logits(torch, q, k, w, idx, S_k, chunk=256):
     return out
 
 
+def forward_logits_dense(torch, q, k, w, chunk=128):
+    """Input preparation for the dense-causal variant: index_score[t, s] =
+    sum_h w relu(q.k) for s <= t, 0 above the diagonal (plain torch, fp32)."""
+    B, S, H, D = q.shape
+    out = torch.zeros((B, S, S), dtype=torch.float32, device=q.device)
+    for b in range(B):
+        kf = k[b].float()
+        for t0 in range(0, S, chunk):
+            z = torch.einsum("chd,sd->chs", q[b, t0:t0 + chunk].float(), kf)
+            I = torch.einsum("ch,chs->cs", w[b, t0:t0 + chunk], torch.relu(z))
+            t = torch.arange(t0, min(S, t0 + chunk), device=q.device)[:, None]
+            s_ = torch.arange(S, device=q.device)[None, :]
+            out[b, t0:t0 + chunk] = torch.where(s_ <= t, I, torch.zeros_like(I))
+    return out
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -256,8 +272,6 @@ def run_ours(args, wl):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     td = dist_init(ws, "nccl")
-    if wl.dense:
-        raise SystemExit("the benchmark times the top-k workloads (the dense variant is a parity case)")
     mode = ibwd.IBWD_DK_DETERMINISTIC if args.mode == "det" else ibwd.IBWD_DK_ATOMIC
 
     # ---- inputs (seeded, synthetic; resident in HBM before timing)
@@ -265,14 +279,15 @@ def run_ours(args, wl):
     q = torch.from_numpy(x["q"].view(np.int16)).to(dev).view(torch.bfloat16)
     k = torch.from_numpy(x["k"].view(np.int16)).to(dev).view(torch.bfloat16)
     w = torch.from_numpy(x["w"]).to(dev)
-    idx = torch.from_numpy(x["idx"]).to(dev)
+    idx = None if wl.dense else torch.from_numpy(x["idx"]).to(dev)
     attn0 = torch.from_numpy(x["attn"]).to(dev)
-    I = forward_logits(torch, q, k, w, idx, wl.S_k)
+    I = forward_logits_dense(torch, q, k, w) if wl.dense else forward_logits(torch, q, k, w, idx, wl.S_k)
     B, S_q, H, D = q.shape
     dq = torch.empty((B, S_q, H, D), dtype=torch.float32, device=dev)
     dw = torch.empty((B, S_q, H), dtype=torch.float32, device=dev)
     dk = torch.empty((B, wl.S_k, D), dtype=torch.float32, device=dev)
-    wsb = torch.empty(ibwd.indexer_bwd_gemm_workspace_size(B, S_q, wl.S_k, H, D, wl.topk, mode),
+    wsb = torch.empty(ibwd.indexer_bwd_dense_gemm_workspace_size(B, S_q, H, D, mode) if wl.dense else
+                      ibwd.indexer_bwd_gemm_workspace_size(B, S_q, wl.S_k, H, D, wl.topk, mode),
                       dtype=torch.uint8, device=dev)
     # score-grad overwrites attn_score with dI: every step gets its own copy
     nbuf = args.steps + args.warmup
@@ -283,10 +298,17 @@ def run_ours(args, wl):
     def step(a, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        ibwd.indexer_bwd_score_grad(I, a, idx, wl.S_k, 1.0, dk if mode == ibwd.IBWD_DK_ATOMIC else None, stream)
+        zero = dk if mode == ibwd.IBWD_DK_ATOMIC else None
+        if wl.dense:
+            ibwd.indexer_bwd_dense_score_grad(I, a, 1.0, zero, stream)
+        else:
+            ibwd.indexer_bwd_score_grad(I, a, idx, wl.S_k, 1.0, zero, stream)
         if ev is not None:
             ev[1].record(stream)
-        ibwd.indexer_bwd_gemm(q, k, w, a, idx, dq, dw, dk, mode, wsb, stream)
+        if wl.dense:
+            ibwd.indexer_bwd_dense_gemm(q, k, w, a, dq, dw, dk, mode, wsb, stream)
+        else:
+            ibwd.indexer_bwd_gemm(q, k, w, a, idx, dq, dw, dk, mode, wsb, stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -334,15 +356,22 @@ def run_ours(args, wl):
     gm_avg = statistics.mean(gm_ms)
     sg_avg = statistics.mean(sg_ms)
     achieved = flops / (gm_avg * 1e-3) / 1e12
-    valid = float((x["idx"] >= 0).mean())
-    sg_bytes = 16.0 * wl.B * wl.S_q * wl.topk + (4.0 * wl.B * wl.S_k * wl.D if mode == ibwd.IBWD_DK_ATOMIC else 0.0)
+    zero_bytes = 4.0 * wl.B * wl.S_k * wl.D if mode == ibwd.IBWD_DK_ATOMIC else 0.0
+    if wl.dense:
+        valid = (wl.S_q + 1) / (2.0 * wl.S_q)
+        # read index_score and attn_score on and below the diagonal, write the full dI rows
+        sg_bytes = 8.0 * wl.B * wl.S_q * (wl.S_q + 1) / 2 + 4.0 * wl.B * wl.S_q * wl.S_q + zero_bytes
+    else:
+        valid = float((x["idx"] >= 0).mean())
+        sg_bytes = 16.0 * wl.B * wl.S_q * wl.topk + zero_bytes
 
     # ---- end to end through the public API from pinned host memory
     e2e = None
     if not args.no_e2e:
-        h = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in
-             (("q", x["q"].view(np.int16)), ("k", x["k"].view(np.int16)), ("w", x["w"]), ("idx", x["idx"]),
-              ("attn", x["attn"]))}
+        arrays = [("q", x["q"].view(np.int16)), ("k", x["k"].view(np.int16)), ("w", x["w"]), ("attn", x["attn"])]
+        if not wl.dense:
+            arrays.append(("idx", x["idx"]))
+        h = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in arrays}
         h["I"] = I.cpu().pin_memory()
         hq = torch.empty((B, S_q, H, D), dtype=torch.float32).pin_memory()
         hw = torch.empty((B, S_q, H), dtype=torch.float32).pin_memory()
@@ -356,7 +385,7 @@ def run_ours(args, wl):
             for n, t in h.items():
                 dbuf[n].copy_(t, non_blocking=True)
             ibwd.indexer_backward(dbuf["q"].view(torch.bfloat16), dbuf["k"].view(torch.bfloat16), dbuf["w"],
-                                  dbuf["I"], dbuf["attn"], dbuf["idx"], dk_mode=mode, workspace=wsb,
+                                  dbuf["I"], dbuf["attn"], dbuf.get("idx"), dk_mode=mode, workspace=wsb,
                                   out=(dq, dw, dk), stream=stream)
             hq.copy_(dq, non_blocking=True)
             hw.copy_(dw, non_blocking=True)
@@ -382,7 +411,7 @@ def run_ours(args, wl):
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": ksteps}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not wl.dense:
         cpu = cpu_baseline(wl, x, I.cpu().numpy(), args.cpu_seconds)
 
     if rank != 0:
@@ -394,7 +423,7 @@ def run_ours(args, wl):
         "vs_baseline": None, "dtype": "f16 tensor-core operands, fp32 accumulate (bf16 inputs)",
         "data": "synthetic (seeded; index_score = forward logits of the seeded q, k, w)",
         "config": {"workload": f"{wl.name}: B={wl.B} H={wl.H} D={wl.D} S_q={wl.S_q} S_k={wl.S_k} "
-                               f"topk={wl.topk}, causal top-k ids",
+                               + ("every causal key (dense)" if wl.dense else f"topk={wl.topk}, {wl.ids} top-k ids"),
                    "dk_mode": args.mode, "l2": "inputs larger than L2 (q alone is 134 MB); "
                                                "a fresh attn_score copy per step",
                    "valid_slot_fraction": round(valid, 4)},
