@@ -243,7 +243,7 @@ __device__ __forceinline__ bool sg_wait(uint64_t* bar, uint32_t parity) {
 __global__ void score_grad_staged(ScoreGradArgs a) {
   extern __shared__ __align__(16) uint8_t sg_smem[];
   __shared__ uint64_t full[NSTG];
-  __shared__ float red[32];
+  __shared__ float red[32], red2[32];
   const int L = a.L, L4 = L / 4;
   const uint32_t row_bytes = (uint32_t)L * 4;
   const uint32_t stage_bytes = 3 * row_bytes;  // I | attn | ids
@@ -290,15 +290,26 @@ __global__ void score_grad_staged(ScoreGradArgs a) {
     __syncthreads();
     return t;
   };
-  auto block_max = [&](float v) {
+  // max of m and sum of s over the block, in one exchange
+  auto block_max_sum = [&](float& m, float& sm) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if (lane == 0) red[wid] = v;
+    for (int o = 16; o > 0; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    }
+    if (lane == 0) {
+      red[wid] = m;
+      red2[wid] = sm;
+    }
     __syncthreads();
-    float t = -INFINITY;
-    for (int k = 0; k < nw; ++k) t = fmaxf(t, red[k]);
+    float tm = -INFINITY, ts = 0.f;
+    for (int k = 0; k < nw; ++k) {
+      tm = fmaxf(tm, red[k]);
+      ts += red2[k];
+    }
     __syncthreads();
-    return t;
+    m = tm;
+    sm = ts;
   };
   bool aborted = false;
   for (long long i = 0; i < nrows; ++i) {
@@ -337,8 +348,7 @@ __global__ void score_grad_staged(ScoreGradArgs a) {
         sa += ys[e];
       }
     }
-    m = block_max(m);
-    sa = block_sum(sa);
+    block_max_sum(m, sa);
     float ex[4], z = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -347,12 +357,12 @@ __global__ void score_grad_staged(ScoreGradArgs a) {
     }
     z = block_sum(z);
     if (in) {
+      // one reciprocal per row (the quotients differ from IEEE division by
+      // at most one rounding)
+      const float rz = 1.0f / z, ra = sa != 0.f ? 1.0f / sa : 0.f;
       float o[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float ahat = sa != 0.f ? __fdiv_rn(ys[e], sa) : 0.f;
-        o[e] = vv[e] ? a.scale * (__fdiv_rn(ex[e], z) - ahat) : 0.f;
-      }
+      for (int e = 0; e < 4; ++e) o[e] = vv[e] ? a.scale * (ex[e] * rz - ys[e] * ra) : 0.f;
       __stcs(reinterpret_cast<float4*>(a.attn_score + r * L) + tid, make_float4(o[0], o[1], o[2], o[3]));
     }
   }
