@@ -35,48 +35,38 @@ import synth  # noqa: E402
 
 METRIC = "indexer-bwd kernel µs & TFLOP/s (frac of bf16 peak), H64 D128 Sq8192 topk1024"
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the anchor workload in atomic mode, kept with the hash of the
-# kernel sources it was taken on; any change to those sources makes it stale
-# and the benchmark then reports null.  The capture and its command are
-# summarised under profiles/.
-PROFILED_SOURCES = "3b8e2613a6cf6b44e2c098c3f87fa402ffc102b0c341bfa7eab2ce804b0eddce"
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# ncu captures of the anchor workload in atomic mode, each kept with the hash
+# of the source files of the kernels it measured; a change to any of those
+# files makes the figure stale and the benchmark then reports null.  The
+# captures and their commands are summarised under profiles/.
+GEMM_FILES = ("gemm.cu", "ptx.cuh", "internal.h", "api.cu")
+SCORE_GRAD_FILES = ("score_grad.cu", "internal.h", "api.cu")
 PROFILED_TRAFFIC = {
-    ("anchor", "atomic"): {"gemm_stage": 206.738944e6 + 222.515968e6 + 1.058560e6,  # gemm_kernel + k_to_f16
-                           "score_grad": 100.696064e6 + 4.952832e6},
+    # gemm_kernel + k_to_f16_kernel of one gemm-stage call
+    ("anchor", "atomic", "gemm_stage"): ("2e37946359922408a8926a368aa6e551a9e9ced9e6f72b11da91f0b216c99b8f", 206.738944e6 + 222.515968e6 + 1.058560e6),
+    ("anchor", "atomic", "score_grad"): ("31aa15be76cbc1ea063eecdc3605f6ccc5395863a2764fdf16dac9e72a62611c", 100.696064e6 + 4.952832e6),
 }
 
 
-def kernel_sources_hash() -> str:
+def sources_hash(files) -> str:
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sparse_attention_indexer_bwd_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in files:
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
 def profiled_traffic(workload: str, mode: str) -> dict:
-    if kernel_sources_hash() != PROFILED_SOURCES:
-        return {}
-    return PROFILED_TRAFFIC.get((workload, mode), {})
-
-
-def parse():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="anchor", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--mode", default="atomic", choices=["atomic", "det"])
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    return ap.parse_args()
+    out = {}
+    for kernel, files in (("gemm_stage", GEMM_FILES), ("score_grad", SCORE_GRAD_FILES)):
+        entry = PROFILED_TRAFFIC.get((workload, mode, kernel))
+        if entry and sources_hash(files) == entry[0]:
+            out[kernel] = entry[1]
+    return out
 
 
 def peaks():
