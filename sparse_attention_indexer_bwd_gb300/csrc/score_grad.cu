@@ -203,11 +203,13 @@ __global__ void __launch_bounds__(BLOCK) score_grad_generic(ScoreGradArgs a, lon
 }
 
 // ------------------------------------------------------- staged rows ---
-// Persistent variant for sparse rows: a CTA of L/4 threads (rounded up to a
-// warp) owns one row at a time, one float4 of each array per thread.  Thread
-// 0 keeps up to NSTG rows in flight in shared memory (bulk copies of the
-// row's index_score, attn_score and ids, 12 bytes per slot), so HBM streams
-// while the block reduces; dI goes out with 16-byte streaming stores.
+// Persistent variant: a CTA of L/4 threads owns one row at a time, one float4
+// of each array per thread.  Thread 0 keeps up to NSTG rows in flight in
+// shared memory (bulk copies of the row's index_score, attn_score and, for
+// sparse rows, ids: 12 bytes per slot; dense rows copy only their causal
+// prefix of the two score arrays), so HBM streams while the block reduces;
+// dI goes out with 16-byte streaming stores (zeros above a dense row's
+// diagonal).
 constexpr int NSTG = 3;
 
 __device__ __forceinline__ uint32_t sg_smem_u32(const void* p) {
@@ -240,13 +242,17 @@ __device__ __forceinline__ bool sg_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__global__ void score_grad_staged(ScoreGradArgs a) {
+// NV float4 of each array per thread: L = 4 * NV * blockDim.x.
+template <int NV>
+__global__ void __launch_bounds__(512, NV == 1 ? 3 : 2) score_grad_staged(ScoreGradArgs a) {
   extern __shared__ __align__(16) uint8_t sg_smem[];
   __shared__ uint64_t full[NSTG];
   __shared__ float red[32], red2[32];
   const int L = a.L, L4 = L / 4;
+  const bool dense = a.idx == nullptr;
+  (void)L4;
   const uint32_t row_bytes = (uint32_t)L * 4;
-  const uint32_t stage_bytes = 3 * row_bytes;  // I | attn | ids
+  const uint32_t stage_bytes = (dense ? 2 : 3) * row_bytes;  // I | attn [| ids]
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   // zero this CTA's share of dK first
   if (a.dk_zero) {
@@ -269,12 +275,15 @@ __global__ void score_grad_staged(ScoreGradArgs a) {
     const long long r = blockIdx.x + i * G;
     const int s = (int)(i % NSTG);
     const uint32_t dst = sg_smem_u32(sg_smem + s * stage_bytes);
+    // dense rows: only slots 0..t hold scores (rounded up to 16 bytes)
+    const uint32_t bytes =
+        dense ? (uint32_t)(((min(L, (int)(r % a.S_q) + 1) * 4) + 15) & ~15) : row_bytes;
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sg_smem_u32(&full[s])),
-                 "r"(stage_bytes)
+                 "r"((dense ? 2 : 3) * bytes)
                  : "memory");
-    sg_bulk(dst, a.index_score + r * L, row_bytes, &full[s]);
-    sg_bulk(dst + row_bytes, a.attn_score + r * L, row_bytes, &full[s]);
-    sg_bulk(dst + 2 * row_bytes, a.idx + r * L, row_bytes, &full[s]);
+    sg_bulk(dst, a.index_score + r * L, bytes, &full[s]);
+    sg_bulk(dst + row_bytes, a.attn_score + r * L, bytes, &full[s]);
+    if (!dense) sg_bulk(dst + 2 * row_bytes, a.idx + r * L, bytes, &full[s]);
   };
   const long long nrows = (a.rows - blockIdx.x + G - 1) / G;
   if (tid == 0)
@@ -321,13 +330,22 @@ __global__ void score_grad_staged(ScoreGradArgs a) {
     }
     const long long r = blockIdx.x + i * G;
     const uint8_t* st = sg_smem + s * stage_bytes;
-    const bool in = tid < L4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-    int4 id = make_int4(-1, -1, -1, -1);
-    if (in) {
-      x = reinterpret_cast<const float4*>(st)[tid];
-      y = reinterpret_cast<const float4*>(st + row_bytes)[tid];
-      id = reinterpret_cast<const int4*>(st + 2 * row_bytes)[tid];
+    const int lim = dense ? min(L, (int)(r % a.S_q) + 1) : L;  // dense: slots beyond t are padding
+    float xs[NV][4], ys[NV][4];
+    int ids[NV][4];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int v4 = tid + k * (int)blockDim.x;  // this thread's k-th float4 of the row
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+      int4 id = make_int4(-1, -1, -1, -1);
+      if (v4 < L4 && v4 * 4 < lim) {
+        x = reinterpret_cast<const float4*>(st)[v4];
+        y = reinterpret_cast<const float4*>(st + row_bytes)[v4];
+        if (!dense) id = reinterpret_cast<const int4*>(st + 2 * row_bytes)[v4];
+      }
+      xs[k][0] = x.x; xs[k][1] = x.y; xs[k][2] = x.z; xs[k][3] = x.w;
+      ys[k][0] = y.x; ys[k][1] = y.y; ys[k][2] = y.z; ys[k][3] = y.w;
+      ids[k][0] = id.x; ids[k][1] = id.y; ids[k][2] = id.z; ids[k][3] = id.w;
     }
     __syncthreads();  // the stage is free: refill it with row i + NSTG
     if (tid == 0 && issued < nrows) {
@@ -336,34 +354,42 @@ __global__ void score_grad_staged(ScoreGradArgs a) {
       issue(issued);
       ++issued;
     }
-    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-    const int ids[4] = {id.x, id.y, id.z, id.w};
-    bool vv[4];
+    bool vv[NV][4];
     float m = -INFINITY, sa = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      vv[e] = in && (unsigned)ids[e] < (unsigned)a.S_k;
-      if (vv[e]) {
-        m = fmaxf(m, xs[e]);
-        sa += ys[e];
+    for (int k = 0; k < NV; ++k) {
+      const int v4 = tid + k * (int)blockDim.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        vv[k][e] = v4 < L4 && (dense ? v4 * 4 + e < lim : (unsigned)ids[k][e] < (unsigned)a.S_k);
+        if (vv[k][e]) {
+          m = fmaxf(m, xs[k][e]);
+          sa += ys[k][e];
+        }
       }
     }
     block_max_sum(m, sa);
-    float ex[4], z = 0.f;
+    float z = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      ex[e] = vv[e] ? expf(xs[e] - m) : 0.f;
-      z += ex[e];
-    }
+    for (int k = 0; k < NV; ++k)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xs[k][e] = vv[k][e] ? expf(xs[k][e] - m) : 0.f;  // now exp(x - max)
+        z += xs[k][e];
+      }
     z = block_sum(z);
-    if (in) {
-      // one reciprocal per row (the quotients differ from IEEE division by
-      // at most one rounding)
-      const float rz = 1.0f / z, ra = sa != 0.f ? 1.0f / sa : 0.f;
-      float o[4];
+    // one reciprocal per row (the quotients differ from IEEE division by at
+    // most one rounding)
+    const float rz = 1.0f / z, ra = sa != 0.f ? 1.0f / sa : 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[e] = vv[e] ? a.scale * (ex[e] * rz - ys[e] * ra) : 0.f;
-      __stcs(reinterpret_cast<float4*>(a.attn_score + r * L) + tid, make_float4(o[0], o[1], o[2], o[3]));
+    for (int k = 0; k < NV; ++k) {
+      const int v4 = tid + k * (int)blockDim.x;
+      if (v4 < L4) {
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = vv[k][e] ? a.scale * (xs[k][e] * rz - ys[k][e] * ra) : 0.f;
+        __stcs(reinterpret_cast<float4*>(a.attn_score + r * L) + v4, make_float4(o[0], o[1], o[2], o[3]));
+      }
     }
   }
   if (aborted) {
@@ -390,25 +416,34 @@ cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st) {
   const bool aligned = (a.L % 4 == 0) && ((uintptr_t)a.index_score % 16 == 0) &&
                        ((uintptr_t)a.attn_score % 16 == 0) && (!a.idx || (uintptr_t)a.idx % 16 == 0) &&
                        (!a.dk_zero || (uintptr_t)a.dk_zero % 16 == 0);
-  // sparse rows of 128..2048 slots (a multiple of 128): the staged kernel
-  if (aligned && a.idx && a.L % 128 == 0 && a.L >= 128 && a.L <= 2048 && a.status && a.num_sms > 0) {
-    const int threads = a.L / 4;
-    const size_t smem = (size_t)NSTG * 12 * a.L;
+  // rows of 128..2048 slots (sparse) or 128..4096 (dense), a multiple of 128:
+  // the staged kernel (one float4 per thread per array; two beyond 2048 slots)
+  const int lmax = a.idx ? 2048 : 4096;
+  const int nv = a.L > 2048 ? 2 : 1;
+  if (aligned && a.L % (128 * nv) == 0 && a.L >= 128 && a.L <= lmax && a.status && a.num_sms > 0) {
+    const int threads = a.L / (4 * nv);
+    const size_t smem = (size_t)NSTG * (a.idx ? 12 : 8) * a.L;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(score_grad_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(score_grad_staged<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            NSTG * 12 * 2048);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(score_grad_staged<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, NSTG * 8 * 4096);
       if (e != cudaSuccess) return e;
       attr_done[dev] = true;
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged, threads, smem);
+    cudaError_t e = nv == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged<2>, threads, smem)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged<1>, threads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long grid = std::min<long long>(a.rows, (long long)a.num_sms * per_sm);
-    score_grad_staged<<<(unsigned)grid, threads, smem, st>>>(a);
+    if (nv == 2)
+      score_grad_staged<2><<<(unsigned)grid, threads, smem, st>>>(a);
+    else
+      score_grad_staged<1><<<(unsigned)grid, threads, smem, st>>>(a);
     return cudaGetLastError();
   }
   if (aligned) {

@@ -20,6 +20,7 @@ SMALL = [
     W("odd_shapes", 1, 7, 40, 131, 97, 53, "causal", 13),              # H, D, topk not tile multiples
     W("dense_small", 1, 64, 128, 200, 200, 0, "dense", 14),
     W("dense_odd", 2, 5, 24, 77, 77, 0, "dense", 15),
+    W("dense_256", 1, 8, 64, 256, 256, 0, "dense", 16),                # staged dense score-grad rows
 ]
 
 
@@ -66,7 +67,7 @@ def test_gemm_only_matches_oracle_on_same_dI(cases, name):
         assert_close(dq, dw, dk, ref, tag=f"{name} gemm-only mode{mode}")
 
 
-@pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "dense_small"])
+@pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "dense_small", "dense_256"])
 def test_determinism(cases, name):
     wl, x, _ = cases[name]
     runs = [gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC) for _ in range(3)]
