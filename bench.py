@@ -102,6 +102,16 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, td, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if td is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_init(ws, backend):
     import torch.distributed as td
     if ws > 1 and not td.is_initialized():
@@ -348,9 +358,7 @@ def run_ours(args, wl):
     if st != ibwd.IBWD_OK:
         raise SystemExit(f"device status after the timed region: {ibwd.status_string(st)}")
     if td:
-        t = torch.tensor([total_ms], device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, td, dev)
     del attn
 
     flops = wl.flops()
@@ -428,9 +436,7 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
         e_ms = (time.perf_counter() - t0) * 1e3 / ksteps
         if td:
-            t = torch.tensor([e_ms], device=dev)
-            td.all_reduce(t, op=td.ReduceOp.MAX)
-            e_ms = float(t.item())
+            e_ms = max_over_ranks(e_ms, td, dev)
         e2e = {"value": ws * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms, "steps": ksteps,
                "note": "host wall clock over the steps; copies in, compute and copies out of consecutive "
