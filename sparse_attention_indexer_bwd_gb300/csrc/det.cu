@@ -14,6 +14,7 @@
 //   segsum:  dK[s] = sum of the key's u rows, in position order.
 // The result is bitwise identical run to run and overwrites dK.
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -263,15 +264,15 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   int* pos = reinterpret_cast<int*>(ws + lay.pos);
   const size_t sh = (size_t)a.S_k * sizeof(int);       // histogram counters
   const size_t sh_place = sh + (size_t)a.S_k;              // cursors and one-byte tags
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; setting the attribute twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (sh_place > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (sh_place > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   hist_kernel<<<(unsigned)lay.nchunks, 256, sh, st>>>(a, hist);
   const long long nk = (long long)a.B * a.S_k;

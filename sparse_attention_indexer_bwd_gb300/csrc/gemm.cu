@@ -47,6 +47,7 @@
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -963,13 +964,13 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     cudaError_t e = launch_det_sort(a, lay, st);
     if (e != cudaSuccess) return e;
   }
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; setting the attribute twice is harmless
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   KParams p{};
   p.q = a.q;

@@ -20,6 +20,7 @@
 // 32*W threads per row that keeps the row in registers (NV float4 per thread
 // per array).  All reductions are fixed-order (bitwise reproducible).
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 
@@ -423,16 +424,16 @@ cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st) {
   if (aligned && a.L % (128 * nv) == 0 && a.L >= 128 && a.L <= lmax && a.status && a.num_sms > 0) {
     const int threads = a.L / (4 * nv);
     const size_t smem = (size_t)NSTG * (a.idx ? 12 : 8) * a.L;
-    static bool attr_done[64] = {};
+    static std::atomic<bool> attr_done[64];  // per device; setting the attribute twice is harmless
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_acquire)) {
       cudaError_t e = cudaFuncSetAttribute(score_grad_staged<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            NSTG * 12 * 2048);
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(score_grad_staged<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, NSTG * 8 * 4096);
       if (e != cudaSuccess) return e;
-      attr_done[dev] = true;
+      attr_done[dev].store(true, std::memory_order_release);
     }
     int per_sm = 0;
     cudaError_t e = nv == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged<2>, threads, smem)

@@ -200,3 +200,29 @@ def test_abi_rejects_bad_arguments_before_launch():
     torch.cuda.synchronize()
     assert torch.equal(d, before)
     assert ibwd.indexer_bwd_last_device_status() == ibwd.IBWD_OK
+
+
+def test_two_host_threads_two_streams(cases):
+    # concurrent calls from two host threads, each on its own stream with its
+    # own workspace and outputs, give the single-call results (dq, dw and the
+    # deterministic dK bitwise)
+    import threading
+    wl, x, _ = cases["multi_tile_ragged"]
+    ref = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC)
+    results = [None, None]
+
+    def work(slot):
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            results[slot] = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC)
+        s.synchronize()
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    for got in results:
+        assert got is not None
+        for a, b in zip(got, ref):
+            assert np.array_equal(a.view(np.int32), b.view(np.int32))
