@@ -206,38 +206,6 @@ def run_reference(args, wl):
 
 # ---------------------------------------------------------------- GPU arm ---
 
-def forward_logits(torch, q, k, w, idx, S_k, chunk=256):
-    """Input preparation: index_score = sum_h w relu(q.k_sel) per valid slot,
-    computed with plain torch ops in fp32 (not part of the timed path)."""
-    B, S_q, H, D = q.shape
-    out = torch.zeros(idx.shape, dtype=torch.float32, device=q.device)
-    for b in range(B):
-        for t0 in range(0, S_q, chunk):
-            ids = idx[b, t0:t0 + chunk].long()
-            valid = (ids >= 0) & (ids < S_k)
-            kg = k[b][ids.clamp(0, S_k - 1)].float()                # [c, topk, D]
-            z = torch.einsum("chd,ctd->cht", q[b, t0:t0 + chunk].float(), kg)
-            I = torch.einsum("ch,cht->ct", w[b, t0:t0 + chunk], torch.relu(z))
-            out[b, t0:t0 + chunk] = torch.where(valid, I, torch.zeros_like(I))
-    return out
-
-
-def forward_logits_dense(torch, q, k, w, chunk=128):
-    """Input preparation for the dense-causal variant: index_score[t, s] =
-    sum_h w relu(q.k) for s <= t, 0 above the diagonal (plain torch, fp32)."""
-    B, S, H, D = q.shape
-    out = torch.zeros((B, S, S), dtype=torch.float32, device=q.device)
-    for b in range(B):
-        kf = k[b].float()
-        for t0 in range(0, S, chunk):
-            z = torch.einsum("chd,sd->chs", q[b, t0:t0 + chunk].float(), kf)
-            I = torch.einsum("ch,chs->cs", w[b, t0:t0 + chunk], torch.relu(z))
-            t = torch.arange(t0, min(S, t0 + chunk), device=q.device)[:, None]
-            s_ = torch.arange(S, device=q.device)[None, :]
-            out[b, t0:t0 + chunk] = torch.where(s_ <= t, I, torch.zeros_like(I))
-    return out
-
-
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -295,7 +263,8 @@ def run_ours(args, wl):
     w = torch.from_numpy(x["w"]).to(dev)
     idx = None if wl.dense else torch.from_numpy(x["idx"]).to(dev)
     attn0 = torch.from_numpy(x["attn"]).to(dev)
-    I = forward_logits_dense(torch, q, k, w) if wl.dense else forward_logits(torch, q, k, w, idx, wl.S_k)
+    # index_score: the forward of the same q, k, w (input preparation, untimed)
+    I = ibwd.indexer_fwd_dense(q, k, w) if wl.dense else ibwd.indexer_fwd(q, k, w, idx)
     B, S_q, H, D = q.shape
     dq = torch.empty((B, S_q, H, D), dtype=torch.float32, device=dev)
     dw = torch.empty((B, S_q, H), dtype=torch.float32, device=dev)
@@ -442,6 +411,27 @@ def run_ours(args, wl):
                "note": "host wall clock over the steps; copies in, compute and copies out of consecutive "
                        "steps overlap on three streams"}
 
+    # the forward kernel on its own (not part of the step): CUDA events around
+    # each launch, inputs resident
+    fwd_flops = (2.0 * wl.B * wl.H * wl.D * wl.S_q * (wl.S_q + 1) / 2.0 if wl.dense else
+                 2.0 * wl.B * wl.S_q * wl.topk * wl.H * wl.D)
+    fwd_ms = []
+    for it in range(13):
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        if wl.dense:
+            ibwd.indexer_fwd_dense(q, k, w, out=I, stream=stream)
+        else:
+            ibwd.indexer_fwd(q, k, w, idx, out=I, stream=stream)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        if it >= 3:
+            fwd_ms.append(f0.elapsed_time(f1))
+    fwd_avg = statistics.mean(fwd_ms)
+    forward = {"us": 1e3 * fwd_avg, "tflops": fwd_flops / (fwd_avg * 1e-3) / 1e12,
+               "note": "forward kernel alone (index_score), 2*slots*H*D FLOP; not part of the step"}
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not wl.dense:
         cpu = cpu_baseline(wl, x, I.cpu().numpy(), args.cpu_seconds)
@@ -453,7 +443,7 @@ def run_ours(args, wl):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 tensor-core operands, fp32 accumulate (bf16 inputs)",
-        "data": "synthetic (seeded; index_score = forward logits of the seeded q, k, w)",
+        "data": "synthetic (seeded; index_score = this library's forward of the seeded q, k, w)",
         "config": {"workload": f"{wl.name}: B={wl.B} H={wl.H} D={wl.D} S_q={wl.S_q} S_k={wl.S_k} "
                                + ("every causal key (dense)" if wl.dense else f"topk={wl.topk}, {wl.ids} top-k ids"),
                    "dk_mode": args.mode, "l2": "inputs larger than L2 (q alone is 134 MB); "
@@ -470,6 +460,7 @@ def run_ours(args, wl):
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                                 "frac": sg_bytes / (sg_avg * 1e-3) / 1e9 / pk["hbm_gbs"],
                                 "traffic": traffic.get("score_grad"), "algorithmic_bytes": sg_bytes},
+        "forward": forward,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,

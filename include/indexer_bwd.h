@@ -150,6 +150,26 @@ IBWD_API int indexer_bwd_gemm_noalloc(const uint16_t* q, const uint16_t* k, cons
                              const int32_t* topk_idx, float* dq, float* dw, float* dk, int B, int S_q,
                              int S_k, int H, int D, int topk, void* stream);
 
+/*
+ * Forward of the indexer: the logits the backward differentiates (#730
+ * benchmark harness: one shared key head scored against every indexer head
+ * of the query, weighted and summed),
+ *   index_score[t,j] = sum_h w[t,h] relu(q[t,h,:] . k[s,:]),  s = topk_idx[t,j],
+ * written as 0 on padding slots (any id outside [0, S_k)).  The same shapes,
+ * layouts and limits as indexer_bwd_gemm:
+ *   q bf16 [B,S_q,H,D];  k bf16 [B,S_k,D];  w fp32 [B,S_q,H];
+ *   topk_idx int32 [B,S_q,topk];  index_score fp32 [B,S_q,topk], fully written.
+ * Products of the bf16 inputs are exact and summed in fp32 (tensor cores).
+ * No workspace.
+ */
+IBWD_API int indexer_fwd(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* topk_idx,
+                         float* index_score, int B, int S_q, int S_k, int H, int D, int topk, void* stream);
+
+/* Dense variant of the forward: every key s <= t; index_score fp32 [B,S,S]
+ * (entry [t,s]), 0 above the diagonal. */
+IBWD_API int indexer_fwd_dense(const uint16_t* q, const uint16_t* k, const float* w, float* index_score, int B,
+                               int S, int H, int D, void* stream);
+
 /* Synchronizes `stream`, then reads and clears this device's status word:
  * IBWD_ERR_TIMEOUT if a kernel's bounded wait expired, IBWD_ERR_BAD_INDEX if a
  * device bounds check failed, IBWD_ERR_CUDA if the stream reports an error,

@@ -39,6 +39,8 @@ EXPORTS = (
     "indexer_bwd_last_device_status",
     "indexer_bwd_status_string",
     "indexer_bwd_gemm_noalloc",
+    "indexer_fwd",
+    "indexer_fwd_dense",
 )
 
 
@@ -77,6 +79,10 @@ def load() -> ctypes.CDLL:
     lib.indexer_bwd_dense_gemm_workspace_size.restype = sz
     lib.indexer_bwd_dense_gemm.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p]
     lib.indexer_bwd_dense_gemm.restype = i
+    lib.indexer_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
+    lib.indexer_fwd.restype = i
+    lib.indexer_fwd_dense.argtypes = [p, p, p, p, i, i, i, i, p]
+    lib.indexer_fwd_dense.restype = i
     lib.indexer_bwd_last_device_status.argtypes = [p]
     lib.indexer_bwd_last_device_status.restype = i
     lib.indexer_bwd_status_string.argtypes = [i]
@@ -205,6 +211,36 @@ def indexer_bwd_status_string(status: int) -> str:
 
 
 # --------------------------------------------------------------- pipeline ---
+
+def indexer_fwd(q, k, w, topk_idx, out=None, stream=None):
+    """Forward logits index_score[t,j] = sum_h w relu(q[t,h].k[topk_idx[t,j]]) (0 on padding)."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k, torch.bfloat16, 3, "k")
+    _need(w, torch.float32, 3, "w")
+    _need(topk_idx, torch.int32, 3, "topk_idx")
+    B, S_q, H, D = q.shape
+    S_k = k.shape[1]
+    topk = topk_idx.shape[-1]
+    if out is None:
+        out = torch.empty((B, S_q, topk), dtype=torch.float32, device=q.device)
+    rc = load().indexer_fwd(_ptr(q), _ptr(k), _ptr(w), _ptr(topk_idx), _ptr(out), B, S_q, S_k, H, D, topk,
+                            _stream(stream))
+    _check(rc, "indexer_fwd")
+    return out
+
+
+def indexer_fwd_dense(q, k, w, out=None, stream=None):
+    """Dense forward: index_score[t,s] for every key s <= t, 0 above the diagonal ([B,S,S])."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k, torch.bfloat16, 3, "k")
+    _need(w, torch.float32, 3, "w")
+    B, S, H, D = q.shape
+    if out is None:
+        out = torch.empty((B, S, S), dtype=torch.float32, device=q.device)
+    rc = load().indexer_fwd_dense(_ptr(q), _ptr(k), _ptr(w), _ptr(out), B, S, H, D, _stream(stream))
+    _check(rc, "indexer_fwd_dense")
+    return out
+
 
 def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale: float = 1.0,
                      dk_mode=IBWD_DK_ATOMIC, workspace=None, out=None, stream=None):

@@ -148,6 +148,39 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
 
 }  // namespace
 
+// The forward: index_score from q, k, w (and topk_idx unless dense).
+int fwd_common(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* idx, bool need_idx, float* out,
+               int B, int S_q, int S_k, int H, int D, int L, void* stream) {
+  if (B < 1 || S_q < 1 || S_k < 1 || L < 1 || H < 1 || D < 1) return IBWD_ERR_INVALID_ARG;
+  if (!shape_ok(B, S_q, S_k, H, D, L)) return IBWD_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, w, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return IBWD_ERR_INVALID_ARG;
+  if (need_idx && !aligned16(idx)) return IBWD_ERR_INVALID_ARG;
+  DeviceInfo* dv = nullptr;
+  int rc = device_info(&dv);
+  if (rc) return rc;
+  for (const void* p : ptrs)
+    if (!dev_ptr_ok(p)) return IBWD_ERR_INVALID_ARG;
+  if (idx && !dev_ptr_ok(idx)) return IBWD_ERR_INVALID_ARG;
+  ibwd::FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.w = w;
+  a.idx = idx;
+  a.out = out;
+  a.B = B;
+  a.S_q = S_q;
+  a.S_k = S_k;
+  a.H = H;
+  a.D = D;
+  a.L = L;
+  a.status = dv->status;
+  a.num_sms = dv->num_sms;
+  cudaError_t e = ibwd::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
+}
+
 extern "C" {
 
 int indexer_bwd_score_grad(const float* index_score, float* attn_score, const int32_t* topk_idx, int B,
@@ -182,6 +215,17 @@ int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const float* w,
                            size_t workspace_bytes, void* stream) {
   return gemm_common(q, k, w, dI, nullptr, false, dq, dw, dk, B, S, S, H, D, S, dk_mode, workspace,
                      workspace_bytes, stream);
+}
+
+int indexer_fwd(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* topk_idx, float* index_score,
+                int B, int S_q, int S_k, int H, int D, int topk, void* stream) {
+  if (!topk_idx) return IBWD_ERR_INVALID_ARG;
+  return fwd_common(q, k, w, topk_idx, true, index_score, B, S_q, S_k, H, D, topk, stream);
+}
+
+int indexer_fwd_dense(const uint16_t* q, const uint16_t* k, const float* w, float* index_score, int B, int S, int H,
+                      int D, void* stream) {
+  return fwd_common(q, k, w, nullptr, false, index_score, B, S, S, H, D, S, stream);
 }
 
 int indexer_bwd_last_device_status(void* stream) {

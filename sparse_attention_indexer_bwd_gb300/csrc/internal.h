@@ -59,4 +59,16 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 
+struct FwdArgs {
+  const uint16_t* q;     // bf16 [rows, H, D]
+  const uint16_t* k;     // bf16 [B, S_k, D]
+  const float* w;        // [rows, H]
+  const int32_t* idx;    // [rows, L] or nullptr (dense: key j of row t is valid iff j <= t)
+  float* out;            // index_score [rows, L]
+  int B, S_q, S_k, H, D, L;
+  unsigned* status;
+  int num_sms;
+};
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t st);
+
 }  // namespace ibwd
