@@ -82,3 +82,26 @@ def test_forward_anchor_sampled_rows():
     rows = np.sort(np.random.default_rng(3).permutation(wl.S_q)[:96])
     ref = oracle.forward_sparse(x["q"][:, rows], x["k"], x["w"][:, rows], x["idx"][:, rows], wl.S_k)
     assert max_rel(got[:, rows], ref) <= TOL_FWD
+
+
+@pytest.mark.parametrize("name", ["multi_tile_ragged", "dense_small"])
+def test_forward_then_backward_against_the_oracle_pipeline(name):
+    # this library's forward feeding its own backward, against the oracle's
+    # forward and backward on the same inputs (tolerances of the backward)
+    from gpu_util import TOL_DI, assert_close, oracle_all
+    wl = next(c for c in CASES if c.name == name)
+    x = synth.make_inputs(wl)
+    q, k, w = t_bf16(x["q"]), t_bf16(x["k"]), t_f32(x["w"])
+    attn = t_f32(x["attn"])
+    if wl.dense:
+        I = ibwd.indexer_fwd_dense(q, k, w)
+        dq, dw, dk = ibwd.indexer_backward(q, k, w, I, attn, None)
+    else:
+        idx = t_i32(x["idx"])
+        I = ibwd.indexer_fwd(q, k, w, idx)
+        dq, dw, dk = ibwd.indexer_backward(q, k, w, I, attn, idx)
+    assert ibwd.indexer_bwd_last_device_status() == ibwd.IBWD_OK
+    x["I"] = ref_fwd(wl, x).astype(np.float32)
+    ref = oracle_all(wl, x)
+    assert max_rel(attn.cpu().numpy(), ref[0]) <= TOL_DI
+    assert_close(dq.cpu().numpy(), dw.cpu().numpy(), dk.cpu().numpy(), ref[1:], tag=f"pipeline/{name}")
