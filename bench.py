@@ -328,6 +328,26 @@ def run_ours(args, wl):
         raise SystemExit(f"device status after the timed region: {ibwd.status_string(st)}")
     if td:
         total_ms = max_over_ranks(total_ms, td, dev)
+
+    # the same steps through the one-call backward (indexer_bwd: the two
+    # kernels queued by one call, the later ones launched programmatically)
+    for a in attn:
+        a.copy_(attn0)
+    torch.cuda.synchronize()
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        ibwd.indexer_backward(q, k, w, I, attn[i], idx, dk_mode=mode, workspace=wsb, out=(dq, dw, dk), stream=stream)
+    w0.record(stream)
+    for i in range(args.steps):
+        ibwd.indexer_backward(q, k, w, I, attn[args.warmup + i], idx, dk_mode=mode, workspace=wsb,
+                              out=(dq, dw, dk), stream=stream)
+    w1.record(stream)
+    torch.cuda.synchronize()
+    whole_ms = w0.elapsed_time(w1) / args.steps
+    st = ibwd.indexer_bwd_last_device_status(stream)
+    if st != ibwd.IBWD_OK:
+        raise SystemExit(f"device status after the one-call steps: {ibwd.status_string(st)}")
     del attn
 
     flops = wl.flops()
@@ -460,6 +480,9 @@ def run_ours(args, wl):
                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                                 "frac": sg_bytes / (sg_avg * 1e-3) / 1e9 / pk["hbm_gbs"],
                                 "traffic": traffic.get("score_grad"), "algorithmic_bytes": sg_bytes},
+        "whole_call": {"us_per_step": 1e3 * whole_ms, "tflops": flops / (whole_ms * 1e-3) / 1e12,
+                       "steps": args.steps,
+                       "note": "the same steps through indexer_bwd (one call per step), timed after the region above"},
         "forward": forward,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

@@ -151,6 +151,31 @@ IBWD_API int indexer_bwd_gemm_noalloc(const uint16_t* q, const uint16_t* k, cons
                              int S_k, int H, int D, int topk, void* stream);
 
 /*
+ * The whole backward in one call: kernel 1 then kernel 2 above, queued on the
+ * same stream (the #730 harness runs them as a pair; the arguments keep the
+ * meanings given above).
+ *   index_score  fp32 [B,S_q,topk], read only
+ *   attn_score   fp32 [B,S_q,topk]: read, then overwritten by dI
+ *   dq, dw       written;  dk  written in both modes (zeroed first in
+ *                IBWD_DK_ATOMIC mode by kernel 1, as through dk_to_zero)
+ *   workspace    at least indexer_bwd_gemm_workspace_size bytes (same shapes
+ *                and dk_mode)
+ * The results are bitwise those of the two calls.  Every check of both calls
+ * happens before either kernel is launched.
+ */
+IBWD_API int indexer_bwd(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                         float* attn_score, const int32_t* topk_idx, float* dq, float* dw, float* dk, int B,
+                         int S_q, int S_k, int H, int D, int topk, float grad_scale, int dk_mode,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dense variant of indexer_bwd: every key s <= t, S_q = S_k = S, scores
+ * [B,S,S]; workspace of indexer_bwd_dense_gemm_workspace_size bytes. */
+IBWD_API int indexer_bwd_dense(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                               float* attn_score, float* dq, float* dw, float* dk, int B, int S, int H, int D,
+                               float grad_scale, int dk_mode, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
  * Forward of the indexer: the logits the backward differentiates (#730
  * benchmark harness: one shared key head scored against every indexer head
  * of the query, weighted and summed),

@@ -41,6 +41,8 @@ EXPORTS = (
     "indexer_bwd_gemm_noalloc",
     "indexer_fwd",
     "indexer_fwd_dense",
+    "indexer_bwd",
+    "indexer_bwd_dense",
 )
 
 
@@ -79,6 +81,10 @@ def load() -> ctypes.CDLL:
     lib.indexer_bwd_dense_gemm_workspace_size.restype = sz
     lib.indexer_bwd_dense_gemm.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, p, sz, p]
     lib.indexer_bwd_dense_gemm.restype = i
+    lib.indexer_bwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, p, sz, p]
+    lib.indexer_bwd.restype = i
+    lib.indexer_bwd_dense.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, f, i, p, sz, p]
+    lib.indexer_bwd_dense.restype = i
     lib.indexer_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
     lib.indexer_fwd.restype = i
     lib.indexer_fwd_dense.argtypes = [p, p, p, p, i, i, i, i, p]
@@ -242,9 +248,58 @@ def indexer_fwd_dense(q, k, w, out=None, stream=None):
     return out
 
 
+def indexer_bwd(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale: float = 1.0,
+                dk_mode=IBWD_DK_ATOMIC, workspace=None, stream=None):
+    """The whole backward in one call (the score-grad kernel, then the gemm
+    stage): dI over attn_score; dq, dw and dk all written."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k, torch.bfloat16, 3, "k")
+    _need(w, torch.float32, 3, "w")
+    _need(index_score, torch.float32, 3, "index_score")
+    _need(attn_score, torch.float32, 3, "attn_score")
+    _need(topk_idx, torch.int32, 3, "topk_idx")
+    _need(dq, torch.float32, 4, "dq")
+    _need(dw, torch.float32, 3, "dw")
+    _need(dk, torch.float32, 3, "dk")
+    B, S_q, H, D = q.shape
+    S_k = k.shape[1]
+    topk = topk_idx.shape[-1]
+    if workspace is None:
+        workspace = torch.empty(indexer_bwd_gemm_workspace_size(B, S_q, S_k, H, D, topk, dk_mode),
+                                dtype=torch.uint8, device=q.device)
+    rc = load().indexer_bwd(_ptr(q), _ptr(k), _ptr(w), _ptr(index_score), _ptr(attn_score), _ptr(topk_idx),
+                            _ptr(dq), _ptr(dw), _ptr(dk), B, S_q, S_k, H, D, topk, float(grad_scale),
+                            int(dk_mode), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream))
+    _check(rc, "indexer_bwd")
+
+
+def indexer_bwd_dense(q, k, w, index_score, attn_score, dq, dw, dk, grad_scale: float = 1.0,
+                      dk_mode=IBWD_DK_ATOMIC, workspace=None, stream=None):
+    """Dense variant of indexer_bwd ([B,S,S] scores, every key s <= t)."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k, torch.bfloat16, 3, "k")
+    _need(w, torch.float32, 3, "w")
+    _need(index_score, torch.float32, 3, "index_score")
+    _need(attn_score, torch.float32, 3, "attn_score")
+    _need(dq, torch.float32, 4, "dq")
+    _need(dw, torch.float32, 3, "dw")
+    _need(dk, torch.float32, 3, "dk")
+    B, S, H, D = q.shape
+    if workspace is None:
+        workspace = torch.empty(indexer_bwd_dense_gemm_workspace_size(B, S, H, D, dk_mode),
+                                dtype=torch.uint8, device=q.device)
+    rc = load().indexer_bwd_dense(_ptr(q), _ptr(k), _ptr(w), _ptr(index_score), _ptr(attn_score), _ptr(dq),
+                                  _ptr(dw), _ptr(dk), B, S, H, D, float(grad_scale), int(dk_mode),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check(rc, "indexer_bwd_dense")
+
+
 def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale: float = 1.0,
                      dk_mode=IBWD_DK_ATOMIC, workspace=None, out=None, stream=None):
-    """Both kernels: dI over attn_score (index_score is kept), then dq, dw, dk.
+    """The whole backward (indexer_bwd / indexer_bwd_dense): dI over
+    attn_score (index_score is kept), then dq, dw, dk.
 
     topk_idx=None selects the dense-causal variant ([B,S,S] scores).
     `out` may supply preallocated (dq, dw, dk) fp32 tensors.
@@ -258,11 +313,9 @@ def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale
         dk = torch.empty((B, S_k, D), dtype=torch.float32, device=q.device)
     else:
         dq, dw, dk = out
-    zero_dk = dk if dk_mode == IBWD_DK_ATOMIC else None
     if topk_idx is None:
-        indexer_bwd_dense_score_grad(index_score, attn_score, grad_scale, zero_dk, stream)
-        indexer_bwd_dense_gemm(q, k, w, attn_score, dq, dw, dk, dk_mode, workspace, stream)
+        indexer_bwd_dense(q, k, w, index_score, attn_score, dq, dw, dk, grad_scale, dk_mode, workspace, stream)
     else:
-        indexer_bwd_score_grad(index_score, attn_score, topk_idx, S_k, grad_scale, zero_dk, stream)
-        indexer_bwd_gemm(q, k, w, attn_score, topk_idx, dq, dw, dk, dk_mode, workspace, stream)
+        indexer_bwd(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale, dk_mode, workspace,
+                    stream)
     return dq, dw, dk

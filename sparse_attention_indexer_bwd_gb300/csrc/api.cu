@@ -101,9 +101,16 @@ size_t workspace_common(int B, int S_q, int S_k, int H, int D, int L, int mode) 
 }
 
 // need_idx: the sparse variant requires topk_idx (the dense one passes NULL).
+// With I (index_score) given this is the whole backward: the score-grad
+// kernel writes dI (from I and the attn_score in the dI buffer) over that
+// buffer and zeroes dk in atomic mode, then the gemm stage runs, its kernels
+// launched programmatically behind the score-grad (cudnn-frontend #730
+// commit list: score-grad and GEMM overlapped through programmatic dependent
+// launch); every check of both happens before either is launched.
 int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const float* dI, const int32_t* idx,
                 bool need_idx, float* dq, float* dw, float* dk, int B, int S_q, int S_k, int H, int D, int L,
-                int mode, void* ws, size_t ws_bytes, void* stream) {
+                int mode, void* ws, size_t ws_bytes, void* stream, const float* I = nullptr,
+                float grad_scale = 0.f) {
   if (mode != IBWD_DK_ATOMIC && mode != IBWD_DK_DETERMINISTIC) return IBWD_ERR_INVALID_ARG;
   if (B < 1 || S_q < 1 || S_k < 1 || L < 1 || H < 1 || D < 1) return IBWD_ERR_INVALID_ARG;
   if (!shape_ok(B, S_q, S_k, H, D, L)) return IBWD_ERR_UNSUPPORTED;
@@ -113,6 +120,8 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   for (const void* p : ptrs)
     if (!aligned16(p)) return IBWD_ERR_INVALID_ARG;
   if (need_idx && !aligned16(idx)) return IBWD_ERR_INVALID_ARG;
+  if (I && (!aligned16(I) || static_cast<const void*>(I) == static_cast<const void*>(dI)))
+    return IBWD_ERR_INVALID_ARG;
   if (!aligned16(ws)) return IBWD_ERR_WORKSPACE;
   DeviceInfo* dv = nullptr;
   int rc = device_info(&dv);
@@ -120,6 +129,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   for (const void* p : ptrs)
     if (!dev_ptr_ok(p)) return IBWD_ERR_INVALID_ARG;
   if (idx && !dev_ptr_ok(idx)) return IBWD_ERR_INVALID_ARG;
+  if (I && !dev_ptr_ok(I)) return IBWD_ERR_INVALID_ARG;
   const size_t need = ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC).total;
   if (!ws || ws_bytes < need || !dev_ptr_ok(ws)) return IBWD_ERR_WORKSPACE;
   ibwd::GemmArgs a{};
@@ -142,6 +152,12 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.ws_bytes = ws_bytes;
   a.status = dv->status;
   a.num_sms = dv->num_sms;
+  if (I) {
+    rc = score_grad_common(I, const_cast<float*>(dI), idx, need_idx, B, S_q, S_k, L, grad_scale,
+                           mode == IBWD_DK_ATOMIC ? dk : nullptr, D, stream);
+    if (rc) return rc;
+    a.after_score_grad = 1;
+  }
   cudaError_t e = ibwd::launch_gemm(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
 }
@@ -215,6 +231,22 @@ int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const float* w,
                            size_t workspace_bytes, void* stream) {
   return gemm_common(q, k, w, dI, nullptr, false, dq, dw, dk, B, S, S, H, D, S, dk_mode, workspace,
                      workspace_bytes, stream);
+}
+
+int indexer_bwd(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score, float* attn_score,
+                const int32_t* topk_idx, float* dq, float* dw, float* dk, int B, int S_q, int S_k, int H, int D,
+                int topk, float grad_scale, int dk_mode, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!index_score || !topk_idx) return IBWD_ERR_INVALID_ARG;
+  return gemm_common(q, k, w, attn_score, topk_idx, true, dq, dw, dk, B, S_q, S_k, H, D, topk, dk_mode, workspace,
+                     workspace_bytes, stream, index_score, grad_scale);
+}
+
+int indexer_bwd_dense(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                      float* attn_score, float* dq, float* dw, float* dk, int B, int S, int H, int D,
+                      float grad_scale, int dk_mode, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!index_score) return IBWD_ERR_INVALID_ARG;
+  return gemm_common(q, k, w, attn_score, nullptr, false, dq, dw, dk, B, S, S, H, D, S, dk_mode, workspace,
+                     workspace_bytes, stream, index_score, grad_scale);
 }
 
 int indexer_fwd(const uint16_t* q, const uint16_t* k, const float* w, const int32_t* topk_idx, float* index_score,

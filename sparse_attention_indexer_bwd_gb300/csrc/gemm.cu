@@ -855,6 +855,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   __syncthreads();
   tc_fence_after();
   cx.tmem = *tmem_slot;
+  // everything above overlaps the previous kernel's tail (programmatic
+  // dependent launch); the inputs it wrote are read only from here on
+  griddep_wait();
   TRACE_CTA(0);
 
   if (warp < W_SCAN) {
@@ -880,8 +883,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
 
 // k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
 // row S_k of each batch zero (padding rows of a tile copy it).
+// Launched programmatically after the score-grad kernel (which writes neither
+// k nor the workspace), it runs alongside it and waits for it before exiting,
+// so that its own completion implies the score-grad's.
 __global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16, int B, int S_k, int D,
                                 unsigned* __restrict__ sched) {
+  griddep_launch_dependents();  // the gemm kernel may start its prologue
   if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the gemm kernel's row counter
   const long long rows = (long long)B * (S_k + 1);
   const long long n = rows * (kDP / 8);
@@ -896,6 +903,26 @@ __global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restri
     *reinterpret_cast<uint4*>(k16 + row * kDP + ch * 8) =
         make_uint4(bf16x2_to_half2(val.x), bf16x2_to_half2(val.y), bf16x2_to_half2(val.z), bf16x2_to_half2(val.w));
   }
+  griddep_wait();
+}
+
+// Launch with programmatic stream serialization when pdl is set: the kernel
+// may start before the previous one on the stream completes and must call
+// griddep_wait() before reading what that one writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                      bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
 unsigned long long gcd_u64(unsigned long long a, unsigned long long b) {
@@ -956,8 +983,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   {
     const long long n = (long long)a.B * (a.S_k + 1) * (kDP / 8);
     const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * a.num_sms);
-    k_to_f16_kernel<<<blocks, 256, 0, st>>>(a.k, k16, a.B, a.S_k, a.D, sched);
-    cudaError_t e = cudaGetLastError();
+    // programmatic only right after this library's score-grad kernel: the
+    // kernel reads k before it waits for its predecessor
+    cudaError_t e = launch_ex(k_to_f16_kernel, (unsigned)blocks, 256u, 0, st, a.after_score_grad != 0, a.k, k16,
+                              a.B, a.S_k, a.D, sched);
     if (e != cudaSuccess) return e;
   }
   if (a.deterministic) {
@@ -1001,8 +1030,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const bool al = (a.L % 4 == 0) && ((uintptr_t)a.dI % 16 == 0) && (p.dense || (uintptr_t)a.idx % 16 == 0);
   p.staged = fits && al;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
-  gemm_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_ex(gemm_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
   if (e != cudaSuccess) return e;
   if (a.deterministic) return launch_det_segsum(a, lay, st);
   return cudaSuccess;

@@ -43,6 +43,7 @@ struct GemmArgs {
   size_t ws_bytes;
   unsigned* status;      // device status word
   int num_sms;
+  int after_score_grad;  // queued right after this library's score-grad kernel (same stream)
 };
 
 struct WsLayout {

@@ -29,6 +29,11 @@ namespace {
 
 constexpr int BLOCK = 256;
 
+// Lets the kernel queued after this one, when it is launched with
+// programmatic stream serialization, start launching now; it still waits for
+// this grid to complete before it reads anything this grid writes.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 template <int W>
 struct RowReduce {
   // Sum/max over the row group (W warps) in a fixed order.
@@ -63,6 +68,7 @@ struct RowReduce {
 // NV float4 per thread per array; W warps per row; BLOCK/(32W) rows per block.
 template <int NV, int W>
 __global__ void __launch_bounds__(BLOCK) score_grad_vec(ScoreGradArgs a, long long row_blocks) {
+  allow_dependent_launch();
   __shared__ float red[BLOCK / 32];
   constexpr int G = 32 * W;                 // threads per row
   constexpr int RPB = BLOCK / G;            // rows per block
@@ -152,6 +158,7 @@ __global__ void __launch_bounds__(BLOCK) score_grad_vec(ScoreGradArgs a, long lo
 
 // Any row length: one block per row, three strided passes.
 __global__ void __launch_bounds__(BLOCK) score_grad_generic(ScoreGradArgs a, long long row_blocks) {
+  allow_dependent_launch();
   __shared__ float red[BLOCK / 32];
   if ((long long)blockIdx.x >= row_blocks) {
     if (a.dk_zero) {
@@ -246,6 +253,7 @@ __device__ __forceinline__ bool sg_wait(uint64_t* bar, uint32_t parity) {
 // NV float4 of each array per thread: L = 4 * NV * blockDim.x.
 template <int NV>
 __global__ void __launch_bounds__(512, NV == 1 ? 3 : 2) score_grad_staged(ScoreGradArgs a) {
+  allow_dependent_launch();
   extern __shared__ __align__(16) uint8_t sg_smem[];
   __shared__ uint64_t full[NSTG];
   __shared__ float red[32], red2[32];

@@ -65,12 +65,30 @@ def oracle_all(wl, x, grad_scale=1.0):
     return dI, dq, dw, dk
 
 
-def gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_ATOMIC, grad_scale=1.0):
-    """Both kernels through the C ABI; returns numpy (dI, dq, dw, dk)."""
+def gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_ATOMIC, grad_scale=1.0, path="whole"):
+    """The backward through the C ABI; returns numpy (dI, dq, dw, dk).
+
+    path "whole": one indexer_bwd / indexer_bwd_dense call; "pair": the
+    score-grad call, then the gemm call."""
     q, k, w = t_bf16(x["q"]), t_bf16(x["k"]), t_f32(x["w"])
     I, attn = t_f32(x["I"]), t_f32(x["attn"])
     idx = None if wl.dense else t_i32(x["idx"])
-    dq, dw, dk = ibwd.indexer_backward(q, k, w, I, attn, idx, grad_scale=grad_scale, dk_mode=dk_mode)
+    if path == "whole":
+        dq, dw, dk = ibwd.indexer_backward(q, k, w, I, attn, idx, grad_scale=grad_scale, dk_mode=dk_mode)
+    else:
+        assert path == "pair"
+        B, S_q, H, D = x["q"].shape
+        S_k = x["k"].shape[1]
+        dq = torch.full((B, S_q, H, D), float("nan"), device=dev())
+        dw = torch.full((B, S_q, H), float("nan"), device=dev())
+        dk = torch.full((B, S_k, D), float("nan"), device=dev())
+        zero = dk if dk_mode == ibwd.IBWD_DK_ATOMIC else None
+        if wl.dense:
+            ibwd.indexer_bwd_dense_score_grad(I, attn, grad_scale, zero)
+            ibwd.indexer_bwd_dense_gemm(q, k, w, attn, dq, dw, dk, dk_mode)
+        else:
+            ibwd.indexer_bwd_score_grad(I, attn, idx, S_k, grad_scale, zero)
+            ibwd.indexer_bwd_gemm(q, k, w, attn, idx, dq, dw, dk, dk_mode)
     st = ibwd.indexer_bwd_last_device_status()
     assert st == ibwd.IBWD_OK, ibwd.status_string(st)
     # index_score is read only (bitwise: it may hold NaN on padded slots)

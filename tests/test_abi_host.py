@@ -68,6 +68,10 @@ def test_shape_errors_need_no_device(lib):
                                 None) == ibwd.IBWD_ERR_UNSUPPORTED
     assert lib.indexer_bwd_dense_gemm(None, None, None, None, None, None, None, 1, 4, 4, 136, 0, None, 0,
                                       None) == ibwd.IBWD_ERR_UNSUPPORTED
+    assert lib.indexer_bwd(None, None, None, None, None, None, None, None, None, 1, 4, 4, 4, 32, 4, 1.0, 3, None, 0,
+                           None) == ibwd.IBWD_ERR_INVALID_ARG
+    assert lib.indexer_bwd(None, None, None, None, None, None, None, None, None, 1, 4, 4, 100, 32, 4, 1.0, 0, None,
+                           0, None) == ibwd.IBWD_ERR_INVALID_ARG
 
 
 def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):

@@ -35,11 +35,12 @@ def cases():
 
 @pytest.mark.parametrize("name", [w.name for w in SMALL])
 @pytest.mark.parametrize("mode", [ibwd.IBWD_DK_ATOMIC, ibwd.IBWD_DK_DETERMINISTIC])
-def test_full_path_matches_oracle(cases, name, mode):
+@pytest.mark.parametrize("path", ["whole", "pair"])
+def test_full_path_matches_oracle(cases, name, mode, path):
     wl, x, ref = cases[name]
-    dI, dq, dw, dk = gpu_all(wl, x, dk_mode=mode)
+    dI, dq, dw, dk = gpu_all(wl, x, dk_mode=mode, path=path)
     assert max_rel(dI, ref[0]) <= TOL_DI
-    assert_close(dq, dw, dk, ref[1:], tag=f"{name}/mode{mode}")
+    assert_close(dq, dw, dk, ref[1:], tag=f"{name}/mode{mode}/{path}")
 
 
 @pytest.mark.parametrize("name", [w.name for w in SMALL])
@@ -68,8 +69,23 @@ def test_gemm_only_matches_oracle_on_same_dI(cases, name):
 
 
 @pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "dense_small", "dense_256"])
+def test_whole_call_equals_the_pair_of_calls(cases, name):
+    # indexer_bwd runs the same two kernels: dI, dq, dw and the
+    # deterministic dK are bitwise those of the two calls
+    wl, x, _ = cases[name]
+    a = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC, path="whole")
+    b = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC, path="pair")
+    for u, v in zip(a, b):
+        assert np.array_equal(u.view(np.int32), v.view(np.int32))
+
+
+@pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "dense_small", "dense_256"])
 def test_determinism(cases, name):
     wl, x, _ = cases[name]
+    # the whole backward, and the pair of calls
+    pr = [gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC, path="pair") for _ in range(2)]
+    for a, b in zip(pr[0], pr[1]):
+        assert np.array_equal(a, b)
     runs = [gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC) for _ in range(3)]
     for r in runs[1:]:
         for a, b in zip(runs[0], r):
