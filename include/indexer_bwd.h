@@ -176,6 +176,44 @@ IBWD_API int indexer_bwd_dense(const uint16_t* q, const uint16_t* k, const float
                                void* stream);
 
 /*
+ * Options of indexer_bwd_ex / indexer_bwd_dense_ex (the #730 benchmark
+ * harness builds its kernels with topk_indices_global=True, takes bf16 dq and
+ * dw outputs, and its full-pipeline time includes a bf16 cast of dK).  A
+ * zero-initialised struct (or NULL) gives the behaviour of indexer_bwd.
+ *   ids_global  0: ids are local to their batch (id s of a row of batch b
+ *               addresses k[b,s]); 1: ids index the flattened [B*S_k] keys,
+ *               and a row of batch b reads id - b*S_k, valid iff that lies
+ *               in [0, S_k) -- an id of another batch is padding, never an
+ *               alias (needs B*S_k < 2^31; ignored by the dense variant)
+ *   dq_bf16     1: dq is bf16 [B,S_q,H,D] (round to nearest even of the fp32
+ *               result) instead of fp32
+ *   dw_bf16     1: dw is bf16 [B,S_q,H] likewise
+ *   dk_bf16     optional device bf16 [B,S_k,D], 16-byte aligned: written with
+ *               the final fp32 dk rounded to nearest even (dk itself is still
+ *               produced in fp32)
+ * Any other value of the int fields is IBWD_ERR_INVALID_ARG.
+ */
+typedef struct {
+  int ids_global;
+  int dq_bf16;
+  int dw_bf16;
+  uint16_t* dk_bf16;
+} ibwd_options;
+
+/* indexer_bwd with options; dq and dw are float* or (bf16) uint16_t* as the
+ * options say.  Same workspace as indexer_bwd. */
+IBWD_API int indexer_bwd_ex(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                            float* attn_score, const int32_t* topk_idx, void* dq, void* dw, float* dk, int B,
+                            int S_q, int S_k, int H, int D, int topk, float grad_scale, int dk_mode,
+                            const ibwd_options* options, void* workspace, size_t workspace_bytes, void* stream);
+
+/* indexer_bwd_dense with options (ids_global does not apply). */
+IBWD_API int indexer_bwd_dense_ex(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                                  float* attn_score, void* dq, void* dw, float* dk, int B, int S, int H, int D,
+                                  float grad_scale, int dk_mode, const ibwd_options* options, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
  * Forward of the indexer: the logits the backward differentiates (#730
  * benchmark harness: one shared key head scored against every indexer head
  * of the query, weighted and summed),

@@ -43,7 +43,15 @@ EXPORTS = (
     "indexer_fwd_dense",
     "indexer_bwd",
     "indexer_bwd_dense",
+    "indexer_bwd_ex",
+    "indexer_bwd_dense_ex",
 )
+
+
+class Options(ctypes.Structure):
+    """ibwd_options of the C header (ids_global, dq_bf16, dw_bf16, dk_bf16)."""
+    _fields_ = [("ids_global", ctypes.c_int), ("dq_bf16", ctypes.c_int), ("dw_bf16", ctypes.c_int),
+                ("dk_bf16", ctypes.c_void_p)]
 
 
 class IndexerBwdError(RuntimeError):
@@ -85,6 +93,11 @@ def load() -> ctypes.CDLL:
     lib.indexer_bwd.restype = i
     lib.indexer_bwd_dense.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, f, i, p, sz, p]
     lib.indexer_bwd_dense.restype = i
+    po = ctypes.POINTER(Options)
+    lib.indexer_bwd_ex.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, f, i, po, p, sz, p]
+    lib.indexer_bwd_ex.restype = i
+    lib.indexer_bwd_dense_ex.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, f, i, po, p, sz, p]
+    lib.indexer_bwd_dense_ex.restype = i
     lib.indexer_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
     lib.indexer_fwd.restype = i
     lib.indexer_fwd_dense.argtypes = [p, p, p, p, i, i, i, i, p]
@@ -296,24 +309,83 @@ def indexer_bwd_dense(q, k, w, index_score, attn_score, dq, dw, dk, grad_scale: 
     _check(rc, "indexer_bwd_dense")
 
 
+def _out_flag(t, name):
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+
+
+def indexer_bwd_ex(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale: float = 1.0,
+                   dk_mode=IBWD_DK_ATOMIC, ids_global: bool = False, dk_bf16=None, workspace=None, stream=None):
+    """indexer_bwd with options: dq / dw may be bfloat16 tensors (rounded to
+    nearest even from the fp32 results), dk_bf16 an optional bfloat16
+    [B,S_k,D] copy of dk, and ids_global=True takes ids into the flattened
+    [B*S_k] keys.  topk_idx=None selects the dense variant."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k, torch.bfloat16, 3, "k")
+    _need(w, torch.float32, 3, "w")
+    _need(index_score, torch.float32, 3, "index_score")
+    _need(attn_score, torch.float32, 3, "attn_score")
+    _need(dq, dq.dtype, 4, "dq")
+    _need(dw, dw.dtype, 3, "dw")
+    _need(dk, torch.float32, 3, "dk")
+    if dk_bf16 is not None:
+        _need(dk_bf16, torch.bfloat16, 3, "dk_bf16")
+    opts = Options(int(bool(ids_global)), _out_flag(dq, "dq"), _out_flag(dw, "dw"),
+                   None if dk_bf16 is None else dk_bf16.data_ptr())
+    B, S_q, H, D = q.shape
+    S_k = k.shape[1]
+    lib = load()
+    if topk_idx is None:
+        if workspace is None:
+            workspace = torch.empty(indexer_bwd_dense_gemm_workspace_size(B, S_q, H, D, dk_mode),
+                                    dtype=torch.uint8, device=q.device)
+        rc = lib.indexer_bwd_dense_ex(_ptr(q), _ptr(k), _ptr(w), _ptr(index_score), _ptr(attn_score), _ptr(dq),
+                                      _ptr(dw), _ptr(dk), B, S_q, H, D, float(grad_scale), int(dk_mode),
+                                      ctypes.byref(opts), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream))
+        _check(rc, "indexer_bwd_dense_ex")
+        return
+    _need(topk_idx, torch.int32, 3, "topk_idx")
+    topk = topk_idx.shape[-1]
+    if workspace is None:
+        workspace = torch.empty(indexer_bwd_gemm_workspace_size(B, S_q, S_k, H, D, topk, dk_mode),
+                                dtype=torch.uint8, device=q.device)
+    rc = lib.indexer_bwd_ex(_ptr(q), _ptr(k), _ptr(w), _ptr(index_score), _ptr(attn_score), _ptr(topk_idx),
+                            _ptr(dq), _ptr(dw), _ptr(dk), B, S_q, S_k, H, D, topk, float(grad_scale),
+                            int(dk_mode), ctypes.byref(opts), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "indexer_bwd_ex")
+
+
 def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale: float = 1.0,
-                     dk_mode=IBWD_DK_ATOMIC, workspace=None, out=None, stream=None):
-    """The whole backward (indexer_bwd / indexer_bwd_dense): dI over
-    attn_score (index_score is kept), then dq, dw, dk.
+                     dk_mode=IBWD_DK_ATOMIC, workspace=None, out=None, stream=None, ids_global: bool = False,
+                     out_dtype=torch.float32, dk_bf16=None):
+    """The whole backward (indexer_bwd / indexer_bwd_dense, or their _ex forms
+    when an option is given): dI over attn_score (index_score is kept), then
+    dq, dw, dk.
 
     topk_idx=None selects the dense-causal variant ([B,S,S] scores).
-    `out` may supply preallocated (dq, dw, dk) fp32 tensors.
+    `out` may supply preallocated (dq, dw, dk) tensors; out_dtype
+    (torch.float32 or torch.bfloat16) is the dtype of dq and dw when they are
+    allocated here; dk is always fp32, and dk_bf16 may receive a bf16 copy.
+    ids_global=True takes ids into the flattened [B*S_k] keys.
     Returns (dq, dw, dk).
     """
     B, S_q, H, D = q.shape
     S_k = k.shape[1]
     if out is None:
-        dq = torch.empty((B, S_q, H, D), dtype=torch.float32, device=q.device)
-        dw = torch.empty((B, S_q, H), dtype=torch.float32, device=q.device)
+        dq = torch.empty((B, S_q, H, D), dtype=out_dtype, device=q.device)
+        dw = torch.empty((B, S_q, H), dtype=out_dtype, device=q.device)
         dk = torch.empty((B, S_k, D), dtype=torch.float32, device=q.device)
     else:
         dq, dw, dk = out
-    if topk_idx is None:
+    if ids_global or dk_bf16 is not None or dq.dtype != torch.float32 or dw.dtype != torch.float32:
+        indexer_bwd_ex(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale, dk_mode, ids_global,
+                       dk_bf16, workspace, stream)
+    elif topk_idx is None:
         indexer_bwd_dense(q, k, w, index_score, attn_score, dq, dw, dk, grad_scale, dk_mode, workspace, stream)
     else:
         indexer_bwd(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale, dk_mode, workspace,

@@ -65,7 +65,7 @@ bool shape_ok(int B, int S_q, int S_k, int H, int D, int L) {
 
 // dense_or_idx: the sparse variant requires topk_idx (the dense one passes NULL).
 int score_grad_common(const float* I, float* A, const int32_t* idx, bool dense_or_idx, int B, int S_q, int S_k,
-                      int L, float grad_scale, float* dk, int D, void* stream) {
+                      int L, float grad_scale, float* dk, int D, void* stream, int ids_global = 0) {
   if (B < 1 || S_q < 1 || S_k < 1 || L < 1) return IBWD_ERR_INVALID_ARG;
   if ((long long)B * S_q * L >= (1LL << 31)) return IBWD_ERR_UNSUPPORTED;
   if (dk && (D < 1 || (long long)B * S_k * D >= (1LL << 40))) return IBWD_ERR_INVALID_ARG;
@@ -91,6 +91,7 @@ int score_grad_common(const float* I, float* A, const int32_t* idx, bool dense_o
   a.dk_numel = dk ? (long long)B * S_k * D : 0;
   a.status = dv->status;
   a.num_sms = dv->num_sms;
+  a.ids_global = ids_global;
   cudaError_t e = ibwd::launch_score_grad(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
 }
@@ -108,14 +109,21 @@ size_t workspace_common(int B, int S_q, int S_k, int H, int D, int L, int mode) 
 // commit list: score-grad and GEMM overlapped through programmatic dependent
 // launch); every check of both happens before either is launched.
 int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const float* dI, const int32_t* idx,
-                bool need_idx, float* dq, float* dw, float* dk, int B, int S_q, int S_k, int H, int D, int L,
+                bool need_idx, void* dq, void* dw, float* dk, int B, int S_q, int S_k, int H, int D, int L,
                 int mode, void* ws, size_t ws_bytes, void* stream, const float* I = nullptr,
-                float grad_scale = 0.f) {
+                float grad_scale = 0.f, const ibwd_options* opt = nullptr) {
   if (mode != IBWD_DK_ATOMIC && mode != IBWD_DK_DETERMINISTIC) return IBWD_ERR_INVALID_ARG;
   if (B < 1 || S_q < 1 || S_k < 1 || L < 1 || H < 1 || D < 1) return IBWD_ERR_INVALID_ARG;
   if (!shape_ok(B, S_q, S_k, H, D, L)) return IBWD_ERR_UNSUPPORTED;
   // the sort keeps a cursor and a tag per key of a batch in shared memory
   if (mode == IBWD_DK_DETERMINISTIC && S_k > 40960) return IBWD_ERR_UNSUPPORTED;
+  const ibwd_options o = opt ? *opt : ibwd_options{};
+  if ((o.ids_global != 0 && o.ids_global != 1) || (o.dq_bf16 != 0 && o.dq_bf16 != 1) ||
+      (o.dw_bf16 != 0 && o.dw_bf16 != 1))
+    return IBWD_ERR_INVALID_ARG;
+  // global ids address the flattened [B*S_k] keys with int32
+  if (o.ids_global && (long long)B * S_k > 2147483647LL) return IBWD_ERR_UNSUPPORTED;
+  if (o.dk_bf16 && !aligned16(o.dk_bf16)) return IBWD_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, w, dI, dq, dw, dk};
   for (const void* p : ptrs)
     if (!aligned16(p)) return IBWD_ERR_INVALID_ARG;
@@ -130,6 +138,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
     if (!dev_ptr_ok(p)) return IBWD_ERR_INVALID_ARG;
   if (idx && !dev_ptr_ok(idx)) return IBWD_ERR_INVALID_ARG;
   if (I && !dev_ptr_ok(I)) return IBWD_ERR_INVALID_ARG;
+  if (o.dk_bf16 && !dev_ptr_ok(o.dk_bf16)) return IBWD_ERR_INVALID_ARG;
   const size_t need = ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC).total;
   if (!ws || ws_bytes < need || !dev_ptr_ok(ws)) return IBWD_ERR_WORKSPACE;
   ibwd::GemmArgs a{};
@@ -138,8 +147,12 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.w = w;
   a.dI = dI;
   a.idx = idx;
-  a.dq = dq;
-  a.dw = dw;
+  a.dq = o.dq_bf16 ? nullptr : static_cast<float*>(dq);
+  a.dw = o.dw_bf16 ? nullptr : static_cast<float*>(dw);
+  a.dq16 = o.dq_bf16 ? static_cast<uint16_t*>(dq) : nullptr;
+  a.dw16 = o.dw_bf16 ? static_cast<uint16_t*>(dw) : nullptr;
+  a.dk16 = o.dk_bf16;
+  a.ids_global = idx ? o.ids_global : 0;
   a.dk = dk;
   a.B = B;
   a.S_q = S_q;
@@ -154,7 +167,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.num_sms = dv->num_sms;
   if (I) {
     rc = score_grad_common(I, const_cast<float*>(dI), idx, need_idx, B, S_q, S_k, L, grad_scale,
-                           mode == IBWD_DK_ATOMIC ? dk : nullptr, D, stream);
+                           mode == IBWD_DK_ATOMIC ? dk : nullptr, D, stream, a.ids_global);
     if (rc) return rc;
     a.after_score_grad = 1;
   }
@@ -239,6 +252,24 @@ int indexer_bwd(const uint16_t* q, const uint16_t* k, const float* w, const floa
   if (!index_score || !topk_idx) return IBWD_ERR_INVALID_ARG;
   return gemm_common(q, k, w, attn_score, topk_idx, true, dq, dw, dk, B, S_q, S_k, H, D, topk, dk_mode, workspace,
                      workspace_bytes, stream, index_score, grad_scale);
+}
+
+int indexer_bwd_ex(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                   float* attn_score, const int32_t* topk_idx, void* dq, void* dw, float* dk, int B, int S_q,
+                   int S_k, int H, int D, int topk, float grad_scale, int dk_mode, const ibwd_options* options,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!index_score || !topk_idx) return IBWD_ERR_INVALID_ARG;
+  return gemm_common(q, k, w, attn_score, topk_idx, true, dq, dw, dk, B, S_q, S_k, H, D, topk, dk_mode, workspace,
+                     workspace_bytes, stream, index_score, grad_scale, options);
+}
+
+int indexer_bwd_dense_ex(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,
+                         float* attn_score, void* dq, void* dw, float* dk, int B, int S, int H, int D,
+                         float grad_scale, int dk_mode, const ibwd_options* options, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!index_score) return IBWD_ERR_INVALID_ARG;
+  return gemm_common(q, k, w, attn_score, nullptr, false, dq, dw, dk, B, S, S, H, D, S, dk_mode, workspace,
+                     workspace_bytes, stream, index_score, grad_scale, options);
 }
 
 int indexer_bwd_dense(const uint16_t* q, const uint16_t* k, const float* w, const float* index_score,

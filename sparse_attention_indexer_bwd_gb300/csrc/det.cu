@@ -26,7 +26,8 @@ constexpr int RB = kSortRows;  // query rows per sort chunk (chunks never stradd
 
 __device__ __forceinline__ bool slot_key(const GemmArgs& a, long long r, int j, int& key) {
   if (a.idx) {
-    key = a.idx[r * a.L + j];
+    const unsigned off = a.ids_global ? (unsigned)((int)r / a.S_q) * (unsigned)a.S_k : 0u;  // rows < 2^31
+    key = (int)((unsigned)a.idx[r * a.L + j] - off);
     return (unsigned)key < (unsigned)a.S_k;
   }
   key = j;
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* 
     const int lim = a.idx ? a.L : min(a.L, t + 1);
     if (j >= lim) return -1;
     if (!a.idx) return j;
-    const int k = __ldg(a.idx + r * a.L + j);
+    const unsigned off = a.ids_global ? (unsigned)((int)r / a.S_q) * (unsigned)a.S_k : 0u;  // rows < 2^31
+    const int k = (int)((unsigned)__ldg(a.idx + r * a.L + j) - off);
     return (unsigned)k < (unsigned)a.S_k ? k : -1;
   };
   for (int t = t0; t < t1; ++t) {

@@ -46,6 +46,8 @@
 //         deterministic mode
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
+#include <cuda_bf16.h>
+
 #include <algorithm>
 #include <atomic>
 
@@ -130,9 +132,15 @@ struct KParams {
   unsigned long long wait_ns;
   int B, S_q, S_k, H, D, L, dense;
   int staged;  // rows are staged in shared memory by bulk copies
+  int ids_global;  // slot ids index the flattened [B*S_k] keys
+  uint16_t* dq16;  // bf16 outputs instead of dq / dw when set
+  uint16_t* dw16;
 };
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// fp32 -> bf16 bits, round to nearest even (the optional bf16 outputs)
+__device__ __forceinline__ uint16_t to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -257,16 +265,20 @@ struct RowSrc {
   const int* pos;      // deterministic: the slots' rows in u (else nullptr)
   int Lr;              // slots to look at
   int S_k;
+  unsigned off;        // global ids: b*S_k of the row's batch (else 0)
   __device__ __forceinline__ bool key(int j, int& s) const {
     if (!idx) {
       s = j;
       return true;
     }
-    s = idx[j];
+    s = (int)((unsigned)idx[j] - off);
     return (unsigned)s < (unsigned)S_k;
   }
 };
 
+// OPT: the instance that serves the interface options (global ids, bf16
+// outputs); the other instance carries none of their instructions.
+template <bool OPT>
 __device__ void scan_role(const KParams& p, const Ctx& cx) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -334,6 +346,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
     RowSrc src;
     src.S_k = p.S_k;
     src.Lr = p.dense ? min(p.L, t + 1) : p.L;
+    src.off = (OPT && p.ids_global) ? (unsigned)((int)r / p.S_q) * (unsigned)p.S_k : 0u;  // rows < 2^31
     if (p.staged) {
       const int buf = (int)(i & 1);
       if (!WAIT(&cx.bars->rowfull[buf], (uint32_t)((i >> 1) & 1))) goto done;
@@ -366,7 +379,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int j = 4 * q + k;
-            const bool v = src.idx ? (unsigned)ii[k] < (unsigned)src.S_k : j < src.Lr;
+            const bool v = src.idx ? (unsigned)ii[k] - src.off < (unsigned)src.S_k : j < src.Lr;
             if (v) {
               ++nv;
               mx = fmaxf(mx, fabsf(dd[k]));
@@ -598,6 +611,7 @@ drain:
 
 // ------------------------------------------------------------ dz group ----
 // Group `hg` (0 or 1) owns heads 32*hg .. 32*hg+31 of every tile row.
+template <bool OPT>
 __device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int hg, long long iq, int r,
                                             int c) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
@@ -606,7 +620,11 @@ __device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int
   const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + hg * 32;
   const float sc = pow2f(-c);
   const int d = qw * 32 + lane;  // TMEM lane = column of dQ
-  float* dst = p.dq + (long long)r * p.H * p.D + d;
+  // dQ element (r, h, d), fp32 or (options) bf16; esh = log2 of the element size
+  const bool b16 = OPT && p.dq16;
+  const int esh = b16 ? 1 : 2;
+  char* dst = (b16 ? reinterpret_cast<char*>(p.dq16) : reinterpret_cast<char*>(p.dq)) +
+              (((long long)r * p.H * p.D + d) << esh);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float v[16];
@@ -620,12 +638,19 @@ __device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         const int hh = hg * 32 + half * 16 + h;
-        if (hh < p.H) dst[(long long)hh * p.D] = v[h] * sc;
+        if (hh < p.H) {
+          char* e = dst + (((long long)hh * p.D) << esh);
+          if (b16)
+            *reinterpret_cast<uint16_t*>(e) = to_bf16(v[h] * sc);
+          else
+            *reinterpret_cast<float*>(e) = v[h] * sc;
+        }
       }
     }
   }
 }
 
+template <bool OPT>
 __device__ void dz_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int s = qw * 32 + lane;  // tile row = TMEM lane
@@ -692,7 +717,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     if (tdz == 0) TRACE(EV_DZ_DONE, g);
     if ((tdz & 31) == 0) TRACE(EV_DZW0 + (tdz >> 5), g);
     if ((flags & F_FIRST) && ep_r >= 0) {
-      dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
+      dq_epilogue<OPT>(p, cx, hg, ep_iq, ep_r, ep_c);
       ep_r = -1;
     }
     if (flags & F_LAST) {
@@ -715,9 +740,13 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
       mbar_arrive(&cx.bars->dwred[iq & 1]);
       if (tdz < kHP) {
         if (!WAIT(&cx.bars->dwred[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
-        if (tdz < p.H)
-          p.dw[(long long)r * p.H + tdz] =
-              (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
+        if (tdz < p.H) {
+          const float dwv = (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
+          if (OPT && p.dw16)
+            p.dw16[(long long)r * p.H + tdz] = to_bf16(dwv);
+          else
+            p.dw[(long long)r * p.H + tdz] = dwv;
+        }
       }
       ep_r = r;
       ep_c = c;
@@ -725,7 +754,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     }
     if (flags & F_END) break;
   }
-  if (ok && ep_r >= 0) dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
+  if (ok && ep_r >= 0) dq_epilogue<OPT>(p, cx, hg, ep_iq, ep_r, ep_c);
 }
 
 // ------------------------------------------------------------ dK group ----
@@ -804,6 +833,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
   }
 }
 
+template <bool OPT>
 __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -863,13 +893,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   if (warp < W_SCAN) {
     gather_role(p, cx);
   } else if (warp == W_SCAN) {
-    scan_role(p, cx);
+    scan_role<OPT>(p, cx);
   } else if (warp == W_MMA) {
     mma_role(p, cx);  // the whole warp runs the loop; one elected lane issues
   } else if (warp < W_DZ0) {
     q_role(p, cx);
   } else if (warp < W_DK0) {
-    dz_role(p, cx);
+    dz_role<OPT>(p, cx);
   } else {
     dk_role(p, cx);
   }
@@ -923,6 +953,21 @@ cudaError_t launch_ex(void (*kern)(KArgs...), unsigned grid, unsigned block, siz
   cfg.attrs = pdl ? attr : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// The final fp32 dK -> bf16 (round to nearest even), 8 values per thread step.
+__global__ void dk_to_bf16_kernel(const float* __restrict__ dk, uint16_t* __restrict__ out, long long n) {
+  const long long n8 = n / 8;  // n = B*S_k*D, D a multiple of 8
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < n8; x += (long long)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(dk)[2 * x];
+    const float4 b = reinterpret_cast<const float4*>(dk)[2 * x + 1];
+    uint4 o;
+    o.x = (uint32_t)to_bf16(a.x) | ((uint32_t)to_bf16(a.y) << 16);
+    o.y = (uint32_t)to_bf16(a.z) | ((uint32_t)to_bf16(a.w) << 16);
+    o.z = (uint32_t)to_bf16(b.x) | ((uint32_t)to_bf16(b.y) << 16);
+    o.w = (uint32_t)to_bf16(b.z) | ((uint32_t)to_bf16(b.w) << 16);
+    reinterpret_cast<uint4*>(out)[x] = o;
+  }
 }
 
 unsigned long long gcd_u64(unsigned long long a, unsigned long long b) {
@@ -997,7 +1042,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
@@ -1009,6 +1056,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.idx = a.idx;
   p.dq = a.dq;
   p.dw = a.dw;
+  p.dq16 = a.dq16;
+  p.dw16 = a.dw16;
+  p.ids_global = a.ids_global;
   p.dk = a.dk;
   p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
   p.pos = a.deterministic ? reinterpret_cast<const int*>(ws + lay.pos) : nullptr;
@@ -1030,10 +1080,21 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const bool al = (a.L % 4 == 0) && ((uintptr_t)a.dI % 16 == 0) && (p.dense || (uintptr_t)a.idx % 16 == 0);
   p.staged = fits && al;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
-  cudaError_t e = launch_ex(gemm_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
+  const bool opt = p.ids_global || p.dq16 || p.dw16;
+  cudaError_t e = launch_ex(opt ? gemm_kernel<true> : gemm_kernel<false>, (unsigned)grid, (unsigned)NTHREADS,
+                            SMEM_BYTES, st, true, p);
   if (e != cudaSuccess) return e;
-  if (a.deterministic) return launch_det_segsum(a, lay, st);
-  return cudaSuccess;
+  if (a.deterministic) {
+    e = launch_det_segsum(a, lay, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.dk16) {
+    const long long n = (long long)a.B * a.S_k * a.D;
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((n / 8 + 255) / 256, 4LL * a.num_sms));
+    dk_to_bf16_kernel<<<blocks, 256, 0, st>>>(a.dk, a.dk16, n);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 #ifdef IBWD_TRACE

@@ -25,6 +25,8 @@ struct ScoreGradArgs {
   long long dk_numel;
   unsigned* status;          // device status word (a bounded wait that gave up)
   int num_sms;
+  int ids_global;            // ids index the flattened [B*S_k] keys: slot id of a row of batch b
+                             // is key id - b*S_k, valid iff that lies in [0, S_k)
 };
 cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st);
 
@@ -44,6 +46,10 @@ struct GemmArgs {
   unsigned* status;      // device status word
   int num_sms;
   int after_score_grad;  // queued right after this library's score-grad kernel (same stream)
+  int ids_global;        // as in ScoreGradArgs
+  uint16_t* dq16;        // if set: dq written here as bf16 (round to nearest even) instead of to dq
+  uint16_t* dw16;        // if set: dw likewise
+  uint16_t* dk16;        // if set: bf16 copy of the final dk, written after it
 };
 
 struct WsLayout {

@@ -10,7 +10,8 @@
 //   p_j    = exp(I_j - m) / sum_valid exp(I - m)      (m = max over valid j)
 //   ahat_j = a_j / sum_valid a                        (0 when the sum is 0)
 //   dI_j   = grad_scale * (p_j - ahat_j) / S_q         (0 on padding slots)
-// A slot is valid iff its id lies in [0, S_k) (dense rows: iff j <= t).
+// A slot is valid iff its id lies in [0, S_k) (dense rows: iff j <= t); with
+// global ids, a row of batch b subtracts b*S_k from each id first.
 // Padding slots are selected out, never multiplied by a mask, so NaN or
 // garbage there never reaches dI.
 //
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(BLOCK) score_grad_vec(ScoreGradArgs a, long lo
   const int4* X4 = a.idx ? reinterpret_cast<const int4*>(a.idx + rr * a.L) : nullptr;
   const int t = (int)(rr % a.S_q);
   const int lim = a.idx ? a.L : min(a.L, t + 1);  // dense: slots beyond t are padding
+  const int off = a.ids_global ? ((int)rr / a.S_q) * a.S_k : 0;  // rows < 2^31
 
   float iv[NV][4], av[NV][4];
   bool vv[NV][4];
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(BLOCK) score_grad_vec(ScoreGradArgs a, long lo
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = v4 * 4 + e;
-      const bool v = in && (X4 ? ((unsigned)ids[e] < (unsigned)a.S_k) : (j < lim));
+      const bool v = in && (X4 ? ((unsigned)ids[e] - (unsigned)off < (unsigned)a.S_k) : (j < lim));
       vv[k][e] = v;
       iv[k][e] = xs[e];
       av[k][e] = ys[e];
@@ -174,7 +176,8 @@ __global__ void __launch_bounds__(BLOCK) score_grad_generic(ScoreGradArgs a, lon
   const int32_t* X = a.idx ? a.idx + r * a.L : nullptr;
   const int t = (int)(r % a.S_q);
   const int lim = a.idx ? a.L : min(a.L, t + 1);
-  auto valid = [&](int j) { return X ? ((unsigned)X[j] < (unsigned)a.S_k) : (j < lim); };
+  const int off = a.ids_global ? ((int)r / a.S_q) * a.S_k : 0;  // rows < 2^31
+  auto valid = [&](int j) { return X ? ((unsigned)X[j] - (unsigned)off < (unsigned)a.S_k) : (j < lim); };
   auto block_reduce = [&](float v, bool is_max) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -250,8 +253,9 @@ __device__ __forceinline__ bool sg_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// NV float4 of each array per thread: L = 4 * NV * blockDim.x.
-template <int NV>
+// NV float4 of each array per thread: L = 4 * NV * blockDim.x.  GLOBAL: the
+// ids are global (a.ids_global), kept out of the other instances.
+template <int NV, bool GLOBAL>
 __global__ void __launch_bounds__(512, NV == 1 ? 3 : 2) score_grad_staged(ScoreGradArgs a) {
   allow_dependent_launch();
   extern __shared__ __align__(16) uint8_t sg_smem[];
@@ -340,6 +344,7 @@ __global__ void __launch_bounds__(512, NV == 1 ? 3 : 2) score_grad_staged(ScoreG
     const long long r = blockIdx.x + i * G;
     const uint8_t* st = sg_smem + s * stage_bytes;
     const int lim = dense ? min(L, (int)(r % a.S_q) + 1) : L;  // dense: slots beyond t are padding
+    const int off = GLOBAL ? ((int)r / a.S_q) * a.S_k : 0;  // rows < 2^31
     float xs[NV][4], ys[NV][4];
     int ids[NV][4];
 #pragma unroll
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(512, NV == 1 ? 3 : 2) score_grad_staged(ScoreG
       const int v4 = tid + k * (int)blockDim.x;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        vv[k][e] = v4 < L4 && (dense ? v4 * 4 + e < lim : (unsigned)ids[k][e] < (unsigned)a.S_k);
+        vv[k][e] = v4 < L4 && (dense ? v4 * 4 + e < lim : (unsigned)ids[k][e] - (unsigned)off < (unsigned)a.S_k);
         if (vv[k][e]) {
           m = fmaxf(m, xs[k][e]);
           sa += ys[k][e];
@@ -436,23 +441,27 @@ cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev].load(std::memory_order_acquire)) {
-      cudaError_t e = cudaFuncSetAttribute(score_grad_staged<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(score_grad_staged<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            NSTG * 12 * 2048);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(score_grad_staged<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, NSTG * 8 * 4096);
+      e = cudaFuncSetAttribute(score_grad_staged<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               NSTG * 12 * 2048);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(score_grad_staged<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               NSTG * 8 * 4096);
       if (e != cudaSuccess) return e;
       attr_done[dev].store(true, std::memory_order_release);
     }
+    // sparse rows take NV = 1 (L <= 2048); global ids only exist for them
+    void (*kern)(ScoreGradArgs) = nv == 2 ? score_grad_staged<2, false>
+                                  : (a.idx && a.ids_global) ? score_grad_staged<1, true>
+                                                            : score_grad_staged<1, false>;
     int per_sm = 0;
-    cudaError_t e = nv == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged<2>, threads, smem)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, score_grad_staged<1>, threads, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long grid = std::min<long long>(a.rows, (long long)a.num_sms * per_sm);
-    if (nv == 2)
-      score_grad_staged<2><<<(unsigned)grid, threads, smem, st>>>(a);
-    else
-      score_grad_staged<1><<<(unsigned)grid, threads, smem, st>>>(a);
+    kern<<<(unsigned)grid, threads, smem, st>>>(a);
     return cudaGetLastError();
   }
   if (aligned) {
