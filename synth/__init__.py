@@ -46,9 +46,11 @@ def _L():
         lib.synth_normal_bf16.argtypes = [u64, u64, i64, dbl, dbl, p]
         lib.synth_topk_causal.argtypes = [u64, u64, i32, i32, i32, i32, p]
         lib.synth_topk_window.argtypes = [u64, u64, i32, i32, i32, i32, i32, p]
+        lib.synth_topk_uniform.argtypes = [u64, u64, i32, i32, i32, i32, p]
         lib.synth_target_sparse.argtypes = [u64, u64, p, i32, i32, i32, i32, dbl, p]
         lib.synth_target_dense.argtypes = [u64, u64, i32, i32, dbl, p]
-        for f in ("synth_topk_causal", "synth_topk_window", "synth_target_sparse", "synth_target_dense"):
+        for f in ("synth_topk_causal", "synth_topk_window", "synth_topk_uniform", "synth_target_sparse",
+                  "synth_target_dense"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -80,6 +82,13 @@ def topk_causal(seed, stream, B, S_q, S_k, topk) -> np.ndarray:
     out = np.empty((B, S_q, topk), dtype=np.int32)
     if _L().synth_topk_causal(seed, stream, B, S_q, S_k, topk, _ptr(out)):
         raise MemoryError("synth_topk_causal")
+    return out
+
+
+def topk_uniform(seed, stream, B, S_q, S_k, topk) -> np.ndarray:
+    out = np.empty((B, S_q, topk), dtype=np.int32)
+    if _L().synth_topk_uniform(seed, stream, B, S_q, S_k, topk, _ptr(out)):
+        raise MemoryError("synth_topk_uniform")
     return out
 
 
@@ -120,7 +129,7 @@ class Workload:
     S_q: int
     S_k: int
     topk: int          # 0 for the dense variant
-    ids: str           # "causal" | "window" | "dense"
+    ids: str           # "causal" | "window" | "uniform" | "dense"
     seed: int
 
     @property
@@ -144,6 +153,11 @@ WORKLOADS = {
     "window_topk2048": Workload("window_topk2048", 1, 64, 128, 8192, 4096, 2048, "window", 3),
     "dense_s4096": Workload("dense_s4096", 1, 64, 128, 4096, 4096, 0, "dense", 4),
 }
+# The top-k sweep of the pages' benchmark harness at the anchor shape with
+# uniform lengths: every row selects topk distinct keys out of all S_k (the
+# causal workloads above are its ragged, monotone-ramp form).
+for _i, _k in enumerate((128, 256, 384, 512, 640, 1024, 1536, 2048)):
+    WORKLOADS[f"uniform_topk{_k}"] = Workload(f"uniform_topk{_k}", 1, 64, 128, 8192, 4096, _k, "uniform", 10 + _i)
 
 
 def make_inputs(wl: Workload) -> dict:
@@ -163,6 +177,8 @@ def make_inputs(wl: Workload) -> dict:
     else:
         if wl.ids == "window":
             idx = topk_window(s, STREAM_IDX, wl.B, wl.S_q, wl.S_k, wl.topk)
+        elif wl.ids == "uniform":
+            idx = topk_uniform(s, STREAM_IDX, wl.B, wl.S_q, wl.S_k, wl.topk)
         else:
             idx = topk_causal(s, STREAM_IDX, wl.B, wl.S_q, wl.S_k, wl.topk)
         out["idx"] = idx

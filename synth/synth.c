@@ -101,8 +101,9 @@ static void shuffle(uint64_t seed, uint64_t stream, uint64_t ctr, int32_t *a, in
   }
 }
 
-/* Distinct causal ids per row, random order, -1 padding at the tail. */
-int synth_topk_causal(uint64_t seed, uint64_t stream, int B, int S_q, int S_k, int topk, int32_t *idx) {
+/* Distinct ids per row in random order, -1 padding at the tail: from the
+ * row's causal keys, or (uniform) from all S_k keys. */
+static int topk_rows(uint64_t seed, uint64_t stream, int B, int S_q, int S_k, int topk, int uniform, int32_t *idx) {
   int64_t rows = (int64_t)B * S_q;
   int bad = 0;
 #pragma omp parallel
@@ -115,7 +116,7 @@ int synth_topk_causal(uint64_t seed, uint64_t stream, int B, int S_q, int S_k, i
 #pragma omp for schedule(dynamic, 16)
       for (int64_t r = 0; r < rows; r++) {
         int64_t t = r % S_q;
-        int64_t n = causal_last(t, S_q, S_k) + 1;
+        int64_t n = uniform ? S_k : causal_last(t, S_q, S_k) + 1;
         int64_t m = n < topk ? n : topk;
         int32_t *row = idx + r * topk;
         uint64_t base = (uint64_t)r << 24;
@@ -127,6 +128,15 @@ int synth_topk_causal(uint64_t seed, uint64_t stream, int B, int S_q, int S_k, i
     }
   }
   return bad;
+}
+
+int synth_topk_causal(uint64_t seed, uint64_t stream, int B, int S_q, int S_k, int topk, int32_t *idx) {
+  return topk_rows(seed, stream, B, S_q, S_k, topk, 0, idx);
+}
+
+/* Every row: min(topk, S_k) distinct ids drawn from all S_k keys. */
+int synth_topk_uniform(uint64_t seed, uint64_t stream, int B, int S_q, int S_k, int topk, int32_t *idx) {
+  return topk_rows(seed, stream, B, S_q, S_k, topk, 1, idx);
 }
 
 /* Local-window ids: rows with more than topk causal keys take topk/2 slots

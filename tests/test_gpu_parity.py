@@ -21,6 +21,7 @@ SMALL = [
     W("dense_small", 1, 64, 128, 200, 200, 0, "dense", 14),
     W("dense_odd", 2, 5, 24, 77, 77, 0, "dense", 15),
     W("dense_256", 1, 8, 64, 256, 256, 0, "dense", 16),                # staged dense score-grad rows
+    W("uniform_small", 1, 16, 64, 130, 512, 256, "uniform", 17),       # uniform lengths, 2 full tiles per row
 ]
 
 
