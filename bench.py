@@ -470,7 +470,11 @@ def run_ours(args, wl):
                                                "a fresh attn_score copy per step",
                    "valid_slot_fraction": round(valid, 4)},
         "us_per_step": 1e3 * ms_step,
+        "tflops_valid_slots": value * valid,
         "kernels_us": {"score_grad": 1e3 * sg_avg, "gemm_stage": 1e3 * gm_avg},
+        "kernels_us_stats": {name: {"median": 1e3 * float(np.median(v)), "min": 1e3 * float(np.min(v)),
+                                    "p90": 1e3 * float(np.percentile(v, 90))}
+                             for name, v in (("score_grad", sg_ms), ("gemm_stage", gm_ms))},
         "score_grad_gbs": sg_bytes / (sg_avg * 1e-3) / 1e9,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / pk["bf16_tflops"], "traffic": traffic.get("gemm_stage"),
