@@ -470,7 +470,8 @@ def run_ours(args, wl):
                                                "a fresh attn_score copy per step",
                    "valid_slot_fraction": round(valid, 4)},
         "us_per_step": 1e3 * ms_step,
-        "tflops_valid_slots": value * valid,
+        # valid slots only (the dense count is already over s <= t)
+        "tflops_valid_slots": value * (1.0 if wl.dense else valid),
         "kernels_us": {"score_grad": 1e3 * sg_avg, "gemm_stage": 1e3 * gm_avg},
         "kernels_us_stats": {name: {"median": 1e3 * float(np.median(v)), "min": 1e3 * float(np.min(v)),
                                     "p90": 1e3 * float(np.percentile(v, 90))}
