@@ -560,8 +560,16 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
     for (;;) {
       int nflags = 0;
       long long niq = iq;
+      // the dK MMA of tile g first: the dK warps wait for it
+      if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
+      TRACE(EV_MMA_DZFULL, g);
+      if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
+      TRACE(EV_MMA_DKEMPTY, g);
+      tc_fence_after();
+      mma_dk(cx, g, (int)(iq & 1));
+      umma_commit_elect(&B->dkfull[g & 1]);
       if (!(flags & F_END)) {
-        // look ahead: Z of tile g+1 overlaps the dz work of tile g
+        // then Z of tile g+1
         const int g1 = g + 1;
         if (!WAITW(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) goto drain;
         TRACE(EV_MMA_MFULL, g1);
@@ -580,14 +588,8 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
         TRACE(EV_MMA_Z, g1);
         umma_commit_elect(&B->zfull[g1 & 1]);
       }
-      if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
-      TRACE(EV_MMA_DZFULL, g);
-      if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
-      TRACE(EV_MMA_DKEMPTY, g);
       if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
       tc_fence_after();
-      mma_dk(cx, g, (int)(iq & 1));
-      umma_commit_elect(&B->dkfull[g & 1]);
       mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
       umma_commit_elect(&B->kempty[g % KST]);
       umma_commit_elect(&B->dzempty[g & 1]);

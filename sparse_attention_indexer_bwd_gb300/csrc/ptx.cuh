@@ -49,31 +49,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, but the thread may stay suspended (not issuing) for up to
-// `hint_ns` while the phase is incomplete; it resumes when the phase completes.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase with the given parity to complete, suspended rather
-// than spinning, so that waiting warps leave the issue slots to working ones.
-// Gives up after `limit_ns` of wall time or as soon as *abort is set by
-// another warp; on a timeout it raises DEV_TIMEOUT in *status and sets
-// *abort.  Returns false when it gave up.
+// Waits for the phase with the given parity to complete: repeated try_wait,
+// which the hardware may suspend for a short, system-chosen time while the
+// phase is open (with a suspend-time hint the gemm kernel measured ~1 %
+// slower).  Gives up after `limit_ns` of wall
+// time or as soon as *abort is set by another warp; on a timeout it raises
+// DEV_TIMEOUT in *status and sets *abort.  Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, DEV_TIMEOUT);
