@@ -160,6 +160,12 @@ IBWD_API int indexer_bwd_gemm_noalloc(const uint16_t* q, const uint16_t* k, cons
  *                IBWD_DK_ATOMIC mode by kernel 1, as through dk_to_zero)
  *   workspace    at least indexer_bwd_gemm_workspace_size bytes (same shapes
  *                and dk_mode)
+ * The fp16 copy of k and the gemm kernel are launched with programmatic
+ * stream serialization behind the score-grad kernel (#730 commit list: the
+ * score-grad and the GEMM overlap through programmatic dependent launch):
+ * they may start while it runs, and each waits for the kernels before it
+ * before reading what they wrote.  Work queued on the stream after this call
+ * still starts only when the whole call has completed.
  * The results are bitwise those of the two calls.  Every check of both calls
  * happens before either kernel is launched.
  */
