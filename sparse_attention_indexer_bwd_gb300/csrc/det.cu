@@ -7,11 +7,15 @@
 // Here the slots are first sorted by key:
 //   sort:    for every key s, the slots (r, j) selecting it, in ascending
 //            (r, j) order, from per-chunk histograms and a scan (no position
-//            atomics, so the order is fixed); the result is each valid
-//            slot's position in that order;
-// then the gemm kernel stores each slot's dK row u at its position, so every
-// key's rows are contiguous, and
-//   segsum:  dK[s] = sum of the key's u rows, in position order.
+//            atomics, so the order is fixed);
+// then the gemm kernel stores each slot's dK row in u, and
+//   segsum:  dK[s] = sum of the key's u rows, in that order.
+// Two layouts of u.  Position mode (a row's ids, dI and positions fit the
+// gemm kernel's row stage): the sort gives each slot its position, the gemm
+// kernel stores the slot's row there, so every key's rows are contiguous and
+// the segment sum streams them.  Slot mode (longer rows): the gemm kernel
+// stores slot r*L + j at row r*L + j, the sort lists the slots in key order,
+// and the segment sum reads the rows through that list.
 // The result is bitwise identical run to run and overwrites dK.
 #include <algorithm>
 #include <atomic>
@@ -131,8 +135,10 @@ __global__ void __launch_bounds__(1024) keyscan_kernel(int* __restrict__ key_sta
 // its key in shared memory and reads the tag back): without duplicates every
 // lane takes the key's cursor directly; with them the lanes rank themselves
 // with a match.
+// order: position mode, order[slot] = position; slot mode, order[position] = slot.
 __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* __restrict__ hist,
-                                                   const int* __restrict__ key_start, int* __restrict__ pos) {
+                                                   const int* __restrict__ key_start, int* __restrict__ order,
+                                                   int position_mode) {
   extern __shared__ int cursor[];  // [S_k] cursors, then [S_k] one-byte tags
   unsigned char* tag = reinterpret_cast<unsigned char*>(cursor + a.S_k);
   const int cpb = (a.S_q + RB - 1) / RB;
@@ -186,7 +192,10 @@ __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* 
         if (!dup) {
           if (v) {
             const int base = cursor[key];
-            pos[slot] = base;
+            if (position_mode)
+              order[slot] = base;
+            else
+              order[base] = slot;
             cursor[key] = base + 1;
           }
         } else {
@@ -195,7 +204,11 @@ __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* 
           if (v) base = cursor[key];
           __syncwarp();
           if (v) {
-            pos[slot] = base + __popc(grp & lt);
+            const int at = base + __popc(grp & lt);
+            if (position_mode)
+              order[slot] = at;
+            else
+              order[at] = slot;
             if ((grp & lt) == 0) cursor[key] = base + __popc(grp);
           }
         }
@@ -213,8 +226,11 @@ __global__ void __launch_bounds__(32) place_kernel(const GemmArgs a, const int* 
 // consecutive rows per step, four steps in flight), then the eight partial
 // sums are added in warp order: a fixed order, so dK is bitwise reproducible.
 constexpr int SEG_WARPS = 8;
+// perm: slot mode, the key-order slot list (u row of position p is perm[p]);
+// position mode, nullptr (u row p).
 __global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const GemmArgs a, const float* __restrict__ u,
-                                                               const int* __restrict__ key_start) {
+                                                               const int* __restrict__ key_start,
+                                                               const int* __restrict__ perm) {
   __shared__ float4 part[SEG_WARPS][32];
   const long long gk = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -224,11 +240,17 @@ __global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const GemmArgs a
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int NF = 4;  // steps in flight per warp
   for (int p0 = beg + w; p0 < end; p0 += NF * SEG_WARPS) {
+    int sl[NF];  // the steps' slots, whose dK rows are u[slot]
+#pragma unroll
+    for (int k = 0; k < NF; ++k) {
+      const int pr = p0 + k * SEG_WARPS;
+      sl[k] = pr < end ? (perm ? __ldg(perm + pr) : pr) : 0;
+    }
     float4 v[NF];
 #pragma unroll
     for (int k = 0; k < NF; ++k) {
       const int pr = p0 + k * SEG_WARPS;
-      v[k] = (on && pr < end) ? __ldcs(reinterpret_cast<const float4*>(u + (long long)pr * a.D + d))
+      v[k] = (on && pr < end) ? __ldcs(reinterpret_cast<const float4*>(u + (long long)sl[k] * a.D + d))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
@@ -263,7 +285,7 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   char* ws = static_cast<char*>(a.ws);
   int* hist = reinterpret_cast<int*>(ws + lay.hist);
   int* key_start = reinterpret_cast<int*>(ws + lay.key_start);
-  int* pos = reinterpret_cast<int*>(ws + lay.pos);
+  int* order = reinterpret_cast<int*>(ws + lay.order);
   const size_t sh = (size_t)a.S_k * sizeof(int);       // histogram counters
   const size_t sh_place = sh + (size_t)a.S_k;              // cursors and one-byte tags
   static std::atomic<bool> attr_set[64];  // per device; setting the attribute twice is harmless
@@ -280,7 +302,7 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   const long long nk = (long long)a.B * a.S_k;
   colscan_kernel<<<(unsigned)(a.B * ((a.S_k + 31) / 32)), 1024, 0, st>>>(a, hist, key_start);
   keyscan_kernel<<<1, 1024, 0, st>>>(key_start, nk);
-  place_kernel<<<(unsigned)lay.nchunks, 32, sh_place, st>>>(a, hist, key_start, pos);
+  place_kernel<<<(unsigned)lay.nchunks, 32, sh_place, st>>>(a, hist, key_start, order, det_position_mode(a) ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -288,8 +310,9 @@ cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream
   char* ws = static_cast<char*>(a.ws);
   const float* u = reinterpret_cast<const float*>(ws + lay.u);
   const int* key_start = reinterpret_cast<const int*>(ws + lay.key_start);
+  const int* perm = det_position_mode(a) ? nullptr : reinterpret_cast<const int*>(ws + lay.order);
   const long long nk = (long long)a.B * a.S_k;
-  segsum_kernel<<<(unsigned)nk, SEG_WARPS * 32, 0, st>>>(a, u, key_start);
+  segsum_kernel<<<(unsigned)nk, SEG_WARPS * 32, 0, st>>>(a, u, key_start, perm);
   return cudaGetLastError();
 }
 

@@ -79,7 +79,8 @@ constexpr uint32_t TM_Z = 0, TM_DK = 128, TM_DQ = 384, TM_COLS = 512;
 
 struct TileMeta {
   int key[kBM];    // selected key (row of k within the batch)
-  int slot[kBM];   // deterministic mode: the slot's row in u (its position in key order)
+  int slot[kBM];   // deterministic mode: the slot's dK row in u (position mode: its position in key
+                   // order; slot mode: j, the row being r*L + j)
   float dis[kBM];  // dI[t, j] * 2^c
   int r, count, c, flags;
 };
@@ -123,8 +124,9 @@ struct KParams {
   float* dq;
   float* dw;
   float* dk;
-  float* u;         // deterministic: per-slot dK rows in key order, or nullptr
-  const int* pos;   // deterministic: each slot's row in u
+  float* u;         // deterministic: per-slot dK rows, or nullptr
+  const int* pos;   // deterministic, position mode: each slot's row in u (its position in key order);
+                    // else nullptr, and slot j of row r has row r*L + j
   unsigned* sched;  // row counter in the workspace, zeroed by k_to_f16_kernel
   unsigned* status;
   long long rows;
@@ -262,7 +264,7 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
 struct RowSrc {
   const int32_t* idx;  // nullptr for dense rows
   const float* dI;
-  const int* pos;      // deterministic: the slots' rows in u (else nullptr)
+  const int* pos;      // deterministic position mode: the slots' rows in u (else nullptr)
   int Lr;              // slots to look at
   int S_k;
   unsigned off;        // global ids: b*S_k of the row's batch (else 0)
@@ -277,7 +279,8 @@ struct RowSrc {
 };
 
 // OPT: the instance that serves the interface options (global ids, bf16
-// outputs); the other instance carries none of their instructions.
+// outputs) and the deterministic slot mode; the other instance carries none
+// of their instructions.
 template <bool OPT>
 __device__ void scan_role(const KParams& p, const Ctx& cx) {
   const int lane = threadIdx.x & 31;
@@ -314,7 +317,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       // this thread's earlier generic reads of the buffer precede the async writes
       fence_proxy_async_smem();
       const uint32_t dst = smem_u32(rowbuf + buf * ROW_BYTES);
-      // packed: [idx (sparse)] dI [pos (deterministic)], L*4 bytes apart
+      // packed: [idx (sparse)] dI [pos (deterministic position mode)], L*4 bytes apart
       const uint32_t stride = (uint32_t)p.L * 4;
       if (p.dense) {
         const uint32_t bytes = (uint32_t)(((min(p.L, t + 1) * 4) + 15) & ~15);
@@ -798,6 +801,7 @@ __device__ __forceinline__ void dk_chunk(float* base, const int* ids, const floa
   }
 }
 
+template <bool OPT>
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3;
   const int kg = (threadIdx.x - W_DK0 * 32) >> 7;  // group: tile rows 64*kg .. 64*kg+63
@@ -807,7 +811,11 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
     const TileMeta& M = cx.meta[ms];
     const int flags = M.flags, c = M.c, r = M.r, count = M.count;
-    float* base = p.u ? p.u : p.dk + (long long)(r / p.S_q) * p.S_k * p.D;
+    // deterministic: the slots' dK rows in u (slot mode, in the options
+    // instance only: the row's block of L rows); else dK of the row's batch, by key
+    float* base = OPT ? (p.u ? (p.pos ? p.u : p.u + (long long)r * p.L * p.D)
+                             : p.dk + (long long)(r / p.S_q) * p.S_k * p.D)
+                      : (p.u ? p.u : p.dk + (long long)(r / p.S_q) * p.S_k * p.D);
     const int* ids = p.u ? M.slot : M.key;
     if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
     if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, g);
@@ -903,7 +911,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   } else if (warp < W_DK0) {
     dz_role<OPT>(p, cx);
   } else {
-    dk_role(p, cx);
+    dk_role<OPT>(p, cx);
   }
 
   tc_fence_before();
@@ -1015,11 +1023,22 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
     off = up(off + (size_t)w.nchunks * S_k * 4);
     w.key_start = off;
     off = up(off + ((size_t)B * S_k + 1) * 4);
-    w.pos = off;
+    w.order = off;
     off = up(off + (size_t)rows * L * 4);
   }
   w.total = off;
   return w;
+}
+
+// Deterministic mode: position mode when a row's ids, dI and sorted positions
+// fit the row stage together (the dK rows then go to u in key order and the
+// segment sum streams them), else slot mode (row r*L + j per slot, read back
+// through the key-order slot list).
+bool det_position_mode(const GemmArgs& a) {
+  if (!a.deterministic) return false;
+  const size_t arrays = a.idx ? 3 : 2;
+  return a.L % 4 == 0 && arrays * (size_t)a.L * 4 <= ROW_BYTES && (uintptr_t)a.dI % 16 == 0 &&
+         (!a.idx || (uintptr_t)a.idx % 16 == 0);
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
@@ -1063,7 +1082,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.ids_global = a.ids_global;
   p.dk = a.dk;
   p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
-  p.pos = a.deterministic ? reinterpret_cast<const int*>(ws + lay.pos) : nullptr;
+  p.pos = det_position_mode(a) ? reinterpret_cast<const int*>(ws + lay.order) : nullptr;
   p.sched = sched;
   p.status = a.status;
   p.rows = (long long)a.B * a.S_q;
@@ -1077,12 +1096,13 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.L = a.L;
   p.dense = a.idx == nullptr;
   // rows are staged in shared memory when they fit and are 16-byte aligned
-  const size_t arrays = (p.dense ? 1 : 2) + (a.deterministic ? 1 : 0);
+  const size_t arrays = (p.dense ? 1 : 2) + (p.pos ? 1 : 0);
   const bool fits = arrays * a.L * 4 <= ROW_BYTES;
   const bool al = (a.L % 4 == 0) && ((uintptr_t)a.dI % 16 == 0) && (p.dense || (uintptr_t)a.idx % 16 == 0);
   p.staged = fits && al;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
-  const bool opt = p.ids_global || p.dq16 || p.dw16;
+  // the options instance also serves the deterministic slot mode
+  const bool opt = p.ids_global || p.dq16 || p.dw16 || (p.u && !p.pos);
   cudaError_t e = launch_ex(opt ? gemm_kernel<true> : gemm_kernel<false>, (unsigned)grid, (unsigned)NTHREADS,
                             SMEM_BYTES, st, true, p);
   if (e != cudaSuccess) return e;

@@ -11,7 +11,7 @@ namespace ibwd {
 constexpr int kBM = 128;  // keys per tile (the MMA M dimension for Z and dK)
 constexpr int kDP = 128;  // head dim padded to 128 (the MMA M dimension for dQ)
 constexpr int kHP = 64;   // indexer heads padded to 64 (the MMA N dimension for Z and dQ)
-constexpr int kSortRows = 4;  // query rows per chunk of the deterministic mode's key sort
+constexpr int kSortRows = 8;  // query rows per chunk of the deterministic mode's key sort
 
 struct ScoreGradArgs {
   const float* index_score;  // [rows, L]
@@ -58,13 +58,18 @@ struct WsLayout {
   size_t u;          // deterministic: per-slot dK rows [rows*L, D] fp32
   size_t hist;       // deterministic: per-chunk key counts [nchunks, S_k] int32
   size_t key_start;  // deterministic: CSR offsets [B*S_k + 1] int32
-  size_t pos;        // deterministic: sorted position of each valid slot r*L + j [rows*L] int32
+  size_t order;      // deterministic [rows*L] int32: position mode, each valid slot's position in key
+                     // order (indexed by slot r*L + j); slot mode, the valid slots in key order
+                     // (ascending (r, j) within a key)
   size_t total;
   long long nchunks;
 };
 WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic);
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
+// Deterministic dK layout: true = dK rows in key order (positions staged with
+// the rows), false = dK rows by slot, summed through a key-order slot list.
+bool det_position_mode(const GemmArgs& a);
 
 struct FwdArgs {
   const uint16_t* q;     // bf16 [rows, H, D]

@@ -80,7 +80,23 @@ def test_whole_call_equals_the_pair_of_calls(cases, name):
         assert np.array_equal(u.view(np.int32), v.view(np.int32))
 
 
-@pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "dense_small", "dense_256"])
+@pytest.mark.parametrize("topk", [1364, 1368])
+def test_deterministic_layouts_at_the_stage_limit(topk):
+    # 12 bytes a slot (ids, dI, sorted positions) fill the gemm kernel's 16 KB
+    # row stage at topk 1364: the dK rows go to u in key order (position
+    # mode); at 1368 they go by slot and are summed through the key-order slot
+    # list (slot mode).  Both against the oracle, both bitwise run to run.
+    wl = W(f"det_layout_{topk}", 1, 4, 32, 48, 4096, topk, "causal", 23)
+    x = case_inputs(wl)
+    ref = oracle_all(wl, x)
+    runs = [gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC) for _ in range(2)]
+    assert_close(*runs[0][1:], ref[1:], tag=f"det topk {topk}")
+    for a, b in zip(runs[0], runs[1]):
+        assert np.array_equal(a.view(np.int32), b.view(np.int32))
+
+
+@pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "odd_shapes", "dense_small", "dense_odd",
+                                  "dense_256"])
 def test_determinism(cases, name):
     wl, x, _ = cases[name]
     # the whole backward, and the pair of calls
