@@ -82,12 +82,17 @@ IBWD_API int indexer_bwd_score_grad(const float* index_score, float* attn_score,
                            int B, int S_q, int S_k, int topk, float grad_scale, float* dk_to_zero,
                            int D, void* stream);
 
-/* Bytes of device workspace indexer_bwd_gemm needs (always > 0: a 256-byte
- * block for the kernel's row counter and an fp16 copy of k, 256 bytes per key
- * row plus one zero row per batch; the deterministic mode adds the per-slot
- * dK rows, 4*D bytes per slot, and the key sort).  The workspace is rewritten
- * by every call: calls that may overlap on the GPU need separate workspaces.
- * 0 for unsupported arguments. */
+/* Bytes of device workspace indexer_bwd_gemm needs (always > 0): a 256-byte
+ * block of counters; an fp16 copy of k, 256 bytes per key row plus one zero
+ * row per batch; and, since the gemm stage takes the query rows in blocks of
+ * four (nb = B * ceil(S_q / 4) blocks) against the union of their keys,
+ * per block 20 bytes and ceil(min(S_k, 4*topk) / 128) tile records of 2560
+ * bytes.  The deterministic mode adds 512 bytes per record and per-entry dK
+ * rows, 4*D bytes for each of nb * min(S_k, 4*topk) entries, plus its key
+ * sort (4*S_k bytes per two blocks).  The dense variant has no records; its
+ * deterministic mode has one dK row per (block, causal key).  The workspace
+ * is rewritten by every call: calls that may overlap on the GPU need
+ * separate workspaces.  0 for unsupported arguments. */
 IBWD_API size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk,
                                        int dk_mode);
 
@@ -129,26 +134,46 @@ IBWD_API int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const 
  * Gemm stage without any allocation (the pages have no counterpart: this is a
  * service of this library).  Same computation, arguments and outputs as
  * indexer_bwd_gemm in IBWD_DK_ATOMIC mode (dk accumulates; zero it first),
- * but it takes no workspace and never calls cudaMalloc, cudaFree or any other
- * allocating routine.  It is meant for callers that cannot allocate device
- * memory where they run the backward: code running inside a memory
- * allocator or pool callback, runtimes that hand out all device memory up
- * front, and launch paths that must not synchronize the device.
- *  - Its scratch (the fp16 copy of k) is a fixed 8 MiB array inside the
- *    library, held by every GPU that loads it until the process exits, so
- *    B * (S_k + 1) <= 32768; larger shapes return IBWD_ERR_UNSUPPORTED before
+ * but it takes no workspace and calls no allocating routine.  It is meant
+ * for callers that cannot allocate device memory where they run the
+ * backward: code running inside a memory allocator or pool callback (an
+ * allocation there would re-enter the allocator), runtimes that hand out all
+ * device memory up front, and launch paths that must not synchronize the
+ * device (cudaMalloc and cudaFree may).
+ *  - It runs a per-row form of the gemm kernel whose only scratch (a row
+ *    counter and the fp16 copy of k) is a fixed 8 MiB array inside the
+ *    library, held by every GPU that loads it until the process exits; hence
+ *    B * (S_k + 1) <= 32768.  Larger shapes return IBWD_ERR_UNSUPPORTED before
  *    anything is launched.
- *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - The first use on a device (this call, indexer_bwd_gemm_noalloc_setup or
+ *    indexer_bwd_gemm_noalloc_status) looks up the array's device address,
+ *    which may load the library's device module (allocating the array) and
+ *    synchronize, and sets the kernel's shared-memory attribute.  Make that
+ *    first use from a context where allocating and synchronizing are allowed,
+ *    and before any stream capture: indexer_bwd_gemm_noalloc_setup does it
+ *    eagerly for the current device.
  *  - Every call shares the one array: calls that overlap on the GPU (two
  *    streams, or two host threads) race and corrupt each other's results.
  *    Each call rewrites the array before reading it.
- *  - A kernel wait that times out is recorded in a status word of this entry
- *    point, not in the one indexer_bwd_last_device_status reports.
+ *  - A kernel wait that times out sets a bit in this entry point's own status
+ *    word (not the one indexer_bwd_last_device_status reports); the word
+ *    keeps its bits across calls until indexer_bwd_gemm_noalloc_status reads
+ *    and clears it.
  */
 IBWD_API int indexer_bwd_gemm_noalloc(const uint16_t* q, const uint16_t* k, const float* w, const float* dI,
                              const int32_t* topk_idx, float* dq, float* dw, float* dk, int B, int S_q,
                              int S_k, int H, int D, int topk, void* stream);
+
+/* The one-time set-up of indexer_bwd_gemm_noalloc for the current device
+ * (see above); IBWD_OK, IBWD_ERR_UNSUPPORTED (not an sm_103 device) or
+ * IBWD_ERR_CUDA. */
+IBWD_API int indexer_bwd_gemm_noalloc_setup(void);
+
+/* Synchronizes `stream`, then reads and clears the status word of
+ * indexer_bwd_gemm_noalloc on the current device: IBWD_ERR_TIMEOUT if a
+ * kernel's bounded wait expired since the last read, IBWD_ERR_CUDA if the
+ * stream reports an error, IBWD_OK otherwise.  Allocates nothing. */
+IBWD_API int indexer_bwd_gemm_noalloc_status(void* stream);
 
 /*
  * The whole backward in one call: kernel 1 then kernel 2 above, queued on the

@@ -39,6 +39,8 @@ EXPORTS = (
     "indexer_bwd_last_device_status",
     "indexer_bwd_status_string",
     "indexer_bwd_gemm_noalloc",
+    "indexer_bwd_gemm_noalloc_setup",
+    "indexer_bwd_gemm_noalloc_status",
     "indexer_fwd",
     "indexer_fwd_dense",
     "indexer_bwd",

@@ -96,9 +96,9 @@ int score_grad_common(const float* I, float* A, const int32_t* idx, bool dense_o
   return e == cudaSuccess ? IBWD_OK : IBWD_ERR_CUDA;
 }
 
-size_t workspace_common(int B, int S_q, int S_k, int H, int D, int L, int mode) {
+size_t workspace_common(int B, int S_q, int S_k, int H, int D, int L, int mode, bool dense) {
   if (!shape_ok(B, S_q, S_k, H, D, L) || (mode != IBWD_DK_ATOMIC && mode != IBWD_DK_DETERMINISTIC)) return 0;
-  return ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC).total;
+  return ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC, dense).total;
 }
 
 // need_idx: the sparse variant requires topk_idx (the dense one passes NULL).
@@ -115,7 +115,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   if (mode != IBWD_DK_ATOMIC && mode != IBWD_DK_DETERMINISTIC) return IBWD_ERR_INVALID_ARG;
   if (B < 1 || S_q < 1 || S_k < 1 || L < 1 || H < 1 || D < 1) return IBWD_ERR_INVALID_ARG;
   if (!shape_ok(B, S_q, S_k, H, D, L)) return IBWD_ERR_UNSUPPORTED;
-  // the sort keeps a cursor and a tag per key of a batch in shared memory
+  // the key sort keeps one counter per key of a batch in shared memory
   if (mode == IBWD_DK_DETERMINISTIC && S_k > 40960) return IBWD_ERR_UNSUPPORTED;
   const ibwd_options o = opt ? *opt : ibwd_options{};
   if ((o.ids_global != 0 && o.ids_global != 1) || (o.dq_bf16 != 0 && o.dq_bf16 != 1) ||
@@ -139,7 +139,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   if (idx && !dev_ptr_ok(idx)) return IBWD_ERR_INVALID_ARG;
   if (I && !dev_ptr_ok(I)) return IBWD_ERR_INVALID_ARG;
   if (o.dk_bf16 && !dev_ptr_ok(o.dk_bf16)) return IBWD_ERR_INVALID_ARG;
-  const size_t need = ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC).total;
+  const size_t need = ibwd::gemm_workspace_layout(B, S_q, S_k, H, D, L, mode == IBWD_DK_DETERMINISTIC, !need_idx).total;
   if (!ws || ws_bytes < need || !dev_ptr_ok(ws)) return IBWD_ERR_WORKSPACE;
   ibwd::GemmArgs a{};
   a.q = q;
@@ -220,7 +220,7 @@ int indexer_bwd_score_grad(const float* index_score, float* attn_score, const in
 }
 
 size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk, int dk_mode) {
-  return workspace_common(B, S_q, S_k, H, D, topk, dk_mode);
+  return workspace_common(B, S_q, S_k, H, D, topk, dk_mode, false);
 }
 
 int indexer_bwd_gemm(const uint16_t* q, const uint16_t* k, const float* w, const float* dI,
@@ -236,7 +236,7 @@ int indexer_bwd_dense_score_grad(const float* index_score, float* attn_score, in
 }
 
 size_t indexer_bwd_dense_gemm_workspace_size(int B, int S, int H, int D, int dk_mode) {
-  return workspace_common(B, S, S, H, D, S, dk_mode);
+  return workspace_common(B, S, S, H, D, S, dk_mode, true);
 }
 
 int indexer_bwd_dense_gemm(const uint16_t* q, const uint16_t* k, const float* w, const float* dI, float* dq,

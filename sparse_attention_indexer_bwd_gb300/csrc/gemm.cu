@@ -1,58 +1,38 @@
-// Gemm stage of the lightning-indexer backward on sm_103a (kernel 2).
+// Gemm stage of the lightning-indexer backward, one query row at a time:
+// the kernel behind the allocation-free entry point (indexer_bwd_gemm_noalloc),
+// whose only scratch is the fp16 copy of k.  Atomic dK, top-k ids local to
+// their batch, fp32 outputs.
 //
 // Definition (cudnn-frontend #730 "optimize SM100 gradient kernels",
-// benchmark-harness comment, ref_grads; #549 names the kernel kernel_gemm and
-// its outputs d_index_q, d_weights, d_index_k), per query row t and selected
-// key s = idx[t,j] (padding ids, i.e. any id outside [0, S_k), are skipped):
-//   z[s,h]  = q[t,h,:] . k[s,:]                       (forward recompute)
-//   dW[t,h] = sum_s dI[t,s] relu(z[s,h])
+// benchmark-harness comment, ref_grads), per query row t and selected key
+// s = idx[t,j] (any id outside [0, S_k) is padding and skipped):
+//   z[s,h]  = q[t,h,:] . k[s,:];   dW[t,h] = sum_s dI[t,s] relu(z[s,h])
 //   dz[s,h] = dI[t,s] w[t,h] [z[s,h] > 0]
-//   dQ[t,h] = sum_s dz[s,h] k[s,:]
-//   dK[s]  += sum_h dz[s,h] q[t,h,:]
+//   dQ[t,h] = sum_s dz[s,h] k[s,:];   dK[s] += sum_h dz[s,h] q[t,h,:]
 //
 // Design: one persistent CTA per SM walks its query rows (a low-discrepancy
-// permutation of all rows, so concurrently running rows are far apart and
-// local-window key sets rarely collide).  Each row's valid slots are
-// compacted into tiles of 128 keys, and the keys are the M = 128 dimension of
-// every tensor-core MMA:
+// permutation of all rows, claimed from a counter).  Each row's valid slots
+// are compacted into tiles of 128 keys, the M = 128 dimension of every MMA:
 //   MMA1  Z^T[128 s, 64 h]   = Ksel[128 s, 128 d] . Q^T          (TMEM, fp32)
 //   MMA2  dK^T[128 d, 128 s] = Q^T[128 d, 64 h] . dz^T[64 h, 128 s] (TMEM, fp32)
 //   MMA3  dQ^T[128 d, 64 h] += Ksel^T[128 d, 128 s] . dz[128 s, 64 h]
-// Operands are fp16 in 128-byte-swizzled shared memory: k is converted once to
-// fp16 (bf16 -> fp16 is exact in fp16 range), q is converted per row, and dz
-// is scaled by a per-row power of two 2^c so that it stays in the fp16 normal
-// range (bf16 dz would cost ~1.6e-3 relative RMS, over the dK budget).  The
-// scale is undone exactly in the fp32 epilogues.
-//
-// The selected key rows are gathered with 16-byte cp.async copies spread over
-// a warp group (16 lanes per 256-byte row, the swizzle applied in the
-// destination address); their completion arrives on the stage barrier.
-// dK is produced transposed (TMEM lane = column d), so that in the epilogue
-// each warp instruction reduces one whole 128-byte line of a dK row.
+// Operands are fp16 in 128-byte-swizzled shared memory (k converted once, q
+// per row, dz with a per-row power-of-two scale 2^c undone in the fp32
+// epilogues).  The selected key rows are gathered by 16-byte cp.async; dK
+// leaves TMEM transposed (lane = column d) for full-line reductions.
 //
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
-//   0-3   gather: 16 cp.async per thread per tile (selected fp16 key rows)
-//   4     scan: row idx/dI staged in shared memory by bulk copies (one row
-//         ahead); valid count, max|dI| and scale; compaction into tile
-//         metadata
-//   5     MMA issuer (one thread) and TMEM owner (512 columns)
-//   6-7   Q loader: q[t] bf16 -> fp16 swizzled tile, w[t] -> shared
-//   8-11  dz group for heads 0-31, 12-15 dz group for heads 32-63: Z from
-//         TMEM -> dW partial sums in registers, dz -> fp16 shared tile; at row
-//         end the dW reduction; one row later the dQ epilogue (TMEM -> fp32)
-//   16-19 dK group for tile rows 0-63, 20-23 dK group for rows 64-127: dK^T
-//         tile from TMEM -> fp32 red.global.add (one 128-byte line per warp
-//         instruction) into dk, or plain stores into the per-slot workspace in
-//         deterministic mode
+//   0-3   gather;  4 scan (row ids and dI staged by bulk copies one row
+//   ahead, compaction into tile metadata);  5 MMA issuer and TMEM owner;
+//   6-7   Q loader;  8-15 dz (two groups of four for heads 0-31 / 32-63: dW
+//   partials, fp16 dz tile, dW reduction and the dQ epilogue);  16-23 dK
+//   (fp32 red.global.add of the transposed tile rows).
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
-#include <cuda_bf16.h>
-
 #include <algorithm>
 #include <atomic>
 
-#include "internal.h"
-#include "ptx.cuh"
+#include "kcommon.cuh"
 
 namespace ibwd {
 namespace {
@@ -66,7 +46,7 @@ constexpr int NGT = 128;                  // gather threads
 constexpr int NQT = 64;                   // Q-loader threads
 constexpr int NDZT = 256;                 // dz threads (two groups of 128)
 constexpr int NDKT = 256;                 // dK threads (two groups of 128)
-constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI [| pos] (sparse), dI [| pos] (dense)
+constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI
 
 constexpr uint32_t KTILE_BYTES = kBM * kDP * 2;   // 32 KB
 constexpr uint32_t KHALF_BYTES = kBM * 64 * 2;    // one 64-column half of a K tile
@@ -79,8 +59,6 @@ constexpr uint32_t TM_Z = 0, TM_DK = 128, TM_DQ = 384, TM_COLS = 512;
 
 struct TileMeta {
   int key[kBM];    // selected key (row of k within the batch)
-  int slot[kBM];   // deterministic mode: the slot's dK row in u (position mode: its position in key
-                   // order; slot mode: j, the row being r*L + j)
   float dis[kBM];  // dI[t, j] * 2^c
   int r, count, c, flags;
 };
@@ -124,31 +102,14 @@ struct KParams {
   float* dq;
   float* dw;
   float* dk;
-  float* u;         // deterministic: per-slot dK rows, or nullptr
-  const int* pos;   // deterministic, position mode: each slot's row in u (its position in key order);
-                    // else nullptr, and slot j of row r has row r*L + j
-  unsigned* sched;  // row counter in the workspace, zeroed by k_to_f16_kernel
+  unsigned* sched;  // row counter in the scratch, zeroed by the k conversion kernel
   unsigned* status;
   long long rows;
   unsigned long long perm_mul;
   unsigned long long wait_ns;
-  int B, S_q, S_k, H, D, L, dense;
+  int B, S_q, S_k, H, D, L;
   int staged;  // rows are staged in shared memory by bulk copies
-  int ids_global;  // slot ids index the flattened [B*S_k] keys
-  uint16_t* dq16;  // bf16 outputs instead of dq / dw when set
-  uint16_t* dw16;
 };
-
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
-
-// fp32 -> bf16 bits, round to nearest even (the optional bf16 outputs)
-__device__ __forceinline__ uint16_t to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 
 __device__ __forceinline__ long long row_of(long long u, const KParams& p) {
   return (long long)(((unsigned long long)u * p.perm_mul) % (unsigned long long)p.rows);
@@ -166,58 +127,9 @@ struct Ctx {
   int* rowq;
 };
 
-// Optional per-tile timeline (clock64 stamps of each role's progress in the
-// first CTAs), compiled only with -DIBWD_TRACE for pipeline analysis.
-enum TraceEv {
-  EV_SCAN_PUB, EV_GATHER_ISSUED, EV_MMA_KFULL, EV_MMA_Z, EV_MMA_DZFULL, EV_MMA_DKEMPTY, EV_MMA_DKDQ,
-  EV_DZ_ZFULL, EV_DZ_DONE, EV_DK_FULL, EV_DK_DONE, EV_Q_READY, EV_MMA_MFULL, EV_MMA_QFULL, EV_GATHER_KEMPTY,
-  EV_DZ_DZEMPTY, EV_DZW0, EV_DK_LD = EV_DZW0 + 8, EV_COUNT
-};
-#ifdef IBWD_TRACE
-constexpr int TRACE_CTAS = 4, TRACE_TILES = 256;
-__device__ unsigned long long g_trace[TRACE_CTAS][EV_COUNT][TRACE_TILES];
-// per CTA (first 1024): clock64 and %globaltimer at the start and at the
-// end, %smid, tiles processed
-constexpr int TRACE_ALL = 1024;
-__device__ unsigned long long g_trace_cta[TRACE_ALL][6];
-__device__ __forceinline__ unsigned long long trace_gtime() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-#define TRACE_CTA(i)                                                   \
-  do {                                                                 \
-    if (blockIdx.x < TRACE_ALL && threadIdx.x == 0) {                  \
-      g_trace_cta[blockIdx.x][(i)*2] = clock64();                      \
-      g_trace_cta[blockIdx.x][(i)*2 + 1] = trace_gtime();              \
-      unsigned smid;                                                   \
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));                \
-      g_trace_cta[blockIdx.x][4] = smid;                               \
-    }                                                                  \
-  } while (0)
-#define TRACE(ev, g)                                                                    \
-  do {                                                                                  \
-    if (blockIdx.x < TRACE_CTAS && (g) >= 0 && (g) < TRACE_TILES) g_trace[blockIdx.x][ev][g] = clock64(); \
-  } while (0)
-#else
-#define TRACE(ev, g) \
-  do {               \
-  } while (0)
-#define TRACE_CTA(i) \
-  do {               \
-  } while (0)
-#endif
-
 #define WAIT(bar, par) mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns)
 // Warp-uniform form for the MMA warp, which must stay converged (elect.sync).
 #define WAITW(bar, par) __all_sync(0xffffffffu, WAIT(bar, par))
-
-// A bounded wait that ignores the abort flag: used only to drain work that
-// was already issued before the kernel may exit.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const KParams& p) {
-  volatile int never = 0;
-  mbar_wait(bar, parity, &never, p.status, p.wait_ns);
-}
 
 // ------------------------------------------------------------ Q loader ----
 __device__ void q_role(const KParams& p, const Ctx& cx) {
@@ -255,33 +167,10 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
     cx.w_s[qb * kHP + tid] = tid < p.H ? __ldg(p.w + r * p.H + tid) : 0.f;
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->qfull[qb]);
-    if (tid == 0) TRACE(EV_Q_READY, (int)i);
   }
 }
 
 // ----------------------------------------------------------------- scan ---
-// Slot source of one query row: the staged copy in shared memory or global.
-struct RowSrc {
-  const int32_t* idx;  // nullptr for dense rows
-  const float* dI;
-  const int* pos;      // deterministic position mode: the slots' rows in u (else nullptr)
-  int Lr;              // slots to look at
-  int S_k;
-  unsigned off;        // global ids: b*S_k of the row's batch (else 0)
-  __device__ __forceinline__ bool key(int j, int& s) const {
-    if (!idx) {
-      s = j;
-      return true;
-    }
-    s = (int)((unsigned)idx[j] - off);
-    return (unsigned)s < (unsigned)S_k;
-  }
-};
-
-// OPT: the instance that serves the interface options (global ids, bf16
-// outputs) and the deterministic slot mode; the other instance carries none
-// of their instructions.
-template <bool OPT>
 __device__ void scan_role(const KParams& p, const Ctx& cx) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -298,8 +187,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
     const long long u = (long long)gridDim.x + v;
     return u < p.rows ? row_of(u, p) : -1;
   };
-  // |w| of a row, loaded early (two heads per lane, H <= 64) and reduced
-  // when the row is scanned
+  // |w| of a row, loaded early (two heads per lane, H <= 64)
   auto w_load = [&](long long r, float& w0, float& w1) {
     w0 = lane < p.H ? __ldg(p.w + r * p.H + lane) : 0.f;
     w1 = lane + 32 < p.H ? __ldg(p.w + r * p.H + lane + 32) : 0.f;
@@ -311,25 +199,15 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
     }
   };
   auto issue_row = [&](long long i, long long r) {
-    const int t = (int)(r % p.S_q);
     const int buf = (int)(i & 1);
     if (lane == 0) {
       // this thread's earlier generic reads of the buffer precede the async writes
       fence_proxy_async_smem();
       const uint32_t dst = smem_u32(rowbuf + buf * ROW_BYTES);
-      // packed: [idx (sparse)] dI [pos (deterministic position mode)], L*4 bytes apart
-      const uint32_t stride = (uint32_t)p.L * 4;
-      if (p.dense) {
-        const uint32_t bytes = (uint32_t)(((min(p.L, t + 1) * 4) + 15) & ~15);
-        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], p.pos ? 2 * bytes : bytes);
-        bulk_g2s(dst, p.dI + r * p.L, bytes, &cx.bars->rowfull[buf]);
-        if (p.pos) bulk_g2s(dst + stride, p.pos + r * p.L, bytes, &cx.bars->rowfull[buf]);
-      } else {
-        mbar_arrive_expect_tx(&cx.bars->rowfull[buf], p.pos ? 3 * stride : 2 * stride);
-        bulk_g2s(dst, p.idx + r * p.L, stride, &cx.bars->rowfull[buf]);
-        bulk_g2s(dst + stride, p.dI + r * p.L, stride, &cx.bars->rowfull[buf]);
-        if (p.pos) bulk_g2s(dst + 2 * stride, p.pos + r * p.L, stride, &cx.bars->rowfull[buf]);
-      }
+      const uint32_t stride = (uint32_t)p.L * 4;  // packed: idx | dI
+      mbar_arrive_expect_tx(&cx.bars->rowfull[buf], 2 * stride);
+      bulk_g2s(dst, p.idx + r * p.L, stride, &cx.bars->rowfull[buf]);
+      bulk_g2s(dst + stride, p.dI + r * p.L, stride, &cx.bars->rowfull[buf]);
     }
     staged_wait = i;
   };
@@ -342,48 +220,38 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
   w_load(r_next, wn0, wn1);
   for (long long i = 0;; ++i) {
     const long long r = r_next;
-    const int t = (int)(r % p.S_q);
     const unsigned pend = claim_issue();
     const float w0 = wn0, w1 = wn1;
     bool last = false;
-    RowSrc src;
-    src.S_k = p.S_k;
-    src.Lr = p.dense ? min(p.L, t + 1) : p.L;
-    src.off = (OPT && p.ids_global) ? (unsigned)((int)r / p.S_q) * (unsigned)p.S_k : 0u;  // rows < 2^31
+    const int32_t* idx;
+    const float* dI;
     if (p.staged) {
       const int buf = (int)(i & 1);
       if (!WAIT(&cx.bars->rowfull[buf], (uint32_t)((i >> 1) & 1))) goto done;
       staged_wait = -1;
       __syncwarp();
       const uint8_t* rb = rowbuf + buf * ROW_BYTES;
-      const uint32_t stride = (uint32_t)p.L * 4;
-      src.idx = p.dense ? nullptr : reinterpret_cast<const int32_t*>(rb);
-      src.dI = reinterpret_cast<const float*>(rb + (p.dense ? 0 : stride));
-      src.pos = p.pos ? reinterpret_cast<const int*>(rb + (p.dense ? 1 : 2) * stride) : nullptr;
+      idx = reinterpret_cast<const int32_t*>(rb);
+      dI = reinterpret_cast<const float*>(rb + (uint32_t)p.L * 4);
     } else {
-      src.idx = p.dense ? nullptr : p.idx + r * p.L;
-      src.dI = p.dI + r * p.L;
-      src.pos = p.pos ? p.pos + r * p.L : nullptr;
+      idx = p.idx + r * p.L;
+      dI = p.dI + r * p.L;
     }
     {
       // pass 1: number of valid slots and max |dI| over them
       int nv = 0;
       float mx = 0.f;
       if (p.staged) {
-        // 16-byte reads of the staged row, four slots per lane (the staged
-        // length is a multiple of 4; dense rows are masked at Lr)
-        const int nq4 = (src.Lr + 3) >> 2;
+        // 16-byte reads of the staged row, four slots per lane (L % 4 == 0)
+        const int nq4 = p.L >> 2;
         for (int q = lane; q < nq4; q += 32) {
-          const float4 dv = reinterpret_cast<const float4*>(src.dI)[q];
-          int4 id = make_int4(0, 0, 0, 0);
-          if (src.idx) id = reinterpret_cast<const int4*>(src.idx)[q];
+          const float4 dv = reinterpret_cast<const float4*>(dI)[q];
+          const int4 id = reinterpret_cast<const int4*>(idx)[q];
           const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
           const int ii[4] = {id.x, id.y, id.z, id.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const int j = 4 * q + k;
-            const bool v = src.idx ? (unsigned)ii[k] - src.off < (unsigned)src.S_k : j < src.Lr;
-            if (v) {
+            if ((unsigned)ii[k] < (unsigned)p.S_k) {
               ++nv;
               mx = fmaxf(mx, fabsf(dd[k]));
             }
@@ -392,11 +260,10 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
       } else {
-        for (int j0 = 0; j0 < src.Lr; j0 += 32) {
+        for (int j0 = 0; j0 < p.L; j0 += 32) {
           const int j = j0 + lane;
-          int s;
-          const bool v = j < src.Lr && src.key(j, s);
-          if (v) mx = fmaxf(mx, fabsf(src.dI[j]));
+          const bool v = j < p.L && (unsigned)idx[j] < (unsigned)p.S_k;
+          if (v) mx = fmaxf(mx, fabsf(dI[j]));
           nv += __popc(__ballot_sync(0xffffffffu, v));
         }
       }
@@ -411,14 +278,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
         w_load(r_next, wn0, wn1);
       }
       // per-row scale 2^c: max |dI w| 2^c lies in [2^13, 2^14), inside fp16 range
-      const float wm = warp_max(fmaxf(fabsf(w0), fabsf(w1)));
-      const float m = mx * wm;
-      int c = 0;
-      if (m > 0.f && m <= 3.0e38f) {
-        int e;
-        frexpf(m, &e);
-        c = max(-120, min(120, 14 - e));
-      }
+      const int c = dz_scale_exponent(mx * warp_max(fmaxf(fabsf(w0), fabsf(w1))));
       const float sc = pow2f(c);
       const int ntiles = max(1, (nv + kBM - 1) / kBM);
       // pass 2: compact the valid slots, in slot order, into tiles of 128
@@ -428,10 +288,10 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
         if (!WAIT(&cx.bars->mempty[ms], (uint32_t)(((g / MST) & 1) ^ 1))) goto done;
         TileMeta& M = cx.meta[ms];
         int fill = 0;
-        while (fill < kBM && jc < src.Lr) {
+        while (fill < kBM && jc < p.L) {
           const int j = jc + lane;
-          int s = 0;
-          const bool v = j < src.Lr && src.key(j, s);
+          const int s = j < p.L ? idx[j] : -1;
+          const bool v = (unsigned)s < (unsigned)p.S_k;
           const unsigned mask = __ballot_sync(0xffffffffu, v);
           const int tot = __popc(mask);
           const int rank = __popc(mask & lt_mask);
@@ -439,8 +299,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
           if (v && rank >= skip && rank < skip + room) {
             const int pos = fill + rank - skip;
             M.key[pos] = s;
-            M.slot[pos] = src.pos ? src.pos[j] : j;
-            M.dis[pos] = src.dI[j] * sc;
+            M.dis[pos] = dI[j] * sc;
           }
           const int taken = min(tot - skip, room);
           fill += taken;
@@ -460,7 +319,6 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
         }
         __syncwarp();
         mbar_arrive(&cx.bars->mfull[ms]);
-        if (lane == 0) TRACE(EV_SCAN_PUB, g);
       }
     }
     __syncwarp();
@@ -468,7 +326,8 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
   }
 done:
   // a row copy still in flight must land before the CTA can exit
-  if (staged_wait >= 0) drain_wait(&cx.bars->rowfull[staged_wait & 1], (uint32_t)((staged_wait >> 1) & 1), p);
+  if (staged_wait >= 0)
+    drain_wait(&cx.bars->rowfull[staged_wait & 1], (uint32_t)((staged_wait >> 1) & 1), p.status, p.wait_ns);
 }
 
 // --------------------------------------------------------------- gather ---
@@ -488,7 +347,6 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
     const long long b = M.r / p.S_q;
     const int st = g % KST;
     if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) break;
-    if (x == 0) TRACE(EV_GATHER_KEMPTY, g);
     const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES + dst_off;
     const __half* kb = p.k16 + b * (p.S_k + 1) * kDP + ch * 8;
     int key[kBM / 8];
@@ -500,7 +358,6 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
 #pragma unroll
     for (int i = 0; i < kBM / 8; ++i) cp_async16(kbase + i * 1024, kb + (long long)key[i] * kDP, 16);
     cp_async_mbar_arrive_noinc(&cx.bars->kfull[st]);
-    if (x == 0) TRACE(EV_GATHER_ISSUED, g);
     if (flags & F_END) break;
   }
   // copies in flight must land before the CTA can exit
@@ -508,16 +365,10 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------------ MMA ---
-// The MMA warp runs its loop with all 32 lanes (waits and descriptor math are
-// warp-uniform, so operands stay in uniform registers); an elected lane issues
-// each tcgen05.mma and commit.
 constexpr uint32_t ID_Z = idesc_f16_f32(128, 64, 0, 0);    // Z^T = K . Q^T
 constexpr uint32_t ID_DKT = idesc_f16_f32(128, 128, 1, 0);  // dK^T = Q^T . dz^T (Q as MN-major A)
 constexpr uint32_t ID_DQ = idesc_f16_f32(128, 64, 1, 1);   // dQ^T = K^T . dz (both MN-major)
 
-// Descriptors are built once per operand buffer; a k-step advances the start
-// address field (address >> 4, 14 bits: shared memory stays below 256 KB, so
-// the addition never carries out of the field).
 __device__ __forceinline__ void mma_z(const Ctx& cx, int g, int qb) {
   const uint64_t a0 = sw128_desc(cx.sbase + OFF_K + (g % KST) * KTILE_BYTES, 16, 1024);
   const uint64_t b0 = sw128_desc(cx.sbase + OFF_Q + qb * QTILE_BYTES, 16, 1024);
@@ -565,9 +416,7 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
       long long niq = iq;
       // the dK MMA of tile g first: the dK warps wait for it
       if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
-      TRACE(EV_MMA_DZFULL, g);
       if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
-      TRACE(EV_MMA_DKEMPTY, g);
       tc_fence_after();
       mma_dk(cx, g, (int)(iq & 1));
       umma_commit_elect(&B->dkfull[g & 1]);
@@ -575,20 +424,16 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
         // then Z of tile g+1
         const int g1 = g + 1;
         if (!WAITW(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) goto drain;
-        TRACE(EV_MMA_MFULL, g1);
         nflags = cx.meta[g1 % MST].flags;
         if (nflags & F_FIRST) {
           niq = iq + 1;
           if (!WAITW(&B->qfull[niq & 1], (uint32_t)((niq >> 1) & 1))) goto drain;
-          TRACE(EV_MMA_QFULL, g1);
         }
         if (!WAITW(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1))) goto drain;
-        TRACE(EV_MMA_KFULL, g1);
         if (!WAITW(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1))) goto drain;
         fence_proxy_async_smem();
         tc_fence_after();
         mma_z(cx, g1, (int)(niq & 1));
-        TRACE(EV_MMA_Z, g1);
         umma_commit_elect(&B->zfull[g1 & 1]);
       }
       if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
@@ -597,39 +442,29 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
       umma_commit_elect(&B->kempty[g % KST]);
       umma_commit_elect(&B->dzempty[g & 1]);
       if (flags & F_LAST) umma_commit_elect(&B->dqfull[iq & 1]);
-      TRACE(EV_MMA_DKDQ, g);
       if (flags & F_END) break;
       ++g;
       flags = nflags;
       iq = niq;
     }
-#ifdef IBWD_TRACE
-    if (blockIdx.x < TRACE_ALL && (threadIdx.x & 31) == 0) g_trace_cta[blockIdx.x][5] = (unsigned long long)g + 1;
-#endif
   }
 drain:
   // every MMA issued so far completes before TMEM can be released
   __syncwarp();
   umma_commit_elect(&B->drain);
-  drain_wait(&B->drain, 0, p);
+  drain_wait(&B->drain, 0, p.status, p.wait_ns);
 }
 
 // ------------------------------------------------------------ dz group ----
 // Group `hg` (0 or 1) owns heads 32*hg .. 32*hg+31 of every tile row.
-template <bool OPT>
-__device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int hg, long long iq, int r,
-                                            int c) {
+__device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int hg, long long iq, int r, int c) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return;
   tc_fence_after();
   const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + hg * 32;
   const float sc = pow2f(-c);
   const int d = qw * 32 + lane;  // TMEM lane = column of dQ
-  // dQ element (r, h, d), fp32 or (options) bf16; esh = log2 of the element size
-  const bool b16 = OPT && p.dq16;
-  const int esh = b16 ? 1 : 2;
-  char* dst = (b16 ? reinterpret_cast<char*>(p.dq16) : reinterpret_cast<char*>(p.dq)) +
-              (((long long)r * p.H * p.D + d) << esh);
+  float* dst = p.dq + (long long)r * p.H * p.D + d;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float v[16];
@@ -643,19 +478,12 @@ __device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         const int hh = hg * 32 + half * 16 + h;
-        if (hh < p.H) {
-          char* e = dst + (((long long)hh * p.D) << esh);
-          if (b16)
-            *reinterpret_cast<uint16_t*>(e) = to_bf16(v[h] * sc);
-          else
-            *reinterpret_cast<float*>(e) = v[h] * sc;
-        }
+        if (hh < p.H) dst[(long long)hh * p.D] = v[h] * sc;
       }
     }
   }
 }
 
-template <bool OPT>
 __device__ void dz_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int s = qw * 32 + lane;  // tile row = TMEM lane
@@ -683,46 +511,42 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     const uint64_t* w2 = reinterpret_cast<const uint64_t*>(cx.w_s + (iq & 1) * kHP + hg * 32);
     const uint64_t dis2 = pack2(__float_as_uint(dis), __float_as_uint(dis));
     if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
-    if (tdz == 0) TRACE(EV_DZ_ZFULL, g);
     if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
-    if (tdz == 0) TRACE(EV_DZ_DZEMPTY, g);
     tc_fence_after();
     const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
     const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
 #pragma unroll
     for (int zh = 0; zh < 2; ++zh) {
-    float z[16];
-    tmem_ld16(za + zh * 16, z);
-    tmem_wait_ld_dep16(z);
-    if (zh == 1) {
-      tc_fence_before();
-      mbar_arrive(&cx.bars->zempty[g & 1]);
-    }
-#pragma unroll
-    for (int c8 = zh * 2; c8 < zh * 2 + 2; ++c8) {
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h0 = c8 * 8 + e * 2;
-        const float z0 = z[h0 - zh * 16], z1 = z[h0 + 1 - zh * 16];
-        const uint64_t dw = mul_f32x2(dis2, w2[h0 >> 1]);
-        const bool p0 = z0 > 0.f, p1 = z1 > 0.f;
-        if (p0) acc[h0] = fmaf(dis, z0, acc[h0]);
-        if (p1) acc[h0 + 1] = fmaf(dis, z1, acc[h0 + 1]);
-        const float d0 = p0 ? __uint_as_float((uint32_t)dw) : 0.f;
-        const float d1 = p1 ? __uint_as_float((uint32_t)(dw >> 32)) : 0.f;
-        pk[e] = pack_half2(d0, d1);
+      float z[16];
+      tmem_ld16(za + zh * 16, z);
+      tmem_wait_ld_dep16(z);
+      if (zh == 1) {
+        tc_fence_before();
+        mbar_arrive(&cx.bars->zempty[g & 1]);
       }
-      const int chunk = hg * 4 + c8;  // 16-byte chunk of the 128-byte dz row
-      st_shared_v4(dzrow + ((chunk ^ (s & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-    }
+#pragma unroll
+      for (int c8 = zh * 2; c8 < zh * 2 + 2; ++c8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h0 = c8 * 8 + e * 2;
+          const float z0 = z[h0 - zh * 16], z1 = z[h0 + 1 - zh * 16];
+          const uint64_t dw = mul_f32x2(dis2, w2[h0 >> 1]);
+          const bool p0 = z0 > 0.f, p1 = z1 > 0.f;
+          if (p0) acc[h0] = fmaf(dis, z0, acc[h0]);
+          if (p1) acc[h0 + 1] = fmaf(dis, z1, acc[h0 + 1]);
+          const float d0 = p0 ? __uint_as_float((uint32_t)dw) : 0.f;
+          const float d1 = p1 ? __uint_as_float((uint32_t)(dw >> 32)) : 0.f;
+          pk[e] = pack_half2(d0, d1);
+        }
+        const int chunk = hg * 4 + c8;  // 16-byte chunk of the 128-byte dz row
+        st_shared_v4(dzrow + ((chunk ^ (s & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+      }
     }
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
-    if (tdz == 0) TRACE(EV_DZ_DONE, g);
-    if ((tdz & 31) == 0) TRACE(EV_DZW0 + (tdz >> 5), g);
     if ((flags & F_FIRST) && ep_r >= 0) {
-      dq_epilogue<OPT>(p, cx, hg, ep_iq, ep_r, ep_c);
+      dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
       ep_r = -1;
     }
     if (flags & F_LAST) {
@@ -745,13 +569,9 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
       mbar_arrive(&cx.bars->dwred[iq & 1]);
       if (tdz < kHP) {
         if (!WAIT(&cx.bars->dwred[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
-        if (tdz < p.H) {
-          const float dwv = (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
-          if (OPT && p.dw16)
-            p.dw16[(long long)r * p.H + tdz] = to_bf16(dwv);
-          else
-            p.dw[(long long)r * p.H + tdz] = dwv;
-        }
+        if (tdz < p.H)
+          p.dw[(long long)r * p.H + tdz] =
+              (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
       }
       ep_r = r;
       ep_c = c;
@@ -759,66 +579,23 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     }
     if (flags & F_END) break;
   }
-  if (ok && ep_r >= 0) dq_epilogue<OPT>(p, cx, hg, ep_iq, ep_r, ep_c);
+  if (ok && ep_r >= 0) dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
 }
 
 // ------------------------------------------------------------ dK group ----
-// TMEM holds dK^T: lane = column d, TMEM column = tile row.  A warp holds 32
-// columns (its lane quarter) of 32 tile rows per chunk.  It passes each half
-// chunk through its own 2 KB of shared memory (row-major, 16 rows x 32
-// floats) and reads it back four rows per instruction, so one 16-byte vector
-// reduction per lane covers four 128-byte lines of four dK rows (a quarter of
-// the instructions of one line per row).
-template <bool RED>
-__device__ __forceinline__ void dk_chunk(float* base, const int* ids, const float (&v)[32], int nrow, float sc,
-                                         int D, int dblk, float* stage) {
-  const int lane = threadIdx.x & 31;
-  const int rsub = lane >> 3, c4 = (lane & 7) * 4;  // this lane's row in a group of four, column offset
-  const bool con = dblk + c4 < D;                    // D % 8 == 0: the whole float4 is in range
-#pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    if (hf * 16 >= nrow) break;  // uniform
-    int idv[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) idv[k] = ids[hf * 16 + rsub + 4 * k];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) stage[e * 32 + lane] = v[hf * 16 + e] * sc;
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = rsub + 4 * k;
-      if (hf * 16 + e < nrow && con) {
-        const float4 x = *reinterpret_cast<const float4*>(stage + e * 32 + c4);
-        float* dst = base + (long long)idv[k] * D + dblk + c4;
-        if (RED)
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x), "f"(x.y), "f"(x.z),
-                       "f"(x.w));
-        else
-          *reinterpret_cast<float4*>(dst) = x;
-      }
-    }
-    __syncwarp();  // the stage is rewritten by the next half
-  }
-}
-
-template <bool OPT>
+// TMEM holds dK^T: lane = column d, TMEM column = tile row.  Group kg owns
+// tile rows 64*kg .. 64*kg+63 in two chunks of 32.
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3;
-  const int kg = (threadIdx.x - W_DK0 * 32) >> 7;  // group: tile rows 64*kg .. 64*kg+63
+  const int kg = (threadIdx.x - W_DK0 * 32) >> 7;
   float* stage = reinterpret_cast<float*>(cx.smem + OFF_DKST) + ((threadIdx.x >> 5) - W_DK0) * (16 * 32);
   for (int g = 0;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
     const TileMeta& M = cx.meta[ms];
     const int flags = M.flags, c = M.c, r = M.r, count = M.count;
-    // deterministic: the slots' dK rows in u (slot mode, in the options
-    // instance only: the row's block of L rows); else dK of the row's batch, by key
-    float* base = OPT ? (p.u ? (p.pos ? p.u : p.u + (long long)r * p.L * p.D)
-                             : p.dk + (long long)(r / p.S_q) * p.S_k * p.D)
-                      : (p.u ? p.u : p.dk + (long long)(r / p.S_q) * p.S_k * p.D);
-    const int* ids = p.u ? M.slot : M.key;
+    float* base = p.dk + (long long)(r / p.S_q) * p.S_k * p.D;
     if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
-    if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, g);
     tc_fence_after();
     const float sc = pow2f(-c);
     const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK + (uint32_t)(g & 1) * 128;
@@ -828,23 +605,16 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
       float v[32];
       tmem_ld32(ta + ch * 32, v);
       tmem_wait_ld_dep(v);
-      if (threadIdx.x == W_DK0 * 32 && ch == 0) TRACE(EV_DK_LD, g);
-      const int nrow = min(32, count - ch * 32);
-      if (p.u)
-        dk_chunk<false>(base, ids + ch * 32, v, nrow, sc, p.D, qw * 32, stage);
-      else
-        dk_chunk<true>(base, ids + ch * 32, v, nrow, sc, p.D, qw * 32, stage);
+      dk_chunk<true>(base, M.key + ch * 32, v, min(32, count - ch * 32), sc, p.D, qw * 32, stage);
     }
     tc_fence_before();
     mbar_arrive(&cx.bars->dkempty[g & 1]);
     mbar_arrive(&cx.bars->mempty[ms]);
-    if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_DONE, g);
     if (flags & F_END) return;
   }
 }
 
-template <bool OPT>
-__global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctx cx;
@@ -895,89 +665,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_kernel(const KParams p) {
   __syncthreads();
   tc_fence_after();
   cx.tmem = *tmem_slot;
-  // everything above overlaps the previous kernel's tail (programmatic
-  // dependent launch); the inputs it wrote are read only from here on
-  griddep_wait();
-  TRACE_CTA(0);
+  griddep_wait();  // the fp16 copy of k is written by the kernel before
 
   if (warp < W_SCAN) {
     gather_role(p, cx);
   } else if (warp == W_SCAN) {
-    scan_role<OPT>(p, cx);
+    scan_role(p, cx);
   } else if (warp == W_MMA) {
     mma_role(p, cx);  // the whole warp runs the loop; one elected lane issues
   } else if (warp < W_DZ0) {
     q_role(p, cx);
   } else if (warp < W_DK0) {
-    dz_role<OPT>(p, cx);
+    dz_role(p, cx);
   } else {
-    dk_role<OPT>(p, cx);
+    dk_role(p, cx);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == W_MMA) tmem_dealloc(cx.tmem, TM_COLS);
-  TRACE_CTA(1);
-}
-
-// k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
-// row S_k of each batch zero (padding rows of a tile copy it).
-// Launched programmatically after the score-grad kernel (which writes neither
-// k nor the workspace), it runs alongside it and waits for it before exiting,
-// so that its own completion implies the score-grad's.
-__global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16, int B, int S_k, int D,
-                                unsigned* __restrict__ sched) {
-  griddep_launch_dependents();  // the gemm kernel may start its prologue
-  if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;  // the gemm kernel's row counter
-  const long long rows = (long long)B * (S_k + 1);
-  const long long n = rows * (kDP / 8);
-  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < n;
-       x += (long long)gridDim.x * blockDim.x) {
-    const int ch = (int)(x % (kDP / 8));
-    const long long row = x / (kDP / 8);
-    const int b = (int)(row / (S_k + 1));
-    const int s = (int)(row % (S_k + 1));
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (s < S_k && ch * 8 < D) val = __ldg(reinterpret_cast<const uint4*>(k + ((long long)b * S_k + s) * D + ch * 8));
-    *reinterpret_cast<uint4*>(k16 + row * kDP + ch * 8) =
-        make_uint4(bf16x2_to_half2(val.x), bf16x2_to_half2(val.y), bf16x2_to_half2(val.z), bf16x2_to_half2(val.w));
-  }
-  griddep_wait();
-}
-
-// Launch with programmatic stream serialization when pdl is set: the kernel
-// may start before the previous one on the stream completes and must call
-// griddep_wait() before reading what that one writes.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_ex(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
-                      bool pdl, Args... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-}
-
-// The final fp32 dK -> bf16 (round to nearest even), 8 values per thread step.
-__global__ void dk_to_bf16_kernel(const float* __restrict__ dk, uint16_t* __restrict__ out, long long n) {
-  const long long n8 = n / 8;  // n = B*S_k*D, D a multiple of 8
-  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < n8; x += (long long)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(dk)[2 * x];
-    const float4 b = reinterpret_cast<const float4*>(dk)[2 * x + 1];
-    uint4 o;
-    o.x = (uint32_t)to_bf16(a.x) | ((uint32_t)to_bf16(a.y) << 16);
-    o.y = (uint32_t)to_bf16(a.z) | ((uint32_t)to_bf16(a.w) << 16);
-    o.z = (uint32_t)to_bf16(b.x) | ((uint32_t)to_bf16(b.y) << 16);
-    o.w = (uint32_t)to_bf16(b.z) | ((uint32_t)to_bf16(b.w) << 16);
-    reinterpret_cast<uint4*>(out)[x] = o;
-  }
 }
 
 unsigned long long gcd_u64(unsigned long long a, unsigned long long b) {
@@ -999,76 +706,31 @@ unsigned long long row_permutation_multiplier(long long rows) {
   return a % (unsigned long long)rows;
 }
 
+std::atomic<bool> g_attr_rows[64];
+
 }  // namespace
 
-cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
-cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
+// Scratch of the per-row kernel: its row counter (one 256-byte block), then
+// the fp16 copy of k, 256 bytes per key row plus one zero row per batch.
+size_t rows_workspace_bytes(int B, int S_k) { return 256 + (size_t)B * ((size_t)S_k + 1) * kDP * 2; }
 
-WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic) {
-  (void)H;
-  WsLayout w{};
-  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  size_t off = 0;
-  w.sched = off;
-  off = up(off + 4);
-  w.k16 = off;
-  off = up(off + (size_t)B * (S_k + 1) * kDP * 2);
-  w.nchunks = 0;
-  if (deterministic) {
-    const long long rows = (long long)B * S_q;
-    w.u = off;
-    off = up(off + (size_t)rows * L * D * 4);
-    w.nchunks = (long long)B * ((S_q + kSortRows - 1) / kSortRows);
-    w.hist = off;
-    off = up(off + (size_t)w.nchunks * S_k * 4);
-    w.key_start = off;
-    off = up(off + ((size_t)B * S_k + 1) * 4);
-    w.order = off;
-    off = up(off + (size_t)rows * L * 4);
-  }
-  w.total = off;
-  return w;
-}
-
-// Deterministic mode: position mode when a row's ids, dI and sorted positions
-// fit the row stage together (the dK rows then go to u in key order and the
-// segment sum streams them), else slot mode (row r*L + j per slot, read back
-// through the key-order slot list).
-bool det_position_mode(const GemmArgs& a) {
-  if (!a.deterministic) return false;
-  const size_t arrays = a.idx ? 3 : 2;
-  return a.L % 4 == 0 && arrays * (size_t)a.L * 4 <= ROW_BYTES && (uintptr_t)a.dI % 16 == 0 &&
-         (!a.idx || (uintptr_t)a.idx % 16 == 0);
-}
-
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
-  const WsLayout lay = gemm_workspace_layout(a.B, a.S_q, a.S_k, a.H, a.D, a.L, a.deterministic);
-  char* ws = static_cast<char*>(a.ws);
-  __half* k16 = reinterpret_cast<__half*>(ws + lay.k16);
-  unsigned* sched = reinterpret_cast<unsigned*>(ws + lay.sched);
-  {
-    const long long n = (long long)a.B * (a.S_k + 1) * (kDP / 8);
-    const int blocks = (int)std::min<long long>((n + 255) / 256, 8LL * a.num_sms);
-    // programmatic only right after this library's score-grad kernel: the
-    // kernel reads k before it waits for its predecessor
-    cudaError_t e = launch_ex(k_to_f16_kernel, (unsigned)blocks, 256u, 0, st, a.after_score_grad != 0, a.k, k16,
-                              a.B, a.S_k, a.D, sched);
-    if (e != cudaSuccess) return e;
-  }
-  if (a.deterministic) {
-    cudaError_t e = launch_det_sort(a, lay, st);
-    if (e != cudaSuccess) return e;
-  }
-  static std::atomic<bool> attr_set[64];  // per device; setting the attribute twice is harmless
+cudaError_t prepare_gemm_rows() {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[dev].store(true, std::memory_order_release);
-  }
+  if (dev >= 0 && dev < 64 && g_attr_rows[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(gemm_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) g_attr_rows[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t st) {
+  char* ws = static_cast<char*>(a.ws);
+  unsigned* sched = reinterpret_cast<unsigned*>(ws);
+  __half* k16 = reinterpret_cast<__half*>(ws + 256);
+  cudaError_t e = prepare_gemm_rows();
+  if (e != cudaSuccess) return e;
+  e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 1, false, a.num_sms, st);
+  if (e != cudaSuccess) return e;
   KParams p{};
   p.q = a.q;
   p.k16 = k16;
@@ -1077,12 +739,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.idx = a.idx;
   p.dq = a.dq;
   p.dw = a.dw;
-  p.dq16 = a.dq16;
-  p.dw16 = a.dw16;
-  p.ids_global = a.ids_global;
   p.dk = a.dk;
-  p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
-  p.pos = det_position_mode(a) ? reinterpret_cast<const int*>(ws + lay.order) : nullptr;
   p.sched = sched;
   p.status = a.status;
   p.rows = (long long)a.B * a.S_q;
@@ -1094,38 +751,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.H = a.H;
   p.D = a.D;
   p.L = a.L;
-  p.dense = a.idx == nullptr;
   // rows are staged in shared memory when they fit and are 16-byte aligned
-  const size_t arrays = (p.dense ? 1 : 2) + (p.pos ? 1 : 0);
-  const bool fits = arrays * a.L * 4 <= ROW_BYTES;
-  const bool al = (a.L % 4 == 0) && ((uintptr_t)a.dI % 16 == 0) && (p.dense || (uintptr_t)a.idx % 16 == 0);
-  p.staged = fits && al;
+  p.staged = 2 * (size_t)a.L * 4 <= ROW_BYTES && a.L % 4 == 0 && (uintptr_t)a.dI % 16 == 0 &&
+             (uintptr_t)a.idx % 16 == 0;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
-  // the options instance also serves the deterministic slot mode
-  const bool opt = p.ids_global || p.dq16 || p.dw16 || (p.u && !p.pos);
-  cudaError_t e = launch_ex(opt ? gemm_kernel<true> : gemm_kernel<false>, (unsigned)grid, (unsigned)NTHREADS,
-                            SMEM_BYTES, st, true, p);
-  if (e != cudaSuccess) return e;
-  if (a.deterministic) {
-    e = launch_det_segsum(a, lay, st);
-    if (e != cudaSuccess) return e;
-  }
-  if (a.dk16) {
-    const long long n = (long long)a.B * a.S_k * a.D;
-    const int blocks = (int)std::max<long long>(1, std::min<long long>((n / 8 + 255) / 256, 4LL * a.num_sms));
-    dk_to_bf16_kernel<<<blocks, 256, 0, st>>>(a.dk, a.dk16, n);
-    e = cudaGetLastError();
-  }
-  return e;
+  return launch_ex(gemm_rows_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
 }
-
-#ifdef IBWD_TRACE
-extern "C" __attribute__((visibility("default"))) int ibwd_trace_read(void* host, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
-}
-extern "C" __attribute__((visibility("default"))) int ibwd_trace_cta_read(void* host, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(host, g_trace_cta, bytes < sizeof(g_trace_cta) ? bytes : sizeof(g_trace_cta));
-}
-#endif
 
 }  // namespace ibwd

@@ -3,15 +3,17 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace ibwd {
 
 // Padded tile geometry of the gemm-stage kernel.
-constexpr int kBM = 128;  // keys per tile (the MMA M dimension for Z and dK)
-constexpr int kDP = 128;  // head dim padded to 128 (the MMA M dimension for dQ)
-constexpr int kHP = 64;   // indexer heads padded to 64 (the MMA N dimension for Z and dQ)
-constexpr int kSortRows = 8;  // query rows per chunk of the deterministic mode's key sort
+constexpr int kBM = 128;  // keys per tile (an MMA dimension of Z and dK)
+constexpr int kDP = 128;  // head dim padded to 128 (the MMA M dimension for dQ and dK)
+constexpr int kHP = 64;   // indexer heads padded to 64
+constexpr int kBlkRows = 4;     // query rows per block of the gemm stage
+constexpr int kSortBlocks = 2;  // blocks per chunk of the deterministic mode's key sort
 
 struct ScoreGradArgs {
   const float* index_score;  // [rows, L]
@@ -52,24 +54,53 @@ struct GemmArgs {
   uint16_t* dk16;        // if set: bf16 copy of the final dk, written after it
 };
 
+// Workspace of the gemm stage (indexer_bwd_gemm and the one-call forms).
+// The query rows are taken in blocks of kBlkRows consecutive rows of one
+// batch; a sparse block's work list is the union of its rows' valid keys,
+// stored as tile records of 128 entries:
+//   int key[128] | float dis[kBlkRows][128] | int pos[128] (deterministic)
+// (dis[r][e]: the sum of dI over row r's slots selecting key e, 0 when row r
+// does not select it; padding entries have key S_k and dis 0).
 struct WsLayout {
-  size_t sched;      // the gemm kernel's row counter (one 256-byte block)
+  size_t sched;      // 256 bytes: [0] the gemm kernel's block counter, [1] the union pass's CTA counter
   size_t k16;        // fp16 copy of k, [B, S_k + 1, 128]
-  size_t u;          // deterministic: per-slot dK rows [rows*L, D] fp32
-  size_t hist;       // deterministic: per-chunk key counts [nchunks, S_k] int32
-  size_t key_start;  // deterministic: CSR offsets [B*S_k + 1] int32
-  size_t order;      // deterministic [rows*L] int32: position mode, each valid slot's position in key
-                     // order (indexed by slot r*L + j); slot mode, the valid slots in key order
-                     // (ascending (r, j) within a key)
+  size_t binfo;      // sparse: int4 per block {tiles, dz scale exponent, entries, 0}
+  size_t border;     // sparse: the blocks in descending tile count (processing order)
+  size_t rec;        // sparse: tile records [nblocks][tcap][rstride bytes]
+  size_t u;          // deterministic: per-entry dK rows [entries_cap, D] fp32, in key order
+  size_t hist;       // deterministic sparse: per-chunk key counts [nchunks, S_k] int32
+  size_t key_start;  // deterministic: CSR offsets into u [B*S_k + 1] int32
   size_t total;
-  long long nchunks;
+  long long nblocks;      // B * nbpb
+  long long nchunks;      // deterministic sparse: B * ceil(nbpb / kSortBlocks)
+  long long entries_cap;  // deterministic: rows of u
+  int nbpb;               // blocks per batch, ceil(S_q / kBlkRows)
+  int tcap;               // sparse: tile records per block, ceil(min(S_k, kBlkRows*L) / 128)
+  int rstride;            // sparse: bytes per tile record (2560, or 3072 with positions)
 };
-WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic);
+WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic, int dense);
 
+// The blocked gemm stage (blk.cu): fp16 copy of k, the union pass (sparse),
+// the deterministic sort (det.cu), the gemm kernel, the segment sum.
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
-// Deterministic dK layout: true = dK rows in key order (positions staged with
-// the rows), false = dK rows by slot, summed through a key-order slot list.
-bool det_position_mode(const GemmArgs& a);
+
+// Deterministic mode (det.cu): the key sort of the blocks' entries (sparse) or
+// the closed-form CSR offsets (dense), run between the union pass and the
+// gemm kernel; the segment sum after it.
+cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
+cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
+
+// fp16 copy of k into k16 ([B][S_k+1][128], zero padded, row S_k zero) that
+// also zeroes nsched words of the counters at sched.  pdl: launched
+// programmatically behind this library's score-grad kernel.
+cudaError_t launch_k_to_f16(const uint16_t* k, __half* k16, int B, int S_k, int D, unsigned* sched, int nsched,
+                            bool pdl, int num_sms, cudaStream_t st);
+
+// The per-row gemm kernel (gemm.cu), atomic dK and no options: served to the
+// allocation-free entry point, whose only scratch is its fp16 copy of k.
+size_t rows_workspace_bytes(int B, int S_k);
+cudaError_t prepare_gemm_rows();  // per device: the kernel's shared-memory attribute
+cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t st);
 
 struct FwdArgs {
   const uint16_t* q;     // bf16 [rows, H, D]

@@ -80,6 +80,36 @@ def test_whole_call_equals_the_pair_of_calls(cases, name):
         assert np.array_equal(u.view(np.int32), v.view(np.int32))
 
 
+@pytest.mark.parametrize("shape", [(24, 70000, 512, "uniform", 0), (12, 40960, 4200, "uniform", 1),
+                                   (40, 3000, 700, "window", 1)])
+def test_union_pass_windows_and_wide_rows(shape):
+    # The gemm stage takes four query rows at a time against the union of
+    # their keys, built per window of at most 32768 keys (4096 when a row has
+    # more than 4096 slots): S_k = 70000 needs three windows, topk = 4200 ten;
+    # the local-window rows repeat keys within a row (summed per key).  Both
+    # against the oracle; the deterministic ones bitwise run to run.
+    S_q, S_k, topk, ids, mode = shape
+    wl = W(f"union_{S_k}_{topk}", 1, 4, 32, S_q, S_k, topk, ids, 23)
+    x = case_inputs(wl)
+    ref = oracle_all(wl, x)
+    runs = [gpu_all(wl, x, dk_mode=mode) for _ in range(2)]
+    assert_close(*runs[0][1:], ref[1:], tag=f"union {shape}")
+    assert np.array_equal(runs[0][1], runs[1][1]) and np.array_equal(runs[0][2], runs[1][2])
+    if mode == ibwd.IBWD_DK_DETERMINISTIC:
+        assert np.array_equal(runs[0][3].view(np.int32), runs[1][3].view(np.int32))
+
+
+@pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "dense_small", "dense_256"])
+def test_whole_call_equals_the_pair_of_calls(cases, name):
+    # indexer_bwd runs the same two kernels: dI, dq, dw and the
+    # deterministic dK are bitwise those of the two calls
+    wl, x, _ = cases[name]
+    a = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC, path="whole")
+    b = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC, path="pair")
+    for u, v in zip(a, b):
+        assert np.array_equal(u.view(np.int32), v.view(np.int32))
+
+
 @pytest.mark.parametrize("topk", [1364, 1368])
 def test_deterministic_layouts_at_the_stage_limit(topk):
     # 12 bytes a slot (ids, dI, sorted positions) fill the gemm kernel's 16 KB
