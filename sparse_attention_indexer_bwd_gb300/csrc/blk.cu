@@ -40,17 +40,18 @@
 // owns one (r,h) for the whole block: dW accumulates in a register over the
 // keys, with no cross-lane reduction per tile.
 //
-// Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
-//   0-3   gather: the tile's 128 fp16 key rows by 16-byte cp.async into a
+// Warp roles (32 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
+//   0-1   gather: the tile's 128 fp16 key rows by 16-byte cp.async into a
 //         K stage (two stages)
-//   4     scan: claims blocks, copies each tile record into a shared ring
+//   2     scan: claims blocks, copies each tile record into a shared ring
 //         (bulk copy; dense blocks: builds it from dI), publishes the block
-//   5     MMA issuer (one elected lane) and TMEM owner
-//   6-7   Q loader: the block's q rows by cp.async, converted to fp16 in
+//   3     Z MMA issuer (one elected lane) and TMEM owner
+//   4     dQ / dK MMA issuer
+//   5-7   Q loader: the block's q rows by cp.async, converted to fp16 in
 //         place; w
-//   8-15  dz: Z -> mask, dW partial, fp16 dz tile; at block end dW and the
+//   8-23  dz: Z -> mask, dW partial, fp16 dz tile; at block end dW and the
 //         dQ epilogue (TMEM -> fp32)
-//   16-23 dK: dK^T tile from TMEM -> fp32 red.global.add (one 128-byte line
+//   24-31 dK: dK^T tile from TMEM -> fp32 red.global.add (one 128-byte line
 //         per warp-instruction lane group) into dk, or plain stores of the
 //         entry's row into u at its sorted position (deterministic mode)
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
@@ -83,9 +84,17 @@ struct UParams {
   unsigned* done;      // CTA counter, zeroed by the k conversion kernel
   long long nblocks;
   int S_q, S_k, H, L, nbpb, tcap, rstride, ids_global;
-  int W;     // key window per pass (multiple of 1024)
-  int dcap;  // per-row capacity of the dedup arrays: min(L, W)
+  int W;       // key window per pass (multiple of 1024)
+  int dcap;    // per-row capacity of the dedup arrays: min(L, W)
+  int staged;  // the block's ids and dI rows are copied into shared memory (Lp = L rounded up to 4)
 };
+
+// Whether a block's dW is summed per key (1) rather than recovered from the
+// dQ accumulator: when the smallest |w| of its heads is zero, below 2^-12 of
+// the largest, or not finite.
+__device__ __forceinline__ int direct_dw(float wmin, float wmax) {
+  return (wmin > 0.f && wmin >= 0x1p-12f * wmax && wmax <= 3.0e38f) ? 0 : 1;
+}
 
 // Exclusive prefix of the popcounts of n words (n a multiple of 32), by one
 // warp; returns the total.
@@ -110,6 +119,28 @@ __device__ __forceinline__ int warp_popc_prefix(const uint32_t* bm, int* pf, int
   return __shfl_sync(FULL, incl, 31);
 }
 
+// Copies the block's rows of a [rows, L] array into shared memory rows of Lp
+// elements (cp.async: 16-byte pieces when the rows are 16-byte aligned, else
+// 4-byte ones), all in flight at once; the caller waits.
+__device__ __forceinline__ void stage_rows(uint32_t dst, const void* src_base, long long row0, int Rb, int L, int Lp) {
+  const char* src = static_cast<const char*>(src_base) + row0 * L * 4;
+  if ((L & 3) == 0) {
+    const int per = L >> 2;  // 16-byte pieces per row
+    for (int x = threadIdx.x; x < Rb * per; x += UT) {
+      const int r = x / per, c = x - r * per;
+      cp_async16(dst + (uint32_t)(r * Lp + 4 * c) * 4, src + ((long long)r * L + 4 * c) * 4, 16);
+    }
+  } else {
+    for (int x = threadIdx.x; x < Rb * L; x += UT) {
+      const int r = x / L, c = x - r * L;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst + (uint32_t)(r * Lp + c) * 4),
+                   "l"(src + ((long long)r * L + c) * 4)
+                   : "memory");
+    }
+  }
+  cp_async_commit();
+}
+
 // One CTA per block.  Per window of W keys: a bitmap of each row's valid keys
 // and of their union; popcount prefixes give every key its rank (row-local
 // and union); each row's dI is summed per distinct key in slot order (rows
@@ -122,11 +153,14 @@ __device__ __forceinline__ int warp_popc_prefix(const uint32_t* bm, int* pf, int
 __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   extern __shared__ __align__(16) uint32_t us[];
   const int WW = p.W >> 5;
+  const int Lp = (p.L + 3) & ~3;
   uint32_t* bm = us;                                      // [5][WW]: rows 0-3, union
   int* pf = reinterpret_cast<int*>(us + 5 * WW);          // [5][WW]
   float* drow = reinterpret_cast<float*>(us + 10 * WW);   // [4][dcap]
+  int* ids_s = reinterpret_cast<int*>(drow + R * p.dcap);  // staged: [4][Lp] ids, then [4][Lp] dI
+  float* dI_s = reinterpret_cast<float*>(ids_s + R * Lp);
   __shared__ int s_cnt[5], s_kmin[4], s_kmax[4];
-  __shared__ float s_wmax[4], s_dmax[4][R];
+  __shared__ float s_wmax[4], s_wmin[4], s_dmax[4][R];
   __shared__ int s_last;
   griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -137,36 +171,65 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   const long long row0 = (long long)bb * p.S_q + t0;
   const unsigned off = p.ids_global ? (unsigned)bb * (unsigned)p.S_k : 0u;  // rows < 2^31
   const bool own = warp < Rb;
-  const int32_t* ir = p.idx + (own ? (row0 + warp) * p.L : 0);
-  const float* dr_in = p.dI + (own ? (row0 + warp) * p.L : 0);
+  // this warp's row: in shared memory when staged, else global
+  const int32_t* ir = p.staged ? ids_s + warp * Lp : p.idx + (own ? (row0 + warp) * p.L : 0);
+  const float* dr_in = p.staged ? dI_s + warp * Lp : p.dI + (own ? (row0 + warp) * p.L : 0);
+  if (p.staged) stage_rows(smem_u32(ids_s), p.idx, row0, Rb, p.L, Lp);
 
-  // key range of the block's valid slots; max |w| per row
-  int kmin = INT_MAX, kmax = -1;
-  float wmax = 0.f;
+  float wmax = 0.f, wmin = 3.0e38f;  // over the row's heads; wmin stays large for rows past the block
   if (own) {
-    for (int j = lane; j < p.L; j += 32) {
-      const int s = (int)((unsigned)__ldg(ir + j) - off);
-      if ((unsigned)s < (unsigned)p.S_k) {
-        kmin = min(kmin, s);
-        kmax = max(kmax, s);
+    for (int h = lane; h < p.H; h += 32) {
+      const float a = fabsf(__ldg(p.w + (row0 + warp) * p.H + h));
+      wmax = fmaxf(wmax, a);
+      wmin = fminf(wmin, a);
+    }
+    wmax = warp_max(wmax);
+    wmin = -warp_max(-wmin);
+  }
+  if (p.staged) {
+    cp_async_wait_all();
+    __syncthreads();
+  }
+  // key range of the block's valid slots (one window covers every key when S_k <= W)
+  int kmin = 0, kmax = p.S_k - 1;
+  if (p.S_k > p.W) {
+    kmin = INT_MAX;
+    kmax = -1;
+    if (own) {
+      for (int j = lane; j < p.L; j += 32) {
+        const int s = (int)((unsigned)ir[j] - off);
+        if ((unsigned)s < (unsigned)p.S_k) {
+          kmin = min(kmin, s);
+          kmax = max(kmax, s);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(FULL, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(FULL, kmax, o));
       }
     }
-    for (int h = lane; h < p.H; h += 32) wmax = fmaxf(wmax, fabsf(__ldg(p.w + (row0 + warp) * p.H + h)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      kmin = min(kmin, __shfl_xor_sync(FULL, kmin, o));
-      kmax = max(kmax, __shfl_xor_sync(FULL, kmax, o));
-      wmax = fmaxf(wmax, __shfl_xor_sync(FULL, wmax, o));
+    if (lane == 0) {
+      s_kmin[warp] = kmin;
+      s_kmax[warp] = kmax;
     }
   }
   if (lane == 0) {
-    s_kmin[warp] = kmin;
-    s_kmax[warp] = kmax;
     s_wmax[warp] = wmax;
+    s_wmin[warp] = wmin;
   }
   __syncthreads();
-  kmin = min(min(s_kmin[0], s_kmin[1]), min(s_kmin[2], s_kmin[3]));
-  kmax = max(max(s_kmax[0], s_kmax[1]), max(s_kmax[2], s_kmax[3]));
+  if (p.S_k > p.W) {
+    kmin = min(min(s_kmin[0], s_kmin[1]), min(s_kmin[2], s_kmin[3]));
+    kmax = max(max(s_kmax[0], s_kmax[1]), max(s_kmax[2], s_kmax[3]));
+  }
+  // dI is written by the kernel before this one (score-grad)
+  griddep_wait();
+  if (p.staged) {
+    stage_rows(smem_u32(dI_s), p.dI, row0, Rb, p.L, Lp);
+    cp_async_wait_all();
+    __syncthreads();
+  }
 
   float dmax[R] = {0.f, 0.f, 0.f, 0.f};
   int base = 0;
@@ -177,17 +240,18 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
     bool dup = false;
     if (own) {
       for (int j = lane; j < p.L; j += 32) {
-        const int s = (int)((unsigned)__ldg(ir + j) - off);
+        const int s = (int)((unsigned)ir[j] - off);
         const unsigned x = (unsigned)(s - w0);
         if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
           const uint32_t bit = 1u << (x & 31);
           const uint32_t old = atomicOr(&bm[warp * WW + (x >> 5)], bit);
           dup |= (old & bit) != 0u;
-          atomicOr(&bm[4 * WW + (x >> 5)], bit);
         }
       }
     }
     dup = __any_sync(FULL, dup);
+    __syncthreads();
+    for (int i = tid; i < WW; i += UT) bm[4 * WW + i] = bm[i] | bm[WW + i] | bm[2 * WW + i] | bm[3 * WW + i];
     __syncthreads();
     for (int x = warp; x < 5; x += UT / 32) {
       const int n = warp_popc_prefix(bm + x * WW, pf + x * WW, WW);
@@ -195,7 +259,6 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
     }
     __syncthreads();
     if (own) {
-      griddep_wait();  // dI is written by the kernel before this one (score-grad)
       float* drr = drow + warp * p.dcap;
       const uint32_t* bmr = bm + warp * WW;
       const int* pfr = pf + warp * WW;
@@ -208,11 +271,11 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
         int rank = -1;
         float v = 0.f;
         if (j < p.L) {
-          const int s = (int)((unsigned)__ldg(ir + j) - off);
+          const int s = (int)((unsigned)ir[j] - off);
           const unsigned x = (unsigned)(s - w0);
           if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
             rank = pfr[x >> 5] + __popc(bmr[x >> 5] & ((1u << (x & 31)) - 1u));
-            v = __ldg(dr_in + j);
+            v = dr_in[j];
           }
         }
         if (!dup) {
@@ -230,41 +293,28 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
       }
     }
     __syncthreads();
-    // the union's entries of this window, in ascending key order
-    for (int i = tid; i < WW; i += UT) {
-      uint32_t m = bm[4 * WW + i];
-      if (!m) continue;
-      int u = base + pf[4 * WW + i];
-      uint32_t mr[R];
-      int pr[R];
+    // the union's entries of this window, in ascending key order: a warp
+    // takes one bitmap word at a time and lane l its bit l, so the set lanes
+    // write consecutive entries
+    for (int i = warp; i < WW; i += UT / 32) {
+      const uint32_t m = bm[4 * WW + i];
+      if (!((m >> lane) & 1u)) continue;
+      const uint32_t below = (1u << lane) - 1u;
+      const int ug = base + pf[4 * WW + i] + __popc(m & below);
+      char* rb = p.rec + ((long long)b * p.tcap + (ug >> 7)) * p.rstride;
+      reinterpret_cast<int*>(rb + REC_KEY)[ug & 127] = w0 + 32 * i + lane;
+      float* dd = reinterpret_cast<float*>(rb + REC_DIS);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        mr[r] = bm[r * WW + i];
-        pr[r] = pf[r * WW + i];
-      }
-      while (m) {
-        const int bit = __ffs(m) - 1;
-        m &= m - 1u;
-        const uint32_t below = (1u << bit) - 1u;
-        char* rb = p.rec + ((long long)b * p.tcap + (u >> 7)) * p.rstride;
-        const int e = u & 127;
-        reinterpret_cast<int*>(rb + REC_KEY)[e] = w0 + 32 * i + bit;
-        float* dd = reinterpret_cast<float*>(rb + REC_DIS);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float d = ((mr[r] >> bit) & 1u) ? drow[r * p.dcap + pr[r] + __popc(mr[r] & below)] : 0.f;
-          dd[r * 128 + e] = d;
-          dmax[r] = fmaxf(dmax[r], fabsf(d));
-        }
-        ++u;
+        const uint32_t mr = bm[r * WW + i];
+        const float d = ((mr >> lane) & 1u) ? drow[r * p.dcap + pf[r * WW + i] + __popc(mr & below)] : 0.f;
+        dd[r * 128 + (ug & 127)] = d;
+        dmax[r] = fmaxf(dmax[r], fabsf(d));
       }
     }
     base += s_cnt[4];
     __syncthreads();  // the next window rewrites the bitmaps
   }
-  // (a block without valid slots never waited above; the counter below was
-  // zeroed by the kernel before this one)
-  griddep_wait();
   const int U = base;
   const int ntiles = max(1, (U + 127) >> 7);
   for (int e = U + tid; e < ntiles * 128; e += UT) {  // padding entries: the zero key row, no weight
@@ -282,12 +332,14 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   }
   __syncthreads();
   if (tid == 0) {
-    float m = 0.f;
+    float m = 0.f, wx = 0.f, wn = 3.0e38f;
     for (int r = 0; r < R; ++r) {
       const float d = fmaxf(fmaxf(s_dmax[0][r], s_dmax[1][r]), fmaxf(s_dmax[2][r], s_dmax[3][r]));
       m = fmaxf(m, d * s_wmax[r]);
+      wx = fmaxf(wx, s_wmax[r]);
+      wn = fminf(wn, s_wmin[r]);
     }
-    p.binfo[b] = make_int4(ntiles, dz_scale_exponent(m), U, 0);
+    p.binfo[b] = make_int4(ntiles, dz_scale_exponent(m), U, direct_dw(wn, wx));
     __threadfence();
     s_last = atomicAdd(p.done, 1u) == (unsigned)(p.nblocks - 1);
   }
@@ -327,9 +379,10 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
 constexpr int KST = 2;  // K-tile stages
 constexpr int MST = 4;  // tile-record ring
 constexpr int BQ = 4;   // block ring (scan -> Q loader)
-constexpr int NTHREADS = 768;
-constexpr int W_GATHER0 = 0, W_SCAN = 4, W_MMA = 5, W_Q0 = 6, W_DZ0 = 8, W_DK0 = 16;
-constexpr int NGT = 128, NQT = 64, NDZT = 256, NDKT = 256;
+constexpr int NTHREADS = 1024;
+constexpr int W_GATHER0 = 0, W_SCAN = 2, W_MMA = 3, W_GMMA = 4, W_Q0 = 5, W_DZ0 = 8, W_DK0 = 24;
+constexpr int NGT = 64, NQT = 96, NDZT = 512, NDKT = 256;
+constexpr int NKQ = 4;  // key quarters of a tile: four dz warps per TMEM lane quarter
 
 constexpr uint32_t KTILE = kBM * kDP * 2;  // 32 KB: [2 d-halves][128 keys][128 B]
 constexpr uint32_t KHALF = kBM * 128;      // 16 KB
@@ -348,7 +401,8 @@ struct Hdr {        // per tile, written by the scan
   int c;            // dz scale exponent of the block
   int flags;
   int batch;
-  int pad[2];
+  int direct;       // dW of this block by per-key accumulation (some |w| is zero or tiny)
+  int pad;
 };
 
 struct Bars {
@@ -370,8 +424,8 @@ constexpr uint32_t OFF_DZ = OFF_Q + 2 * QDH;
 constexpr uint32_t OFF_REC = OFF_DZ + 2 * DZKC;
 constexpr uint32_t OFF_HDR = OFF_REC + MST * REC_BYTES;
 constexpr uint32_t OFF_W = OFF_HDR + MST * sizeof(Hdr);      // [4 rows][64 heads] fp32
-constexpr uint32_t OFF_DWP = OFF_W + NR * 4;                 // dW partials [2 key halves][256]
-constexpr uint32_t OFF_DKST = OFF_DWP + 2 * NR * 4;          // dK transpose stages, 2 KB per dK warp
+constexpr uint32_t OFF_DWP = OFF_W + NR * 4;                 // dW partials [4][256]
+constexpr uint32_t OFF_DKST = OFF_DWP + NKQ * NR * 4;        // dK transpose stages, 2 KB per dK warp
 constexpr uint32_t OFF_BQ = OFF_DKST + (NDKT / 32) * 2048;   // int4 per block ring slot
 constexpr uint32_t OFF_BARS = OFF_BQ + BQ * 16;
 constexpr uint32_t OFF_MISC = OFF_BARS + sizeof(Bars);
@@ -425,6 +479,34 @@ __device__ __forceinline__ const int* rec_pos(const Ctx& cx, int ms) {
 // Warp-uniform form for the MMA warp, which must stay converged (elect.sync).
 #define WAITW(bar, par) __all_sync(FULL, WAIT(bar, par))
 
+// Optional per-tile timeline (clock64 stamps of each role's progress in the
+// first CTAs), compiled only with -DIBWD_TRACE for pipeline analysis.
+enum TraceEv {
+  EV_SCAN_PUB, EV_GATHER_ISSUED, EV_MMA_ZA, EV_MMA_ZB, EV_MMA_DQ, EV_MMA_DK, EV_DZ_ZA, EV_DZ_ZB, EV_DZ_DONE,
+  EV_DK_FULL, EV_DK_DONE, EV_Q_START, EV_Q_DONE, EV_COUNT
+};
+#ifdef IBWD_TRACE
+constexpr int TRACE_CTAS = 4, TRACE_TILES = 512;
+__device__ unsigned long long g_trace[TRACE_CTAS][EV_COUNT][TRACE_TILES];
+constexpr int TRACE_ALL = 1024;
+__device__ unsigned long long g_trace_cta[TRACE_ALL][4];  // clock64 start, end; tiles; blocks
+#define TRACE(ev, g)                                                                                      \
+  do {                                                                                                    \
+    if (blockIdx.x < TRACE_CTAS && (g) >= 0 && (g) < TRACE_TILES) g_trace[blockIdx.x][ev][g] = clock64(); \
+  } while (0)
+#define TRACE_CTA(i, v)                                                   \
+  do {                                                                    \
+    if (blockIdx.x < TRACE_ALL) g_trace_cta[blockIdx.x][i] = (v);         \
+  } while (0)
+#else
+#define TRACE(ev, g) \
+  do {               \
+  } while (0)
+#define TRACE_CTA(i, v) \
+  do {                  \
+  } while (0)
+#endif
+
 // Dense blocks in descending work: the last blocks of each batch first.
 __device__ __forceinline__ long long dense_block_at(const BParams& p, long long pos) {
   const long long jb = p.nbpb - 1 - pos / p.B;
@@ -454,17 +536,18 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
     const int t0 = jb * R;
     const int Rb = min(R, p.S_q - t0);
     const int row0 = batch * p.S_q + t0;
-    int ntiles, c, U;
+    int ntiles, c, U, direct;
     if (!p.dense) {
       const int4 bi = __ldg(p.binfo + b);
       ntiles = bi.x;
       c = bi.y;
       U = bi.z;
+      direct = bi.w;
     } else {
       // keys [0, t0 + Rb); the scale from max |dI| over each row's causal keys and max |w|
       U = t0 + Rb;
       ntiles = (U + kBM - 1) / kBM;
-      float m = 0.f;
+      float m = 0.f, wx = 0.f, wn = 3.0e38f;
       for (int r = 0; r < Rb; ++r) {
         const float* dr = p.dI + (long long)(row0 + r) * p.S_q;
         const int n = t0 + r + 1;
@@ -489,11 +572,19 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
         } else {
           for (int j = lane; j < n; j += 32) mx = fmaxf(mx, fabsf(__ldg(dr + j)));
         }
-        float wm = 0.f;
-        for (int h = lane; h < p.H; h += 32) wm = fmaxf(wm, fabsf(__ldg(p.w + (long long)(row0 + r) * p.H + h)));
-        m = fmaxf(m, warp_max(mx) * warp_max(wm));
+        float wm = 0.f, wl = 3.0e38f;
+        for (int h = lane; h < p.H; h += 32) {
+          const float a = fabsf(__ldg(p.w + (long long)(row0 + r) * p.H + h));
+          wm = fmaxf(wm, a);
+          wl = fminf(wl, a);
+        }
+        wm = warp_max(wm);
+        m = fmaxf(m, warp_max(mx) * wm);
+        wx = fmaxf(wx, wm);
+        wn = fminf(wn, -warp_max(-wl));
       }
       c = dz_scale_exponent(m);
+      direct = direct_dw(wn, wx);
     }
     // publish the block to the Q loader; warm L2 with its q rows
     if (!WAIT(&B->bempty[i % BQ], ((i / BQ) & 1) ^ 1)) return;
@@ -521,10 +612,11 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
       uint8_t* rs = cx.smem + OFF_REC + ms * REC_BYTES;
       if (!p.dense) {
         if (lane == 0) {
-          cx.hdr[ms] = Hdr{row0, Rb, max(count, 0), c, flags, batch, {0, 0}};
+          cx.hdr[ms] = Hdr{row0, Rb, max(count, 0), c, flags, batch, direct, 0};
           fence_proxy_async_smem();  // earlier generic reads of the slot precede the async writes
           mbar_arrive_expect_tx(&B->mfull[ms], copy_bytes);
           bulk_g2s(smem_u32(rs), p.rec + ((long long)b * p.tcap + k) * p.rstride, copy_bytes, &B->mfull[ms]);
+          TRACE(EV_SCAN_PUB, g);
         }
       } else {
         int* key = reinterpret_cast<int*>(rs + REC_KEY);
@@ -548,7 +640,7 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
         }
         __syncwarp();
         if (lane == 0) {
-          cx.hdr[ms] = Hdr{row0, Rb, count, c, flags, batch, {0, 0}};
+          cx.hdr[ms] = Hdr{row0, Rb, count, c, flags, batch, direct, 0};
           mbar_arrive(&B->mfull[ms]);
         }
       }
@@ -566,14 +658,16 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
 }
 
 // --------------------------------------------------------------- gather ---
-// Thread x copies chunk (x % 16) of entries (x / 16) + 8i, i = 0..15: every
+// Thread x copies chunk (x % 16) of entries (x / 16) + 4i, i = 0..31: every
 // warp instruction moves two whole 256-byte key rows.  Row e of the tile
 // lands in the 128-byte-swizzle layout: half (chunk / 8), XOR (chunk % 8) ^
 // (e % 8).  Each thread's copies arrive on the stage barrier when they land.
 __device__ void gather_role(const BParams& p, const Ctx& cx) {
-  const int x = threadIdx.x - W_GATHER0 * 32;  // 0..127
+  const int x = threadIdx.x - W_GATHER0 * 32;  // 0..63
   const int rsub = x >> 4, ch = x & 15;
-  const uint32_t dst_off = (ch >> 3) * KHALF + rsub * 128 + (((ch & 7) ^ rsub) << 4);
+  // rows rsub + 4i: (row % 8) alternates between rsub and rsub + 4
+  const uint32_t off0 = (ch >> 3) * KHALF + rsub * 128 + (((ch & 7) ^ rsub) << 4);
+  const uint32_t off1 = (ch >> 3) * KHALF + (rsub + 4) * 128 + (((ch & 7) ^ (rsub + 4)) << 4);
   for (int g = 0;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&cx.bars->mfull[ms], (g / MST) & 1)) break;
@@ -581,14 +675,16 @@ __device__ void gather_role(const BParams& p, const Ctx& cx) {
     const int* keys = rec_key(cx, ms);
     const int st = g % KST;
     if (!WAIT(&cx.bars->kempty[st], ((g / KST) & 1) ^ 1)) break;
-    const uint32_t kbase = cx.sbase + OFF_K + st * KTILE + dst_off;
+    const uint32_t kbase = cx.sbase + OFF_K + st * KTILE;
     const __half* kb = p.k16 + (long long)batch * (p.S_k + 1) * kDP + ch * 8;
-    int key[kBM / 8];
-#pragma unroll
-    for (int i = 0; i < kBM / 8; ++i) key[i] = keys[rsub + 8 * i];  // padding entries hold the zero row S_k
-#pragma unroll
-    for (int i = 0; i < kBM / 8; ++i) cp_async16(kbase + i * 1024, kb + (long long)key[i] * kDP, 16);
+#pragma unroll 4
+    for (int i2 = 0; i2 < kBM / 8; ++i2) {  // rows rsub + 8*i2 and rsub + 4 + 8*i2
+      const int k0 = keys[rsub + 8 * i2], k1 = keys[rsub + 4 + 8 * i2];  // padding entries hold the zero row S_k
+      cp_async16(kbase + off0 + i2 * 1024, kb + (long long)k0 * kDP, 16);
+      cp_async16(kbase + off1 + i2 * 1024, kb + (long long)k1 * kDP, 16);
+    }
     cp_async_mbar_arrive_noinc(&cx.bars->kfull[st]);
+    if (x == 0) TRACE(EV_GATHER_ISSUED, g);
     if (flags & F_END) break;
   }
   cp_async_wait_all();  // copies in flight must land before the CTA can exit
@@ -600,7 +696,7 @@ __device__ void gather_role(const BParams& p, const Ctx& cx) {
 // (bf16 -> fp16 keeps the element size); rows past the block, heads past H
 // and columns past D are zero.
 __device__ void q_role(const BParams& p, const Ctx& cx) {
-  const int tid = threadIdx.x - W_Q0 * 32;  // 0..63
+  const int tid = threadIdx.x - W_Q0 * 32;  // 0..95
   Bars* B = cx.bars;
   const int4* bq = reinterpret_cast<const int4*>(cx.smem + OFF_BQ);
   float* w_s = reinterpret_cast<float*>(cx.smem + OFF_W);
@@ -611,31 +707,36 @@ __device__ void q_role(const BParams& p, const Ctx& cx) {
     if (row0 < 0) return;
     // the previous block's last MMAs that read Q (and its w) are complete
     if (!WAIT(&B->qempty, (i & 1) ^ 1)) return;
-    constexpr int NCH = NR * 16 / NQT;  // 16-byte chunks per thread: 64
-#pragma unroll 8
-    for (int m = 0; m < NCH; ++m) {
-      const int x = tid + NQT * m;
+    if (tid == 0) TRACE(EV_Q_START, (int)i);
+    constexpr int NCHUNK = NR * 16;  // 16-byte chunks of the block
+#pragma unroll 4
+    for (int x = tid; x < NCHUNK; x += NQT) {
       const int n = x >> 4, c = x & 15, r = n >> 6, h = n & 63;
       const bool ok = r < Rb && h < p.H && c * 8 < p.D;
       const uint16_t* src = ok ? p.q + ((long long)(row0 + r) * p.H + h) * p.D + c * 8 : p.q;
       cp_async16(cx.sbase + OFF_Q + (c >> 3) * QDH + n * 128 + (((c & 7) ^ (n & 7)) << 4), src, ok ? 16u : 0u);
     }
+    float wv[(NR + NQT - 1) / NQT];  // w of the block, loaded while the copies fly
+#pragma unroll
+    for (int k = 0; k < (NR + NQT - 1) / NQT; ++k) {
+      const int e = tid + NQT * k, r = e >> 6, h = e & 63;
+      wv[k] = (e < NR && r < Rb && h < p.H) ? __ldg(p.w + (long long)(row0 + r) * p.H + h) : 0.f;
+    }
     cp_async_wait_all();
-#pragma unroll 8
-    for (int m = 0; m < NCH; ++m) {
-      const int x = tid + NQT * m;
+#pragma unroll 4
+    for (int x = tid; x < NCHUNK; x += NQT) {
       const int n = x >> 4, c = x & 15;
       const uint32_t a = cx.sbase + OFF_Q + (c >> 3) * QDH + n * 128 + (((c & 7) ^ (n & 7)) << 4);
       uint32_t v0, v1, v2, v3;
       asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(a));
       st_shared_v4(a, bf16x2_to_half2(v0), bf16x2_to_half2(v1), bf16x2_to_half2(v2), bf16x2_to_half2(v3));
     }
-    for (int e = tid; e < NR; e += NQT) {
-      const int r = e >> 6, h = e & 63;
-      w_s[e] = (r < Rb && h < p.H) ? __ldg(p.w + (long long)(row0 + r) * p.H + h) : 0.f;
-    }
+#pragma unroll
+    for (int k = 0; k < (NR + NQT - 1) / NQT; ++k)
+      if (tid + NQT * k < NR) w_s[tid + NQT * k] = wv[k];
     fence_proxy_async_smem();
     mbar_arrive(&B->qfull);
+    if (tid == 0) TRACE(EV_Q_DONE, (int)i);
   }
 }
 
@@ -676,215 +777,255 @@ __device__ __forceinline__ void mma_dq(const Ctx& cx, int st, bool first) {
                    (first && k == 0) ? 0u : 1u);
 }
 
-// Issue order per tile g: Z of rows 0-1, Z of rows 2-3 (once the dz warps
-// have read the first), Z of rows 0-1 of tile g+1 when it belongs to the
-// same block, then dQ of g (its key stage is then free for the gather) and
-// dK of g (once the dK warps have drained the previous dK).  At a block's
-// last tile the next block's Z waits for its q rows, which may only be
-// written once that tile's dK MMA (the last reader of Q) is complete.
-__device__ void mma_role(const BParams& p, const Ctx& cx) {
+// Two issuing warps share the tensor pipe.  The Z issuer runs the Z MMAs of
+// every tile (rows 0-1, then rows 2-3, each as soon as the dz warps have
+// read the previous Z out of TMEM); the G issuer runs the dQ and dK MMAs of
+// a tile once its dz tile is complete (the dK MMA also once the dK warps have
+// drained the previous dK), so a slow dK drain holds back only the dK MMA,
+// not the recompute of the next tiles.
+// A block's next Z waits for its q rows, which the Q loader writes once the
+// last dK MMA of the previous block (the last reader of Q) is complete.
+__device__ void zmma_role(const BParams& p, const Ctx& cx) {
   Bars* B = cx.bars;
   long long g = 0, i = 0, zi = 0;
-  int flags;
-  if (!WAITW(&B->mfull[0], 0)) goto drain;
-  flags = cx.hdr[0].flags;
-  if (!WAITW(&B->qfull, 0) || !WAITW(&B->kfull[0], 0)) goto drain;
-  // the operands were written by cp.async and generic stores: order them
-  // before the tensor core's reads
-  fence_proxy_async_smem();
-  tc_fence_after();
-  mma_z(cx, 0, 0);
-  umma_commit_elect(&B->zfull);
-  zi = 1;
-  for (;;) {
-    const int st = (int)(g % KST);
-    if (!WAITW(&B->zempty, (zi & 1) ^ 1)) goto drain;
-    tc_fence_after();
-    mma_z(cx, st, 1);
-    umma_commit_elect(&B->zfull);
-    ++zi;
-    const bool more = !(flags & F_END);
-    const bool same = more && !(flags & F_LAST);
-    int nflags = 0;
-    if (same) {
-      const long long g1 = g + 1;
-      if (!WAITW(&B->mfull[g1 % MST], (g1 / MST) & 1)) goto drain;
-      nflags = cx.hdr[g1 % MST].flags;
-      if (!WAITW(&B->kfull[g1 % KST], (g1 / KST) & 1)) goto drain;
-      if (!WAITW(&B->zempty, (zi & 1) ^ 1)) goto drain;
+  for (;; ++g) {
+    const int ms = (int)(g % MST), st = (int)(g % KST);
+    if (!WAITW(&B->mfull[ms], (g / MST) & 1)) break;
+    const int flags = cx.hdr[ms].flags;
+    if ((flags & F_FIRST) && !WAITW(&B->qfull, i & 1)) break;
+    if (!WAITW(&B->kfull[st], (g / KST) & 1)) break;
+    bool ok = true;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      if (!WAITW(&B->zempty, (zi & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      // the operands were written by cp.async and generic stores: order them
+      // before the tensor core's reads
       fence_proxy_async_smem();
       tc_fence_after();
-      mma_z(cx, (int)(g1 % KST), 0);
+      mma_z(cx, st, half);
       umma_commit_elect(&B->zfull);
+      TRACE(half == 0 ? EV_MMA_ZA : EV_MMA_ZB, (int)g);
       ++zi;
     }
-    if (!WAITW(&B->dzfull, g & 1)) goto drain;
-    if ((flags & F_FIRST) && !WAITW(&B->dqempty, (i & 1) ^ 1)) goto drain;
+    if (!ok) break;
+    if (flags & F_LAST) ++i;
+    if (flags & F_END) break;
+  }
+  // every MMA issued so far completes before TMEM can be released
+  __syncwarp();
+  umma_commit_elect(&B->drain);
+  drain_wait(&B->drain, 0, p.status, p.wait_ns);
+  if ((threadIdx.x & 31) == 0) TRACE_CTA(2, (unsigned long long)g + 1);
+}
+
+__device__ void gmma_role(const BParams& p, const Ctx& cx) {
+  Bars* B = cx.bars;
+  long long i = 0;
+  for (long long g = 0;; ++g) {
+    const int ms = (int)(g % MST), st = (int)(g % KST);
+    if (!WAITW(&B->mfull[ms], (g / MST) & 1)) break;
+    const int flags = cx.hdr[ms].flags;
+    if (!WAITW(&B->dzfull, g & 1)) break;
+    if ((flags & F_FIRST) && !WAITW(&B->dqempty, (i & 1) ^ 1)) break;
     tc_fence_after();
     mma_dq(cx, st, (flags & F_FIRST) != 0);
+    TRACE(EV_MMA_DQ, (int)g);
+    // the key stage: its Z MMAs completed before the dz tile could be written
     umma_commit_elect(&B->kempty[st]);
     if (flags & F_LAST) umma_commit_elect(&B->dqfull);
-    if (!WAITW(&B->dkempty, (g & 1) ^ 1)) goto drain;
+    if (!WAITW(&B->dkempty, (g & 1) ^ 1)) break;
     tc_fence_after();
     mma_dk(cx);
+    TRACE(EV_MMA_DK, (int)g);
     umma_commit_elect(&B->dkfull);
     umma_commit_elect(&B->dzempty);
-    if (flags & F_LAST) umma_commit_elect(&B->qempty);
-    if (!more) break;
-    if (!same) {  // block boundary: the next block's first Z
+    if (flags & F_LAST) {
+      umma_commit_elect(&B->qempty);
       ++i;
-      const long long g1 = g + 1;
-      if (!WAITW(&B->mfull[g1 % MST], (g1 / MST) & 1)) goto drain;
-      nflags = cx.hdr[g1 % MST].flags;
-      if (!WAITW(&B->qfull, i & 1) || !WAITW(&B->kfull[g1 % KST], (g1 / KST) & 1)) goto drain;
-      if (!WAITW(&B->zempty, (zi & 1) ^ 1)) goto drain;
-      fence_proxy_async_smem();
-      tc_fence_after();
-      mma_z(cx, (int)(g1 % KST), 0);
-      umma_commit_elect(&B->zfull);
-      ++zi;
     }
-    ++g;
-    flags = nflags;
+    if (flags & F_END) break;
   }
-drain:
-  // every MMA issued so far completes before TMEM can be released
   __syncwarp();
   umma_commit_elect(&B->drain);
   drain_wait(&B->drain, 0, p.status, p.wait_ns);
 }
 
 // ------------------------------------------------------------- dz group ---
-// dz warp w (0..7): TMEM lane quarter q = w % 4, key half hr = w / 4.  For
+// dz warp w (0..15): TMEM lane quarter q = w % 4, key quarter kq = w / 4.  For
 // each Z buffer (rows 0-1, then rows 2-3) a thread owns the (r,h) row
-// 32q + lane of it and the 64 keys 64hr .. 64hr+63: it loads their z, sums
-// dI * relu(z) into its dW accumulator and writes dz (fp16) into its dz row.
-__device__ void dq_epilogue(const BParams& p, const Ctx& cx, const Hdr& hd, long long i) {
-  const int dzw = (threadIdx.x >> 5) - W_DZ0, q = dzw & 3, hr = dzw >> 2, lane = threadIdx.x & 31;
+// 32q + lane of it and the 32 keys 32kq .. 32kq+31 of every tile: it loads
+// their z (16 at a time), releases the buffer after the second load, and
+// writes dz = dI w 2^c [z > 0] (fp16) into its 64 bytes of the dz row.
+//
+// dW.  Summing dz z over the keys gives w 2^c dW, and sum_s dz z =
+// q . (sum_s dz k_s) = q . dQraw, the dQ accumulator before its 2^-c scale:
+// so dW = (q . dQraw) / (w 2^c), one dot product per (r,h) at block end.
+// Blocks where some |w| is zero or below 2^-12 of the block's largest (the
+// dz of those heads would lose precision or vanish) accumulate
+// dW = sum_s dI relu(z) per key instead (Hdr::direct).
+__device__ void dz_epilogue(const BParams& p, const Ctx& cx, int row0, int Rb, int c, int direct, int i,
+                            float acc0, float acc1, float wv0, float wv1) {
+  const int dzw = (threadIdx.x >> 5) - W_DZ0, q = (threadIdx.x >> 5) & 3, kq = dzw >> 2, lane = threadIdx.x & 31;
+  const int tdz = threadIdx.x - W_DZ0 * 32;
+  float* dwp = reinterpret_cast<float*>(cx.smem + OFF_DWP);
+  if (direct) {  // per-key sums of the four key quarters
+    dwp[kq * NR + 32 * q + lane] = acc0;
+    dwp[kq * NR + 128 + 32 * q + lane] = acc1;
+  }
   if (!WAIT(&cx.bars->dqfull, i & 1)) return;
   tc_fence_after();
   const int d = 32 * q + lane;  // TMEM lane = column of dQ
-  const float sc = pow2f(-hd.c);
+  const float sc = pow2f(-c);
+  const int r = kq;             // dQ columns 64kq .. 64kq+63: the heads of row kq
+  const bool rowok = r < Rb;
 #pragma unroll 1
   for (int cc = 0; cc < 4; ++cc) {
-    float v[32];
-    tmem_ld32(cx.tmem + ((uint32_t)(32 * q) << 16) + TM_DQ + 128 * hr + 32 * cc, v);
-    tmem_wait_ld_dep(v);
+    float v[16];
+    tmem_ld16(cx.tmem + ((uint32_t)(32 * q) << 16) + TM_DQ + 64 * kq + 16 * cc, v);
+    tmem_wait_ld_dep16(v);
     if (cc == 3) {
       tc_fence_before();
       mbar_arrive(&cx.bars->dqempty);
     }
-    const int r = 2 * hr + (cc >> 1), h0 = 32 * (cc & 1);
-    if (r < hd.Rb && d < p.D) {
-      const long long e0 = ((long long)(hd.row0 + r) * p.H + h0) * p.D + d;
+    const int h0 = 16 * cc;
+    const long long e0 = ((long long)(row0 + r) * p.H + h0) * p.D + d;
+    if (rowok && d < p.D) {
       if (p.dq16) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < 16; ++j)
           if (h0 + j < p.H) p.dq16[e0 + (long long)j * p.D] = to_bf16(v[j] * sc);
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < 16; ++j)
           if (h0 + j < p.H) p.dq[e0 + (long long)j * p.D] = v[j] * sc;
       }
+    }
+    if (!direct) {
+      // q[r,h,d] dQraw[r,h,d] for this lane's d, then summed over the warp's
+      // 32 columns d: four exchange steps and a last add leave head h0 + l
+      // summed in lanes l and l + 16
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const bool on = rowok && d < p.D && h0 + j < p.H;
+        const float qv = on ? __uint_as_float((uint32_t)__ldg(p.q + e0 + (long long)j * p.D) << 16) : 0.f;
+        v[j] *= qv;
+      }
+#pragma unroll
+      for (int step = 0; step < 4; ++step) {
+        const int o = 16 >> step, nn = 8 >> step;
+        const bool upper = (lane & (o >> 1)) != 0;
+#pragma unroll
+        for (int k = 0; k < nn; ++k) {
+          const float send = upper ? v[k] : v[k + nn];
+          const float keep = upper ? v[k + nn] : v[k];
+          v[k] = keep + __shfl_xor_sync(FULL, send, o >> 1);
+        }
+      }
+      v[0] += __shfl_xor_sync(FULL, v[0], 16);
+      if (lane < 16) dwp[q * NR + r * kHP + h0 + lane] = v[0];
+    }
+  }
+  mbar_arrive(&cx.bars->dwbar);
+  if (!WAIT(&cx.bars->dwbar, i & 1)) return;
+  if (tdz < NR) {
+    const int rr = tdz >> 6, h = tdz & 63;
+    if (rr < Rb && h < p.H) {
+      // the four partials in a fixed order
+      const float s4 = ((dwp[tdz] + dwp[NR + tdz]) + dwp[2 * NR + tdz]) + dwp[3 * NR + tdz];
+      // thread tdz holds w of (r,h) = tdz: buffer half tdz / 128
+      const float dwv = direct ? s4 : s4 / ((tdz < 128 ? wv0 : wv1) * pow2f(c));
+      const long long e = (long long)(row0 + rr) * p.H + h;
+      if (p.dw16)
+        p.dw16[e] = to_bf16(dwv);
+      else
+        p.dw[e] = dwv;
     }
   }
 }
 
 __device__ void dz_role(const BParams& p, const Ctx& cx) {
-  const int dzw = (threadIdx.x >> 5) - W_DZ0, q = dzw & 3, hr = dzw >> 2, lane = threadIdx.x & 31;
-  const int tdz = threadIdx.x - W_DZ0 * 32;  // 0..255
+  const int dzw = (threadIdx.x >> 5) - W_DZ0, lane = threadIdx.x & 31;
+  const int q = (threadIdx.x >> 5) & 3, kq = dzw >> 2;
+  const int tdz = threadIdx.x - W_DZ0 * 32;  // 0..511
   const int nrow = 32 * q + lane;            // (r,h) row within a Z buffer
   const float* w_s = reinterpret_cast<const float*>(cx.smem + OFF_W);
-  float* dwp = reinterpret_cast<float*>(cx.smem + OFF_DWP);
   Bars* B = cx.bars;
-  float acc0 = 0.f, acc1 = 0.f;  // dW partial sums of this thread's (r,h) row in each Z buffer
-  float wv0 = 0.f, wv1 = 0.f;
-  long long zi = 0, i = -1;
-  for (long long g = 0;; ++g) {
-    const int ms = (int)(g % MST);
+  const uint32_t ta = cx.tmem + ((uint32_t)(32 * q) << 16) + TM_Z + 32 * kq;
+  // dz rows nrow (rows 0-1) and 128 + nrow (rows 2-3), keys 32kq.. in key chunk kq/2
+  const uint32_t rowa = cx.sbase + OFF_DZ + (kq >> 1) * DZKC + nrow * 128;
+  const uint32_t rowb = rowa + 128 * 128;
+  float acc0 = 0.f, acc1 = 0.f, wv0 = 0.f, wv1 = 0.f;
+  int zi = 0, i = -1;  // tiles and blocks of one CTA stay far below 2^31
+  for (int g = 0;; ++g) {
+    const int ms = g % MST;
     if (!WAIT(&B->mfull[ms], (g / MST) & 1)) return;
-    const Hdr hd = cx.hdr[ms];
-    if (hd.flags & F_FIRST) {
+    const int flags = cx.hdr[ms].flags, c = cx.hdr[ms].c, direct = cx.hdr[ms].direct;
+    if (flags & F_FIRST) {
       ++i;
       if (!WAIT(&B->qfull, i & 1)) return;
       wv0 = w_s[nrow];
       wv1 = w_s[128 + nrow];
       acc0 = acc1 = 0.f;
     }
-    const float sc = pow2f(hd.c);
     const float* disb = rec_dis(cx, ms);
 #pragma unroll 1
     for (int x = 0; x < 2; ++x) {
       const int r = 2 * x + (q >> 1);
-      const float wsc = (x == 0 ? wv0 : wv1) * sc;
-      float ae = 0.f, ao = 0.f;  // this tile's sums over even / odd keys
-      const float* dr = disb + r * kBM + 64 * hr;
+      const float wsc = (x == 0 ? wv0 : wv1) * pow2f(c);
+      const uint64_t wsc2 = pack2(__float_as_uint(wsc), __float_as_uint(wsc));
+      const float* dr = disb + r * kBM + 32 * kq;
       if (!WAIT(&B->zfull, zi & 1)) return;
+      if (tdz == 0) TRACE(x == 0 ? EV_DZ_ZA : EV_DZ_ZB, g);
       tc_fence_after();
-      const uint32_t ta = cx.tmem + ((uint32_t)(32 * q) << 16) + TM_Z + 64 * hr;
-      uint32_t pk[32];
+      uint32_t pk[16];
+      float ad = 0.f;  // direct dW: this tile's sum
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float z[32];
-        tmem_ld32(ta + 32 * cc, z);
-        tmem_wait_ld_dep(z);
-        if (cc == 1) {
+      for (int hh = 0; hh < 2; ++hh) {  // keys 16hh .. 16hh+15 of the thread's 32
+        float z[16];
+        tmem_ld16(ta + 16 * hh, z);
+        tmem_wait_ld_dep16(z);
+        if (hh == 1) {
           tc_fence_before();
-          mbar_arrive(&B->zempty);
+          mbar_arrive(&B->zempty);  // the buffer is free for the next Z MMA
         }
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dr + 32 * cc + 4 * j4);
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float dzv[4];
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dr + 16 * hh + 4 * j4);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float zz = z[4 * j4 + e];
-            if (e & 1)
-              ao = fmaf(dd[e], fmaxf(zz, 0.f), ao);
-            else
-              ae = fmaf(dd[e], fmaxf(zz, 0.f), ae);
-            dzv[e] = zz > 0.f ? dd[e] * wsc : 0.f;
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const float z0 = z[4 * j4 + 2 * e2], z1 = z[4 * j4 + 2 * e2 + 1];
+            const float dA = e2 == 0 ? d4.x : d4.z, dB = e2 == 0 ? d4.y : d4.w;
+            const uint64_t t2 = mul_f32x2(pack2(__float_as_uint(dA), __float_as_uint(dB)), wsc2);  // dI w 2^c
+            const float v0 = z0 > 0.f ? __uint_as_float((uint32_t)t2) : 0.f;
+            const float v1 = z1 > 0.f ? __uint_as_float((uint32_t)(t2 >> 32)) : 0.f;
+            pk[8 * hh + 2 * j4 + e2] = pack_half2(v0, v1);
+            if (direct) ad = fmaf(dA, fmaxf(z0, 0.f), fmaf(dB, fmaxf(z1, 0.f), ad));
           }
-          pk[16 * cc + 2 * j4] = pack_half2(dzv[0], dzv[1]);
-          pk[16 * cc + 2 * j4 + 1] = pack_half2(dzv[2], dzv[3]);
         }
       }
       ++zi;
       if (x == 0)
-        acc0 += ae + ao;
+        acc0 += ad;
       else
-        acc1 += ae + ao;
+        acc1 += ad;
       // the dz tile is free once the previous tile's dQ and dK MMAs are complete
       if (x == 0 && !WAIT(&B->dzempty, (g & 1) ^ 1)) return;
-      const uint32_t n = 128 * x + nrow;
-      const uint32_t rowa = cx.sbase + OFF_DZ + hr * DZKC + n * 128;
+      const uint32_t row = x == 0 ? rowa : rowb;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        st_shared_v4(rowa + ((c8 ^ (n & 7)) << 4), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const uint32_t c8 = (kq & 1) * 4 + c4;
+        st_shared_v4(row + ((c8 ^ (nrow & 7)) << 4), pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+      }
     }
     fence_proxy_async_smem();
     mbar_arrive(&B->dzfull);
-    if (hd.flags & F_LAST) {
-      // dW[t,h]: the two key halves' partial sums, added in a fixed order
-      dwp[hr * NR + nrow] = acc0;
-      dwp[hr * NR + 128 + nrow] = acc1;
-      mbar_arrive(&B->dwbar);
-      if (!WAIT(&B->dwbar, i & 1)) return;
-      {
-        const int r = tdz >> 6, h = tdz & 63;
-        if (r < hd.Rb && h < p.H) {
-          const float v = dwp[tdz] + dwp[NR + tdz];
-          const long long e = (long long)(hd.row0 + r) * p.H + h;
-          if (p.dw16)
-            p.dw16[e] = to_bf16(v);
-          else
-            p.dw[e] = v;
-        }
-      }
-      dq_epilogue(p, cx, hd, i);
-    }
-    if (hd.flags & F_END) return;
+    if (tdz == 0) TRACE(EV_DZ_DONE, g);
+    if (flags & F_LAST)
+      dz_epilogue(p, cx, cx.hdr[ms].row0, cx.hdr[ms].Rb, c, direct, i, acc0, acc1, wv0, wv1);
+    if (flags & F_END) return;
   }
 }
 
@@ -903,24 +1044,23 @@ __device__ void dk_role(const BParams& p, const Ctx& cx) {
     float* base = p.u ? p.u : p.dk + (long long)batch * p.S_k * p.D;
     const int* ids = p.u ? rec_pos(cx, ms) : rec_key(cx, ms);
     if (!WAIT(&B->dkfull, g & 1)) return;
+    if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, (int)g);
     tc_fence_after();
     const float sc = pow2f(-c);
     const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK;
 #pragma unroll 1
     for (int ch = kg * 2; ch < kg * 2 + 2; ++ch) {
       if (ch * 32 >= count) break;  // uniform: the remaining entries are padding
-      float v[32];
-      tmem_ld32(ta + ch * 32, v);
-      tmem_wait_ld_dep(v);
       const int nrow = min(32, count - ch * 32);
       if (p.u)
-        dk_chunk<false>(base, ids + ch * 32, v, nrow, sc, p.D, qw * 32, stage);
+        dk_chunk_tmem<false>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage);
       else
-        dk_chunk<true>(base, ids + ch * 32, v, nrow, sc, p.D, qw * 32, stage);
+        dk_chunk_tmem<true>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage);
     }
     tc_fence_before();
     mbar_arrive(&B->dkempty);
     mbar_arrive(&B->mempty[ms]);
+    if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_DONE, (int)g);
     if (flags & F_END) return;
   }
 }
@@ -962,7 +1102,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
     mbar_init(&B->dqfull, 1);
     mbar_init(&B->dqempty, NDZT);
     mbar_init(&B->dwbar, NDZT);
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain, 2);  // one commit from each MMA issuer
     *cx.abort = 0;
     fence_barrier_init();
   }
@@ -977,13 +1117,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
   // everything above overlaps the previous kernel's tail (programmatic
   // dependent launch); the inputs it wrote are read only from here on
   griddep_wait();
+  if (threadIdx.x == 0) TRACE_CTA(0, clock64());
 
   if (warp < W_SCAN) {
     gather_role(p, cx);
   } else if (warp == W_SCAN) {
     scan_role(p, cx);
   } else if (warp == W_MMA) {
-    mma_role(p, cx);  // the whole warp runs the loop; one elected lane issues
+    zmma_role(p, cx);  // the whole warp runs the loop; one elected lane issues
+  } else if (warp == W_GMMA) {
+    gmma_role(p, cx);
   } else if (warp < W_DZ0) {
     q_role(p, cx);
   } else if (warp < W_DK0) {
@@ -996,6 +1139,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
   __syncthreads();
   tc_fence_after();
   if (warp == W_MMA) tmem_dealloc(cx.tmem, TM_COLS);
+  if (threadIdx.x == 0) TRACE_CTA(1, clock64());
 }
 
 // k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
@@ -1039,15 +1183,18 @@ __global__ void dk_to_bf16_kernel(const float* __restrict__ dk, uint16_t* __rest
 }
 
 // Key window of the union pass and the dedup capacity per row (both bounded
-// so that its shared memory stays under ~104 KB for any shape).
-void union_geometry(int S_k, int L, int& W, int& dcap) {
+// so that its shared memory stays under ~104 KB for any shape), and whether
+// the block's rows are staged in shared memory (rows of up to 2048 slots).
+void union_geometry(int S_k, int L, int& W, int& dcap, int& staged) {
   const long long skr = ((long long)S_k + 1023) / 1024 * 1024;
   W = (int)std::min<long long>(skr, L <= 4096 ? 32768 : 4096);
   dcap = std::min(L, W);
+  staged = L <= 2048 ? 1 : 0;
 }
 
-size_t union_smem_bytes(int W, int dcap) {
-  const size_t s = (size_t)10 * (W / 32) * 4 + (size_t)R * dcap * 4;
+size_t union_smem_bytes(int W, int dcap, int L, int staged) {
+  size_t s = (size_t)10 * (W / 32) * 4 + (size_t)R * dcap * 4;
+  if (staged) s += (size_t)2 * R * ((L + 3) & ~3) * 4;
   return std::max<size_t>(s, 2 * NBUCKET * 4);
 }
 
@@ -1147,8 +1294,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     u.tcap = lay.tcap;
     u.rstride = lay.rstride;
     u.ids_global = a.ids_global;
-    union_geometry(a.S_k, a.L, u.W, u.dcap);
-    const size_t sh = union_smem_bytes(u.W, u.dcap);
+    union_geometry(a.S_k, a.L, u.W, u.dcap, u.staged);
+    const size_t sh = union_smem_bytes(u.W, u.dcap, a.L, u.staged);
     // (its static arrays come on top of the dynamic bytes: always raise the limit)
     if (!set_smem_attr((const void*)union_kernel, sh, g_attr_union)) return cudaErrorInvalidValue;
     // it reads the ids before its predecessor completes and dI only after
@@ -1204,5 +1351,17 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   }
   return e;
 }
+
+#ifdef IBWD_TRACE
+extern "C" __attribute__((visibility("default"))) int ibwd_trace_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace));
+}
+extern "C" __attribute__((visibility("default"))) int ibwd_trace_poll_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_poll_count, bytes < sizeof(g_poll_count) ? bytes : sizeof(g_poll_count));
+}
+extern "C" __attribute__((visibility("default"))) int ibwd_trace_cta_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_trace_cta, bytes < sizeof(g_trace_cta) ? bytes : sizeof(g_trace_cta));
+}
+#endif
 
 }  // namespace ibwd

@@ -52,15 +52,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete: repeated try_wait,
 // which the hardware may suspend for a short, system-chosen time while the
 // phase is open (with a suspend-time hint the gemm kernel measured ~1 %
-// slower).  Gives up after `limit_ns` of wall
-// time or as soon as *abort is set by another warp; on a timeout it raises
+// slower).  Gives up after `limit_ns` of wall time or once *abort is set by
+// another warp (both checked every eight polls); on a timeout it raises
 // DEV_TIMEOUT in *status and sets *abort.  Returns false when it gave up.
+#ifdef IBWD_TRACE
+// failed polls per warp of the first CTA (pipeline analysis builds only)
+__device__ unsigned long long g_poll_count[64];
+#define IBWD_COUNT_POLL()                                                               \
+  do {                                                                                  \
+    if (blockIdx.x == 0 && (threadIdx.x & 31) == 0) atomicAdd(&g_poll_count[threadIdx.x >> 5], 1ull); \
+  } while (0)
+#else
+#define IBWD_COUNT_POLL() \
+  do {                    \
+  } while (0)
+#endif
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // the abort flag and the clock are checked once per eight polls
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      if (mbar_try_wait(bar, parity)) return true;
+      IBWD_COUNT_POLL();
+    }
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, DEV_TIMEOUT);
@@ -163,6 +181,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 bit, 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld_dep8(float (&v)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7])
+               :
+               : "memory");
 }
 
 // 32 lanes x 32 bit, 32 consecutive columns.
