@@ -39,14 +39,14 @@ def _L():
         lib = ctypes.CDLL(build())
         i, d, p = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         lib.oracle_set_threads.argtypes = [i]
-        lib.oracle_forward_sparse.argtypes = [p, p, p, p, i, i, i, i, i, i, p]
+        lib.oracle_forward_sparse.argtypes = [p, p, p, p, i, i, i, i, i, i, d, p]
         lib.oracle_score_grad_sparse.argtypes = [p, p, p, i, i, i, i, d, p]
         lib.oracle_score_grad_dense.argtypes = [p, p, i, i, d, p]
-        lib.oracle_gemm_sparse.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p, p]
-        lib.oracle_gemm_sparse_rows.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, i, p, p]
-        lib.oracle_forward_dense.argtypes = [p, p, p, i, i, i, i, p]
-        lib.oracle_gemm_dense.argtypes = [p, p, p, p, i, i, i, i, p, p, p]
-        lib.oracle_gemm_dense_rows.argtypes = [p, p, p, p, i, i, i, i, p, i, p, p]
+        lib.oracle_gemm_sparse.argtypes = [p, p, p, p, p, i, i, i, i, i, i, d, p, p, p]
+        lib.oracle_gemm_sparse_rows.argtypes = [p, p, p, p, p, i, i, i, i, i, i, d, p, i, p, p]
+        lib.oracle_forward_dense.argtypes = [p, p, p, i, i, i, i, d, p]
+        lib.oracle_gemm_dense.argtypes = [p, p, p, p, i, i, i, i, d, p, p, p]
+        lib.oracle_gemm_dense_rows.argtypes = [p, p, p, p, i, i, i, i, d, p, i, p, p]
         _lib = lib
     return _lib
 
@@ -66,14 +66,14 @@ def set_threads(n: int = 0) -> int:
     return int(_L().oracle_set_threads(n))
 
 
-def forward_sparse(q, k, w, idx, S_k: int) -> np.ndarray:
-    """I[b,t,j] = sum_h w relu(q[b,t,h].k[b,idx]) (0 on padding), float64."""
+def forward_sparse(q, k, w, idx, S_k: int, sm_scale: float = 1.0) -> np.ndarray:
+    """I[b,t,j] = sum_h w relu(sm_scale q[b,t,h].k[b,idx]) (0 on padding), float64."""
     B, S_q, H, D = q.shape
     topk = idx.shape[-1]
     q, qp = _c(q, np.uint16); k, kp = _c(k, np.uint16)
     w, wp = _c(w, np.float32); idx, ip = _c(idx, np.int32)
     out = np.empty((B, S_q, topk), np.float64)
-    _check(_L().oracle_forward_sparse(qp, kp, wp, ip, B, S_q, S_k, H, D, topk,
+    _check(_L().oracle_forward_sparse(qp, kp, wp, ip, B, S_q, S_k, H, D, topk, float(sm_scale),
                                       out.ctypes.data_as(ctypes.c_void_p)), "forward_sparse")
     return out
 
@@ -98,7 +98,7 @@ def score_grad_dense(index_score, attn_score, grad_scale: float = 1.0) -> np.nda
     return out
 
 
-def gemm_sparse(q, k, w, dI, idx, S_k: int):
+def gemm_sparse(q, k, w, dI, idx, S_k: int, sm_scale: float = 1.0):
     """(dq [B,S_q,H,D], dw [B,S_q,H], dk [B,S_k,D]) in float64."""
     B, S_q, H, D = q.shape
     topk = idx.shape[-1]
@@ -109,12 +109,12 @@ def gemm_sparse(q, k, w, dI, idx, S_k: int):
     dw = np.empty((B, S_q, H), np.float64)
     dk = np.empty((B, S_k, D), np.float64)
     vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    _check(_L().oracle_gemm_sparse(qp, kp, wp, dp, ip, B, S_q, S_k, H, D, topk,
+    _check(_L().oracle_gemm_sparse(qp, kp, wp, dp, ip, B, S_q, S_k, H, D, topk, float(sm_scale),
                                    vp(dq), vp(dw), vp(dk)), "gemm_sparse")
     return dq, dw, dk
 
 
-def gemm_sparse_rows(q, k, w, dI_rows, idx, S_k: int, rows):
+def gemm_sparse_rows(q, k, w, dI_rows, idx, S_k: int, rows, sm_scale: float = 1.0):
     """dQ/dW of the listed global rows (b*S_q + t); dI_rows is [len(rows), topk]."""
     B, S_q, H, D = q.shape
     topk = idx.shape[-1]
@@ -126,21 +126,21 @@ def gemm_sparse_rows(q, k, w, dI_rows, idx, S_k: int, rows):
     dq = np.empty((n, H, D), np.float64)
     dw = np.empty((n, H), np.float64)
     vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    _check(_L().oracle_gemm_sparse_rows(qp, kp, wp, dp, ip, B, S_q, S_k, H, D, topk,
+    _check(_L().oracle_gemm_sparse_rows(qp, kp, wp, dp, ip, B, S_q, S_k, H, D, topk, float(sm_scale),
                                         vp(rows), n, vp(dq), vp(dw)), "gemm_sparse_rows")
     return dq, dw
 
 
-def forward_dense(q, k, w) -> np.ndarray:
+def forward_dense(q, k, w, sm_scale: float = 1.0) -> np.ndarray:
     B, S, H, D = q.shape
     q, qp = _c(q, np.uint16); k, kp = _c(k, np.uint16); w, wp = _c(w, np.float32)
     out = np.empty((B, S, S), np.float64)
-    _check(_L().oracle_forward_dense(qp, kp, wp, B, S, H, D,
+    _check(_L().oracle_forward_dense(qp, kp, wp, B, S, H, D, float(sm_scale),
                                      out.ctypes.data_as(ctypes.c_void_p)), "forward_dense")
     return out
 
 
-def gemm_dense(q, k, w, dI):
+def gemm_dense(q, k, w, dI, sm_scale: float = 1.0):
     B, S, H, D = q.shape
     q, qp = _c(q, np.uint16); k, kp = _c(k, np.uint16); w, wp = _c(w, np.float32)
     dI, dp = _c(dI, np.float64)
@@ -148,11 +148,12 @@ def gemm_dense(q, k, w, dI):
     dw = np.empty((B, S, H), np.float64)
     dk = np.empty((B, S, D), np.float64)
     vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    _check(_L().oracle_gemm_dense(qp, kp, wp, dp, B, S, H, D, vp(dq), vp(dw), vp(dk)), "gemm_dense")
+    _check(_L().oracle_gemm_dense(qp, kp, wp, dp, B, S, H, D, float(sm_scale), vp(dq), vp(dw), vp(dk)),
+           "gemm_dense")
     return dq, dw, dk
 
 
-def gemm_dense_rows(q, k, w, dI_rows, rows):
+def gemm_dense_rows(q, k, w, dI_rows, rows, sm_scale: float = 1.0):
     B, S, H, D = q.shape
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     q, qp = _c(q, np.uint16); k, kp = _c(k, np.uint16); w, wp = _c(w, np.float32)
@@ -161,6 +162,6 @@ def gemm_dense_rows(q, k, w, dI_rows, rows):
     dq = np.empty((n, H, D), np.float64)
     dw = np.empty((n, H), np.float64)
     vp = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    _check(_L().oracle_gemm_dense_rows(qp, kp, wp, dp, B, S, H, D, vp(rows), n, vp(dq), vp(dw)),
+    _check(_L().oracle_gemm_dense_rows(qp, kp, wp, dp, B, S, H, D, float(sm_scale), vp(rows), n, vp(dq), vp(dw)),
            "gemm_dense_rows")
     return dq, dw

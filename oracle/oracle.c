@@ -18,18 +18,26 @@
  * positive out-of-range id) is padding and contributes nothing ([P2] harness,
  * padding-equivalence check).  Ids are local to their batch.
  *
- *   forward:    z[t,j,h] = q[t,h,:] . k[s,:];  I[t,j] = sum_h w[t,h] relu(z)
+ *   forward:    z[t,j,h] = sm_scale * (q[t,h,:] . k[s,:]);
+ *               I[t,j] = sum_h w[t,h] relu(z)
  *   score-grad: p = softmax over valid j of I[t,:];  ahat = a / sum_valid a;
  *               dI[t,j] = grad_scale * (p_j - ahat_j) / S_q   (0 if invalid)
  *               -- the gradient of (grad_scale/S_q) sum_t KL(ahat_t || p_t);
  *               the pages name the inputs and the in-place output but print no
  *               formula, so this plain reading is taken.
  *   gemm stage: dW[t,h]  = sum_j dI relu(z)
- *               dz       = dI w[t,h] [z > 0]
+ *               dz       = dI w[t,h] [z > 0] sm_scale
  *               dQ[t,h]  = sum_j dz k[s]
  *               dK[s]   += sum_{t,h} dz q[t,h]
  *               ([P2] ref_grads, with sm_scale = 1; the ReLU derivative at
  *               z = 0 is taken as 0, as the strict comparison there states.)
+ *   sm_scale:   the logit scale of the [P2] harness, which runs with
+ *               sm_scale = 1.0 and calls the kernel's scaling a runtime fold
+ *               that is then a no-op.  Read as a factor inside the ReLU, the
+ *               plain reading; dz is the chain rule through it.  For
+ *               sm_scale > 0, relu(s x) = s relu(x), so I, dW, dQ and dK all
+ *               scale by s; sm_scale = 1 gives the unscaled definitions
+ *               exactly.
  *
  * Dense variant: every key s <= t is selected (S_q == S_k); scores are
  * indexed [t, s] and entries with s > t are zero.
@@ -80,7 +88,7 @@ int oracle_set_threads(int n) {
  * s = einsum(q, k_sel) the same way). */
 int oracle_forward_sparse(const uint16_t *q16, const uint16_t *k16, const float *w,
                           const int32_t *idx, int B, int S_q, int S_k, int H, int D,
-                          int topk, double *I) {
+                          int topk, double sm_scale, double *I) {
   double *q = widen_bf16(q16, (size_t)B * S_q * H * D);
   double *k = widen_bf16(k16, (size_t)B * S_k * D);
   if (!q || !k) { free(q); free(k); return 1; }
@@ -95,7 +103,7 @@ int oracle_forward_sparse(const uint16_t *q16, const uint16_t *k16, const float 
       if (slot_valid(s, S_k)) {
         const double *kr = k + (b * S_k + s) * D;
         for (int h = 0; h < H; h++) {
-          double z = dot(qr + (int64_t)h * D, kr, D);
+          double z = sm_scale * dot(qr + (int64_t)h * D, kr, D);
           if (z > 0.0) acc += (double)w[r * H + h] * z;
         }
       }
@@ -195,8 +203,8 @@ int oracle_score_grad_dense(const float *index_score, const float *attn_score, i
  * keys[j] < 0 marks padding.  Accumulates dQ/dW for the row and, when dk is
  * non-NULL, the row's dK contribution into dk (a per-thread partial). */
 static void gemm_row(const double *qr, const double *kb, const float *wr, const double *dIr,
-                     const int32_t *keys, int n, int H, int D, double *dqr, double *dwr,
-                     double *dk) {
+                     const int32_t *keys, int n, int H, int D, double sm_scale, double *dqr,
+                     double *dwr, double *dk) {
   for (int h = 0; h < H; h++) {
     dwr[h] = 0.0;
     for (int d = 0; d < D; d++) dqr[(int64_t)h * D + d] = 0.0;
@@ -208,10 +216,10 @@ static void gemm_row(const double *qr, const double *kb, const float *wr, const 
     double g = dIr[j];
     for (int h = 0; h < H; h++) {
       const double *qh = qr + (int64_t)h * D;
-      double z = dot(qh, kr, D);
+      double z = sm_scale * dot(qh, kr, D);
       if (!(z > 0.0)) continue;            /* relu(z) = 0 and [z > 0] = 0 */
       dwr[h] += g * z;                     /* dW += dI * relu(z) */
-      double dz = g * (double)wr[h];       /* dz = dI w [z > 0] */
+      double dz = g * (double)wr[h] * sm_scale;  /* dz = dI w [z > 0] sm_scale */
       double *dqh = dqr + (int64_t)h * D;
       for (int d = 0; d < D; d++) dqh[d] += dz * kr[d];  /* dQ[t,h] += dz k[s] */
       if (dk) {
@@ -233,7 +241,8 @@ static void sum_partials(double *dk, double *part, int nth, size_t n) {
  * [P2] ref_grads is the fp64 definition followed here, written as loops. */
 int oracle_gemm_sparse(const uint16_t *q16, const uint16_t *k16, const float *w,
                        const double *dI, const int32_t *idx, int B, int S_q, int S_k,
-                       int H, int D, int topk, double *dq, double *dw, double *dk) {
+                       int H, int D, int topk, double sm_scale, double *dq, double *dw,
+                       double *dk) {
   double *q = widen_bf16(q16, (size_t)B * S_q * H * D);
   double *k = widen_bf16(k16, (size_t)B * S_k * D);
   int nth = omp_get_max_threads();
@@ -258,7 +267,7 @@ int oracle_gemm_sparse(const uint16_t *q16, const uint16_t *k16, const float *w,
           keys[j] = slot_valid(s, S_k) ? s : -1;
         }
         gemm_row(q + r * H * D, k + b * S_k * D, w + r * H, dI + r * topk, keys, topk, H, D,
-                 dq + r * H * D, dw + r * H, part + (size_t)th * dkn + (size_t)b * S_k * D);
+                 sm_scale, dq + r * H * D, dw + r * H, part + (size_t)th * dkn + (size_t)b * S_k * D);
       }
       free(keys);
     }
@@ -274,8 +283,8 @@ int oracle_gemm_sparse(const uint16_t *q16, const uint16_t *k16, const float *w,
  * check sampled rows of a full-size problem one by one. */
 int oracle_gemm_sparse_rows(const uint16_t *q16, const uint16_t *k16, const float *w,
                             const double *dI_rows, const int32_t *idx, int B, int S_q, int S_k,
-                            int H, int D, int topk, const int64_t *rows, int nrows, double *dq,
-                            double *dw) {
+                            int H, int D, int topk, double sm_scale, const int64_t *rows,
+                            int nrows, double *dq, double *dw) {
   (void)B;
   int bad = 0;
 #pragma omp parallel
@@ -303,7 +312,7 @@ int oracle_gemm_sparse_rows(const uint16_t *q16, const uint16_t *k16, const floa
             keys[j] = -1;
           }
         }
-        gemm_row(qr, kr, w + r * H, dI_rows + (int64_t)i * topk, keys, topk, H, D,
+        gemm_row(qr, kr, w + r * H, dI_rows + (int64_t)i * topk, keys, topk, H, D, sm_scale,
                  dq + (int64_t)i * H * D, dw + (int64_t)i * H, NULL);
       }
     }
@@ -316,7 +325,7 @@ int oracle_gemm_sparse_rows(const uint16_t *q16, const uint16_t *k16, const floa
 
 /* Dense forward: I[b,t,s] for s <= t, 0 above the diagonal. */
 int oracle_forward_dense(const uint16_t *q16, const uint16_t *k16, const float *w, int B, int S,
-                         int H, int D, double *I) {
+                         int H, int D, double sm_scale, double *I) {
   double *q = widen_bf16(q16, (size_t)B * S * H * D);
   double *k = widen_bf16(k16, (size_t)B * S * D);
   if (!q || !k) { free(q); free(k); return 1; }
@@ -329,7 +338,7 @@ int oracle_forward_dense(const uint16_t *q16, const uint16_t *k16, const float *
       if (s <= t) {
         const double *kr = k + (b * S + s) * D;
         for (int h = 0; h < H; h++) {
-          double z = dot(q + r * H * D + (int64_t)h * D, kr, D);
+          double z = sm_scale * dot(q + r * H * D + (int64_t)h * D, kr, D);
           if (z > 0.0) acc += (double)w[r * H + h] * z;
         }
       }
@@ -343,7 +352,8 @@ int oracle_forward_dense(const uint16_t *q16, const uint16_t *k16, const float *
 
 /* Dense gemm stage: every causal key s <= t is selected; dI is [B,S,S]. */
 int oracle_gemm_dense(const uint16_t *q16, const uint16_t *k16, const float *w, const double *dI,
-                      int B, int S, int H, int D, double *dq, double *dw, double *dk) {
+                      int B, int S, int H, int D, double sm_scale, double *dq, double *dw,
+                      double *dk) {
   double *q = widen_bf16(q16, (size_t)B * S * H * D);
   double *k = widen_bf16(k16, (size_t)B * S * D);
   int nth = omp_get_max_threads();
@@ -364,7 +374,7 @@ int oracle_gemm_dense(const uint16_t *q16, const uint16_t *k16, const float *w, 
       for (int64_t r = 0; r < rows; r++) {
         int64_t b = r / S, t = r % S;
         for (int s = 0; s < S; s++) keys[s] = (s <= t) ? s : -1;
-        gemm_row(q + r * H * D, k + b * S * D, w + r * H, dI + r * S, keys, S, H, D,
+        gemm_row(q + r * H * D, k + b * S * D, w + r * H, dI + r * S, keys, S, H, D, sm_scale,
                  dq + r * H * D, dw + r * H, part + (size_t)th * dkn + (size_t)b * S * D);
       }
       free(keys);
@@ -379,8 +389,8 @@ int oracle_gemm_dense(const uint16_t *q16, const uint16_t *k16, const float *w, 
 
 /* Dense dQ/dW for a list of global rows only. */
 int oracle_gemm_dense_rows(const uint16_t *q16, const uint16_t *k16, const float *w,
-                           const double *dI_rows, int B, int S, int H, int D, const int64_t *rows,
-                           int nrows, double *dq, double *dw) {
+                           const double *dI_rows, int B, int S, int H, int D, double sm_scale,
+                           const int64_t *rows, int nrows, double *dq, double *dw) {
   (void)B;
   int bad = 0;
 #pragma omp parallel
@@ -399,7 +409,7 @@ int oracle_gemm_dense_rows(const uint16_t *q16, const uint16_t *k16, const float
         for (int x = 0; x < H * D; x++) qr[x] = bf16_to_double(q16[r * H * D + x]);
         for (int64_t x = 0; x < (int64_t)S * D; x++) kb[x] = bf16_to_double(k16[b * S * D + x]);
         for (int s = 0; s < S; s++) keys[s] = (s <= t) ? s : -1;
-        gemm_row(qr, kb, w + r * H, dI_rows + (int64_t)i * S, keys, S, H, D,
+        gemm_row(qr, kb, w + r * H, dI_rows + (int64_t)i * S, keys, S, H, D, sm_scale,
                  dq + (int64_t)i * H * D, dw + (int64_t)i * H, NULL);
       }
     }

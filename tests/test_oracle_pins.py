@@ -6,8 +6,9 @@ transposed operand, a wrong index or padding rule) fails at least one:
 
 * hand-derived closed-form case (tests/golden/hand_case.json);
 * central finite differences of the KL loss (score-grad) and of the linear
-  functional L = sum dI * I(q, k, w) (gemm stage), with loss functions written
-  here, never calling the oracle's gradient code;
+  functional L = sum dI * I(q, k, w) (gemm stage, at logit scales 1, 0.37 and
+  0.0884), with loss functions written here, never calling the oracle's
+  gradient code;
 * homogeneity: <dW,w> = <dQ,q> = <dK,k> = sum dI*I (I is positively
   1-homogeneous in each of q, k, w);
 * row invariants of dI (sums to zero; padding is exactly zero; one valid slot
@@ -165,7 +166,7 @@ def test_score_grad_padding_ignores_garbage_and_oob():
 
 # ------------------------------------------------------------ gemm stage ---
 
-def np_forward(q, k, w, idx, S_k):
+def np_forward(q, k, w, idx, S_k, sm_scale=1.0):
     """The forward written with numpy for the finite-difference loss."""
     B, S_q, H, D = q.shape
     I = np.zeros(idx.shape)
@@ -174,22 +175,23 @@ def np_forward(q, k, w, idx, S_k):
             for j in range(idx.shape[-1]):
                 s = idx[b, t, j]
                 if 0 <= s < S_k:
-                    z = q[b, t] @ k[b, s]
+                    z = sm_scale * (q[b, t] @ k[b, s])
                     I[b, t, j] = float(np.sum(w[b, t] * np.maximum(z, 0.0)))
     return I
 
 
-def test_forward_and_gemm_match_finite_differences():
+@pytest.mark.parametrize("sm_scale", [1.0, 0.37, 0.0884])
+def test_forward_and_gemm_match_finite_differences(sm_scale):
     q16, k16, w, idx, attn = small_case(seed=13, S_q=10, S_k=9, H=3, D=5, topk=6)
     S_k = 9
     dI = synth.normal_f32(4, 9, idx.shape).astype(np.float64)
     dI[(idx < 0)] = 0.0
     q, k, w64 = bf16(q16), bf16(k16), w.astype(np.float64)
     # the oracle's forward agrees with the numpy forward
-    np.testing.assert_allclose(oracle.forward_sparse(q16, k16, w, idx, S_k), np_forward(q, k, w64, idx, S_k),
-                               rtol=1e-13, atol=1e-13)
-    dq, dw, dk = oracle.gemm_sparse(q16, k16, w, dI, idx, S_k)
-    L = lambda q_, k_, w_: float(np.sum(dI * np_forward(q_, k_, w_, idx, S_k)))
+    np.testing.assert_allclose(oracle.forward_sparse(q16, k16, w, idx, S_k, sm_scale),
+                               np_forward(q, k, w64, idx, S_k, sm_scale), rtol=1e-13, atol=1e-13)
+    dq, dw, dk = oracle.gemm_sparse(q16, k16, w, dI, idx, S_k, sm_scale)
+    L = lambda q_, k_, w_: float(np.sum(dI * np_forward(q_, k_, w_, idx, S_k, sm_scale)))
     h = 1e-6
     rng = np.random.default_rng(1)
 
@@ -278,26 +280,41 @@ def test_rows_variant_matches_full():
     np.testing.assert_array_equal(dwr, dw.reshape(-1, 3)[rows])
 
 
-def test_dense_equals_sparse_with_every_causal_key():
+@pytest.mark.parametrize("sm_scale", [1.0, 0.5])
+def test_dense_equals_sparse_with_every_causal_key(sm_scale):
     S, H, D = 24, 3, 8
+    sc = dict(sm_scale=sm_scale)
     q16 = synth.normal_bf16(1, 1, (1, S, H, D)); k16 = synth.normal_bf16(1, 2, (1, S, D))
     w = synth.normal_f32(1, 3, (1, S, H))
     idx = np.where(np.arange(S)[None, :] <= np.arange(S)[:, None], np.arange(S)[None, :], -1)
     idx = idx.astype(np.int32)[None]
-    I_s = oracle.forward_sparse(q16, k16, w, idx, S)
-    I_d = oracle.forward_dense(q16, k16, w)
+    I_s = oracle.forward_sparse(q16, k16, w, idx, S, **sc)
+    I_d = oracle.forward_dense(q16, k16, w, **sc)
     np.testing.assert_array_equal(I_s, I_d)
     a = synth.target_dense(1, 5, 1, S)
     dI_s = oracle.score_grad_sparse(I_s.astype(np.float32), a, idx, S)
     dI_d = oracle.score_grad_dense(I_d.astype(np.float32), a)
     np.testing.assert_array_equal(dI_s, dI_d)
-    for x, y in zip(oracle.gemm_sparse(q16, k16, w, dI_s, idx, S), oracle.gemm_dense(q16, k16, w, dI_d)):
+    for x, y in zip(oracle.gemm_sparse(q16, k16, w, dI_s, idx, S, **sc), oracle.gemm_dense(q16, k16, w, dI_d, **sc)):
         np.testing.assert_array_equal(x, y)
     rows = np.array([0, 7, 23])
-    dqr, dwr = oracle.gemm_dense_rows(q16, k16, w, dI_d.reshape(S, S)[rows], rows)
-    dq, dw, _ = oracle.gemm_dense(q16, k16, w, dI_d)
+    dqr, dwr = oracle.gemm_dense_rows(q16, k16, w, dI_d.reshape(S, S)[rows], rows, **sc)
+    dq, dw, _ = oracle.gemm_dense(q16, k16, w, dI_d, **sc)
     np.testing.assert_array_equal(dqr, dq[0, rows])
     np.testing.assert_array_equal(dwr, dw[0, rows])
+
+
+def test_logit_scale_is_a_power_of_two_factor_on_every_output():
+    # relu(s x) = s relu(x) for s > 0: with s = 2^-3 every output of the
+    # scaled definitions is the unscaled one times s, exactly
+    q16, k16, w, idx, attn = small_case(seed=17, S_q=30, S_k=25, H=3, D=8, topk=9)
+    S_k = 25
+    s = 0.125
+    np.testing.assert_array_equal(oracle.forward_sparse(q16, k16, w, idx, S_k, s),
+                                  s * oracle.forward_sparse(q16, k16, w, idx, S_k))
+    dI = synth.normal_f32(3, 9, idx.shape).astype(np.float64)
+    for x, y in zip(oracle.gemm_sparse(q16, k16, w, dI, idx, S_k, s), oracle.gemm_sparse(q16, k16, w, dI, idx, S_k)):
+        np.testing.assert_allclose(x, s * y, rtol=1e-14, atol=1e-300)
 
 
 def test_duplicate_ids_count_as_separate_slots():
