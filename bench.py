@@ -11,6 +11,10 @@ whole step (6*S_q*topk*H*D per step, all ranks), inputs resident in HBM;
 results copied inside the timed region; `roofline` covers the gemm-stage
 kernel; `cpu_baseline` times the fp64 oracle on a bounded row sample.
 `--impl reference` times the oracle itself as the reference arm.
+`other_configs` adds, measured in the same run, the gemm-stage and score-grad
+kernel times of the other contract configurations (both dK modes of the
+anchor and the window workload, the S_q = 4096 top-k 512 shape, the dense
+variant).
 With N > 1 every rank runs an independent replica (weak scaling); the path
 has no exchange step between replicas.
 """
@@ -80,6 +84,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other contract configurations")
+    ap.add_argument("--extra-steps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -244,6 +250,79 @@ class Clocks:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# The other contract configurations, measured in the same run (gemm-stage
+# and score-grad kernel times only; no end-to-end or CPU legs).
+EXTRA_CONFIGS = (("anchor", "det"), ("sq4096_topk512", "atomic"), ("window_topk2048", "atomic"),
+                 ("window_topk2048", "det"), ("dense_s4096", "atomic"), ("dense_s4096", "det"))
+
+
+def measure_config(ibwd, torch, dev, name, mode_name, steps, warmup, pk):
+    """Score-grad and gemm-stage kernel times of one workload and dK mode,
+    timed with CUDA events on the launching stream over `steps` steps (each
+    with a fresh attn_score copy; inputs larger than L2)."""
+    wl = synth.WORKLOADS[name]
+    mode = ibwd.IBWD_DK_DETERMINISTIC if mode_name == "det" else ibwd.IBWD_DK_ATOMIC
+    x = synth.make_inputs(wl)
+    q = torch.from_numpy(x["q"].view(np.int16)).to(dev).view(torch.bfloat16)
+    k = torch.from_numpy(x["k"].view(np.int16)).to(dev).view(torch.bfloat16)
+    w = torch.from_numpy(x["w"]).to(dev)
+    idx = None if wl.dense else torch.from_numpy(x["idx"]).to(dev)
+    attn0 = torch.from_numpy(x["attn"]).to(dev)
+    I = ibwd.indexer_fwd_dense(q, k, w) if wl.dense else ibwd.indexer_fwd(q, k, w, idx)
+    B, S_q, H, D = q.shape
+    dq = torch.empty((B, S_q, H, D), dtype=torch.float32, device=dev)
+    dw = torch.empty((B, S_q, H), dtype=torch.float32, device=dev)
+    dk = torch.empty((B, wl.S_k, D), dtype=torch.float32, device=dev)
+    wsb = torch.empty(ibwd.indexer_bwd_dense_gemm_workspace_size(B, S_q, H, D, mode) if wl.dense else
+                      ibwd.indexer_bwd_gemm_workspace_size(B, S_q, wl.S_k, H, D, wl.topk, mode),
+                      dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    attn = [attn0.clone() for _ in range(2)]
+    sg, gm = [], []
+    for i in range(warmup + steps):
+        a = attn[i & 1]
+        a.copy_(attn0)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        zero = dk if mode == ibwd.IBWD_DK_ATOMIC else None
+        ev[0].record(stream)
+        if wl.dense:
+            ibwd.indexer_bwd_dense_score_grad(I, a, 1.0, zero, stream)
+        else:
+            ibwd.indexer_bwd_score_grad(I, a, idx, wl.S_k, 1.0, zero, stream)
+        ev[1].record(stream)
+        if wl.dense:
+            ibwd.indexer_bwd_dense_gemm(q, k, w, a, dq, dw, dk, mode, wsb, stream)
+        else:
+            ibwd.indexer_bwd_gemm(q, k, w, a, idx, dq, dw, dk, mode, wsb, stream)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            sg.append(ev[0].elapsed_time(ev[1]))
+            gm.append(ev[1].elapsed_time(ev[2]))
+    st = ibwd.indexer_bwd_last_device_status(stream)
+    if st != ibwd.IBWD_OK:
+        raise SystemExit(f"device status after {name}/{mode_name}: {ibwd.status_string(st)}")
+    flops = wl.flops()
+    valid = 1.0 if wl.dense else float((x["idx"] >= 0).mean())
+    zero_bytes = 4.0 * wl.B * wl.S_k * wl.D if mode == ibwd.IBWD_DK_ATOMIC else 0.0
+    sg_bytes = (8.0 * wl.B * wl.S_q * (wl.S_q + 1) / 2 + 4.0 * wl.B * wl.S_q * wl.S_q if wl.dense else
+                16.0 * wl.B * wl.S_q * wl.topk) + zero_bytes
+    gmed = float(np.median(gm))
+    sgmed = float(np.median(sg))
+    return {
+        "workload": f"{wl.name}: B={wl.B} H={wl.H} D={wl.D} S_q={wl.S_q} S_k={wl.S_k} "
+                    + ("every causal key (dense)" if wl.dense else f"topk={wl.topk}, {wl.ids} top-k ids"),
+        "dk_mode": mode_name, "steps": steps,
+        "gemm_stage_us": {"median": 1e3 * gmed, "min": 1e3 * float(np.min(gm)), "p90": 1e3 * float(np.percentile(gm, 90))},
+        "tflops": flops / (gmed * 1e-3) / 1e12,
+        "frac_nominal": flops / (gmed * 1e-3) / 1e12 / pk["bf16_tflops"],
+        "frac_valid_slots": valid * flops / (gmed * 1e-3) / 1e12 / pk["bf16_tflops"],
+        "valid_slot_fraction": round(valid, 4),
+        "score_grad_us": 1e3 * sgmed,
+        "score_grad_gbs": sg_bytes / (sgmed * 1e-3) / 1e9,
+    }
 
 
 def run_ours(args, wl):
@@ -456,6 +535,16 @@ def run_ours(args, wl):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and not wl.dense:
         cpu = cpu_baseline(wl, x, I.cpu().numpy(), args.cpu_seconds)
 
+    # the other contract configurations (one GPU runs; rank 0 of a replica job)
+    extra = None
+    if rank == 0 and not args.no_extra:
+        extra = []
+        for name, mname in EXTRA_CONFIGS:
+            if name == wl.name and mname == args.mode:
+                continue
+            extra.append(measure_config(ibwd, torch, dev, name, mname, args.extra_steps, 3, peaks()))
+            torch.cuda.empty_cache()
+
     if rank != 0:
         return
     traffic = profiled_traffic(wl.name, args.mode)
@@ -478,7 +567,8 @@ def run_ours(args, wl):
                              for name, v in (("score_grad", sg_ms), ("gemm_stage", gm_ms))},
         "score_grad_gbs": sg_bytes / (sg_avg * 1e-3) / 1e9,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / pk["bf16_tflops"], "traffic": traffic.get("gemm_stage"),
+                     "frac": achieved / pk["bf16_tflops"], "frac_valid_slots": achieved * valid / pk["bf16_tflops"],
+                     "traffic": traffic.get("gemm_stage"),
                      "note": f"gemm-stage call (fp16 copy of k + main kernel), nominal 6*S_q*topk*H*D FLOP; "
                              f"peak = {pk['src']} dense bf16 burst (fp16 dense rate is the same)"},
         "roofline_score_grad": {"bound": "hbm", "achieved": sg_bytes / (sg_avg * 1e-3) / 1e9,
@@ -493,6 +583,7 @@ def run_ours(args, wl):
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "other_configs": extra,
     }
     print(json.dumps(line), flush=True)
 

@@ -29,7 +29,10 @@
  *    dK mode also needs S_k <= 40960 (its key sort keeps per-key state in
  *    shared memory).
  *  - q and k entries must lie in fp16 range (|x| <= 65504): the gemm stage
- *    feeds fp16 tensor-core operands converted exactly from bf16.
+ *    feeds fp16 tensor-core operands converted from bf16, exactly for
+ *    2^-14 <= |x| <= 65504 and to fp16 subnormals (absolute error at most
+ *    2^-25) below that.  A larger or non-finite entry is reported as
+ *    IBWD_ERR_RANGE by indexer_bwd_last_device_status.
  *  - The library allocates no memory on the compute path.  The deterministic
  *    mode uses the caller's workspace.  One 4-byte device status word per
  *    device is allocated on first use and kept until process exit.
@@ -57,7 +60,7 @@ typedef enum {
   IBWD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
   IBWD_ERR_CUDA = 4,        /* a CUDA runtime call failed */
   IBWD_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (device status) */
-  IBWD_ERR_BAD_INDEX = 6    /* a device-side bounds check failed (device status) */
+  IBWD_ERR_RANGE = 6        /* a q or k entry outside the fp16 operand range (device status) */
 } ibwd_status;
 
 typedef enum {
@@ -222,6 +225,16 @@ IBWD_API int indexer_bwd_dense(const uint16_t* q, const uint16_t* k, const float
  *   dk_bf16     optional device bf16 [B,S_k,D], 16-byte aligned: written with
  *               the final fp32 dk rounded to nearest even (dk itself is still
  *               produced in fp32)
+ *   sm_scale    logit scale s of the forward the gradients belong to,
+ *               I[t,j] = sum_h w[t,h] relu(s q[t,h,:] . k[s_j,:]) (#730
+ *               benchmark harness: sm_scale, 1.0 there, folded into the
+ *               kernels at run time).  0 means 1.  For s > 0,
+ *               relu(s x) = s relu(x), so dq, dw and dk are s times the
+ *               unscaled results for the same dI; the factor is folded into
+ *               the outputs' power-of-two scale (one fp32 multiply each, no
+ *               extra rounding when s = 1).  index_score must be the scaled
+ *               forward's (the score-grad reads it as given).  Negative, NaN
+ *               or infinite values are IBWD_ERR_INVALID_ARG.
  * Any other value of the int fields is IBWD_ERR_INVALID_ARG.
  */
 typedef struct {
@@ -229,6 +242,7 @@ typedef struct {
   int dq_bf16;
   int dw_bf16;
   uint16_t* dk_bf16;
+  float sm_scale;
 } ibwd_options;
 
 /* indexer_bwd with options; dq and dw are float* or (bf16) uint16_t* as the
@@ -265,9 +279,10 @@ IBWD_API int indexer_fwd_dense(const uint16_t* q, const uint16_t* k, const float
                                int S, int H, int D, void* stream);
 
 /* Synchronizes `stream`, then reads and clears this device's status word:
- * IBWD_ERR_TIMEOUT if a kernel's bounded wait expired, IBWD_ERR_BAD_INDEX if a
- * device bounds check failed, IBWD_ERR_CUDA if the stream reports an error,
- * IBWD_OK otherwise. */
+ * IBWD_ERR_TIMEOUT if a kernel's bounded wait expired, IBWD_ERR_RANGE if a
+ * q or k entry of a gemm-stage call lay outside the fp16 operand range, IBWD_ERR_CUDA if the stream reports an error,
+ * IBWD_OK otherwise.  A gemm-stage call that
+ * reports IBWD_ERR_TIMEOUT or IBWD_ERR_RANGE has left dq, dw and dk undefined. */
 IBWD_API int indexer_bwd_last_device_status(void* stream);
 
 /* Static English description of a status code. */

@@ -25,7 +25,7 @@ IBWD_ERR_UNSUPPORTED = 2
 IBWD_ERR_WORKSPACE = 3
 IBWD_ERR_CUDA = 4
 IBWD_ERR_TIMEOUT = 5
-IBWD_ERR_BAD_INDEX = 6
+IBWD_ERR_RANGE = 6
 IBWD_DK_ATOMIC = 0
 IBWD_DK_DETERMINISTIC = 1
 
@@ -51,9 +51,9 @@ EXPORTS = (
 
 
 class Options(ctypes.Structure):
-    """ibwd_options of the C header (ids_global, dq_bf16, dw_bf16, dk_bf16)."""
+    """ibwd_options of the C header (ids_global, dq_bf16, dw_bf16, dk_bf16, sm_scale)."""
     _fields_ = [("ids_global", ctypes.c_int), ("dq_bf16", ctypes.c_int), ("dw_bf16", ctypes.c_int),
-                ("dk_bf16", ctypes.c_void_p)]
+                ("dk_bf16", ctypes.c_void_p), ("sm_scale", ctypes.c_float)]
 
 
 class IndexerBwdError(RuntimeError):
@@ -320,11 +320,14 @@ def _out_flag(t, name):
 
 
 def indexer_bwd_ex(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale: float = 1.0,
-                   dk_mode=IBWD_DK_ATOMIC, ids_global: bool = False, dk_bf16=None, workspace=None, stream=None):
+                   dk_mode=IBWD_DK_ATOMIC, ids_global: bool = False, dk_bf16=None, workspace=None, stream=None,
+                   sm_scale: float = 1.0):
     """indexer_bwd with options: dq / dw may be bfloat16 tensors (rounded to
     nearest even from the fp32 results), dk_bf16 an optional bfloat16
-    [B,S_k,D] copy of dk, and ids_global=True takes ids into the flattened
-    [B*S_k] keys.  topk_idx=None selects the dense variant."""
+    [B,S_k,D] copy of dk, ids_global=True takes ids into the flattened
+    [B*S_k] keys, and sm_scale is the forward's logit scale
+    (I = sum_h w relu(sm_scale q.k); the gradients scale by it).
+    topk_idx=None selects the dense variant."""
     _need(q, torch.bfloat16, 4, "q")
     _need(k, torch.bfloat16, 3, "k")
     _need(w, torch.float32, 3, "w")
@@ -336,7 +339,7 @@ def indexer_bwd_ex(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_
     if dk_bf16 is not None:
         _need(dk_bf16, torch.bfloat16, 3, "dk_bf16")
     opts = Options(int(bool(ids_global)), _out_flag(dq, "dq"), _out_flag(dw, "dw"),
-                   None if dk_bf16 is None else dk_bf16.data_ptr())
+                   None if dk_bf16 is None else dk_bf16.data_ptr(), float(sm_scale))
     B, S_q, H, D = q.shape
     S_k = k.shape[1]
     lib = load()
@@ -364,7 +367,7 @@ def indexer_bwd_ex(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_
 
 def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale: float = 1.0,
                      dk_mode=IBWD_DK_ATOMIC, workspace=None, out=None, stream=None, ids_global: bool = False,
-                     out_dtype=torch.float32, dk_bf16=None):
+                     out_dtype=torch.float32, dk_bf16=None, sm_scale: float = 1.0):
     """The whole backward (indexer_bwd / indexer_bwd_dense, or their _ex forms
     when an option is given): dI over attn_score (index_score is kept), then
     dq, dw, dk.
@@ -373,7 +376,9 @@ def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale
     `out` may supply preallocated (dq, dw, dk) tensors; out_dtype
     (torch.float32 or torch.bfloat16) is the dtype of dq and dw when they are
     allocated here; dk is always fp32, and dk_bf16 may receive a bf16 copy.
-    ids_global=True takes ids into the flattened [B*S_k] keys.
+    ids_global=True takes ids into the flattened [B*S_k] keys.  sm_scale is
+    the forward's logit scale, I = sum_h w relu(sm_scale q.k): index_score
+    must come from that forward, and dq, dw, dk scale by it.
     Returns (dq, dw, dk).
     """
     B, S_q, H, D = q.shape
@@ -384,9 +389,10 @@ def indexer_backward(q, k, w, index_score, attn_score, topk_idx=None, grad_scale
         dk = torch.empty((B, S_k, D), dtype=torch.float32, device=q.device)
     else:
         dq, dw, dk = out
-    if ids_global or dk_bf16 is not None or dq.dtype != torch.float32 or dw.dtype != torch.float32:
+    if (ids_global or dk_bf16 is not None or dq.dtype != torch.float32 or dw.dtype != torch.float32
+            or sm_scale != 1.0):
         indexer_bwd_ex(q, k, w, index_score, attn_score, topk_idx, dq, dw, dk, grad_scale, dk_mode, ids_global,
-                       dk_bf16, workspace, stream)
+                       dk_bf16, workspace, stream, sm_scale)
     elif topk_idx is None:
         indexer_bwd_dense(q, k, w, index_score, attn_score, dq, dw, dk, grad_scale, dk_mode, workspace, stream)
     else:

@@ -124,6 +124,9 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   // global ids address the flattened [B*S_k] keys with int32
   if (o.ids_global && (long long)B * S_k > 2147483647LL) return IBWD_ERR_UNSUPPORTED;
   if (o.dk_bf16 && !aligned16(o.dk_bf16)) return IBWD_ERR_INVALID_ARG;
+  // the logit scale: 0 (unset) or positive and finite
+  if (!(o.sm_scale == 0.f || (o.sm_scale > 0.f && o.sm_scale <= 3.4028234663852886e38f)))
+    return IBWD_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, w, dI, dq, dw, dk};
   for (const void* p : ptrs)
     if (!aligned16(p)) return IBWD_ERR_INVALID_ARG;
@@ -153,6 +156,7 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.dw16 = o.dw_bf16 ? static_cast<uint16_t*>(dw) : nullptr;
   a.dk16 = o.dk_bf16;
   a.ids_global = idx ? o.ids_global : 0;
+  a.sm_scale = o.sm_scale == 0.f ? 1.f : o.sm_scale;
   a.dk = dk;
   a.B = B;
   a.S_q = S_q;
@@ -300,7 +304,7 @@ int indexer_bwd_last_device_status(void* stream) {
   if (cudaMemcpy(&word, dv->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return IBWD_ERR_CUDA;
   if (word && cudaMemset(dv->status, 0, sizeof word) != cudaSuccess) return IBWD_ERR_CUDA;
   if (word & 1u) return IBWD_ERR_TIMEOUT;
-  if (word & 2u) return IBWD_ERR_BAD_INDEX;
+  if (word & 2u) return IBWD_ERR_RANGE;
   return IBWD_OK;
 }
 
@@ -312,7 +316,7 @@ const char* indexer_bwd_status_string(int status) {
     case IBWD_ERR_WORKSPACE: return "workspace missing or too small";
     case IBWD_ERR_CUDA: return "CUDA runtime error";
     case IBWD_ERR_TIMEOUT: return "a kernel wait timed out";
-    case IBWD_ERR_BAD_INDEX: return "a device bounds check failed";
+    case IBWD_ERR_RANGE: return "a q or k entry lies outside the fp16 range of the tensor-core operands";
     default: return "unknown status";
   }
 }

@@ -127,9 +127,11 @@ struct Ctx {
   int* rowq;
 };
 
-#define WAIT(bar, par) mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns)
-// Warp-uniform form for the MMA warp, which must stay converged (elect.sync).
-#define WAITW(bar, par) __all_sync(0xffffffffu, WAIT(bar, par))
+// Every role waits with whole, converged warps; the vote makes the outcome
+// warp-uniform, so that a wait that gives up in one lane never leaves the
+// others of its warp in a warp-collective instruction alone.
+#define WAIT(bar, par) __all_sync(0xffffffffu, mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns))
+#define WAITW(bar, par) WAIT(bar, par)
 
 // ------------------------------------------------------------ Q loader ----
 __device__ void q_role(const KParams& p, const Ctx& cx) {
@@ -145,6 +147,7 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
     if (i >= 2 && !WAIT(&cx.bars->dqfull[qb], (uint32_t)(((i - 2) >> 1) & 1))) return;
     const uint16_t* qr = p.q + r * p.H * p.D;
     const uint32_t qs = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+    bool bad = false;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       uint4 v[8];
@@ -160,10 +163,13 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
         const int x = tid + (half * 8 + it) * NQT;
         const int h = x >> 4, ch = x & 15;
         const uint32_t dst = qs + (ch >> 3) * QHALF_BYTES + h * 128 + (((ch & 7) ^ (h & 7)) << 4);
+        bad |= bf16x2_out_of_fp16(v[it].x) || bf16x2_out_of_fp16(v[it].y) || bf16x2_out_of_fp16(v[it].z) ||
+               bf16x2_out_of_fp16(v[it].w);
         st_shared_v4(dst, bf16x2_to_half2(v[it].x), bf16x2_to_half2(v[it].y), bf16x2_to_half2(v[it].z),
                      bf16x2_to_half2(v[it].w));
       }
     }
+    if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) atomicOr(p.status, DEV_FP16_RANGE);
     cx.w_s[qb * kHP + tid] = tid < p.H ? __ldg(p.w + r * p.H + tid) : 0.f;
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->qfull[qb]);
@@ -729,7 +735,7 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t st) {
   __half* k16 = reinterpret_cast<__half*>(ws + 256);
   cudaError_t e = prepare_gemm_rows();
   if (e != cudaSuccess) return e;
-  e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 1, false, a.num_sms, st);
+  e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 1, a.status, false, a.num_sms, st);
   if (e != cudaSuccess) return e;
   KParams p{};
   p.q = a.q;

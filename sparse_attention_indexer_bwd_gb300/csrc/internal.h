@@ -52,6 +52,7 @@ struct GemmArgs {
   uint16_t* dq16;        // if set: dq written here as bf16 (round to nearest even) instead of to dq
   uint16_t* dw16;        // if set: dw likewise
   uint16_t* dk16;        // if set: bf16 copy of the final dk, written after it
+  float sm_scale;        // logit scale s (> 0; 0 reads as 1): dq, dw, dk are s times the unscaled results
 };
 
 // Workspace of the gemm stage (indexer_bwd_gemm and the one-call forms).
@@ -91,10 +92,11 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
 cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
 
 // fp16 copy of k into k16 ([B][S_k+1][128], zero padded, row S_k zero) that
-// also zeroes nsched words of the counters at sched.  pdl: launched
+// also zeroes nsched words of the counters at sched and raises the
+// fp16-range bit of *status for an entry outside the fp16 range.  pdl: launched
 // programmatically behind this library's score-grad kernel.
 cudaError_t launch_k_to_f16(const uint16_t* k, __half* k16, int B, int S_k, int D, unsigned* sched, int nsched,
-                            bool pdl, int num_sms, cudaStream_t st);
+                            unsigned* status, bool pdl, int num_sms, cudaStream_t st);
 
 // The per-row gemm kernel (gemm.cu), atomic dK and no options: served to the
 // allocation-free entry point, whose only scratch is its fp16 copy of k.

@@ -135,6 +135,6 @@ extern "C" int indexer_bwd_gemm_noalloc_status(void* stream) {
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return IBWD_ERR_CUDA;
   }
   if (word & 1u) return IBWD_ERR_TIMEOUT;
-  if (word & 2u) return IBWD_ERR_BAD_INDEX;
+  if (word & 2u) return IBWD_ERR_RANGE;
   return IBWD_OK;
 }

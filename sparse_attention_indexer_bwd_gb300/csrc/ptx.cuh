@@ -11,8 +11,8 @@ namespace ibwd {
 // ---------------------------------------------------------------- status --
 // Device status word bits (reported by indexer_bwd_last_device_status).
 enum : unsigned {
-  DEV_TIMEOUT = 1u << 0,   // a bounded wait gave up
-  DEV_BAD_INDEX = 1u << 1  // an index failed a device-side bounds check
+  DEV_TIMEOUT = 1u << 0,    // a bounded wait gave up
+  DEV_FP16_RANGE = 1u << 1  // a q or k entry lies outside the fp16 range of the tensor-core operands
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -363,7 +363,15 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // bf16 pair (packed in a uint32, low half first) -> fp16 pair.  Exact for
-// |x| in fp16 range; values below 2^-24 flush to zero, above 65504 become inf.
+// 2^-14 <= |x| <= 65504; smaller magnitudes round to fp16 subnormals
+// (absolute error at most 2^-25; below 2^-25 they become zero), larger ones
+// and non-finite values become inf or NaN (see bf16x2_out_of_fp16).
+// True when either bf16 of the pair has |x| > 65504 or is not finite (the
+// largest finite fp16 is 65504, bf16 0x477F; bf16 0x4780 is 65536).
+__device__ __forceinline__ bool bf16x2_out_of_fp16(uint32_t v) {
+  return (v & 0x7FFFu) > 0x477Fu || ((v >> 16) & 0x7FFFu) > 0x477Fu;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_to_half2(uint32_t v) {
   float lo = __uint_as_float(v << 16);
   float hi = __uint_as_float(v & 0xFFFF0000u);

@@ -79,10 +79,15 @@ def test_shape_errors_need_no_device(lib):
     # options: flags other than 0/1 are rejected before any device call
     import ctypes
     p = ctypes.c_void_p(16)  # never dereferenced: the option check comes first
-    for bad in (ibwd.Options(2, 0, 0, None), ibwd.Options(0, 3, 0, None), ibwd.Options(0, 0, -1, None)):
+    for bad in (ibwd.Options(2, 0, 0, None), ibwd.Options(0, 3, 0, None), ibwd.Options(0, 0, -1, None),
+                ibwd.Options(0, 0, 0, None, -1.0), ibwd.Options(0, 0, 0, None, float("nan")),
+                ibwd.Options(0, 0, 0, None, float("inf")), ibwd.Options(0, 0, 0, None, -0.0 - 1e-30)):
         assert lib.indexer_bwd_ex(p, p, p, p, p, p, p, p, p, 1, 4, 4, 4, 32, 4, 1.0, 0, ctypes.byref(bad), p,
                                   1 << 20, None) == ibwd.IBWD_ERR_INVALID_ARG
-    assert ctypes.sizeof(ibwd.Options) == 24  # matches the C struct (3 ints, padding, a pointer)
+        assert lib.indexer_bwd_dense_ex(p, p, p, p, p, p, p, p, 1, 4, 4, 32, 1.0, 0, ctypes.byref(bad), p,
+                                        1 << 20, None) == ibwd.IBWD_ERR_INVALID_ARG
+    # matches the C struct: 3 ints, padding, a pointer, a float, padding
+    assert ctypes.sizeof(ibwd.Options) == 32 and ibwd.Options.sm_scale.offset == 24
     assert lib.indexer_bwd(None, None, None, None, None, None, None, None, None, 1, 4, 4, 100, 32, 4, 1.0, 0, None,
                            0, None) == ibwd.IBWD_ERR_INVALID_ARG
 

@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import synth
+import oracle
 import sparse_attention_indexer_bwd_gb300 as ibwd
 from gpu_util import assert_close, case_inputs, oracle_all, t_bf16, t_f32, t_i32
 
@@ -74,3 +75,29 @@ def test_global_ids_match_local_ids_and_never_alias(mode):
     xl["idx"] = local
     ref = oracle_all(wl, xl)
     assert_close(got[1].cpu().numpy(), got[2].cpu().numpy(), got[3].cpu().numpy(), ref[1:], tag="global ids")
+
+
+@pytest.mark.parametrize("sm_scale", [0.5, 0.0884])
+@pytest.mark.parametrize("wl", [W("scale_sparse", 2, 40, 64, 300, 260, 150, "causal", 34),
+                                W("scale_dense", 1, 8, 64, 200, 200, 0, "dense", 35)], ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", [ibwd.IBWD_DK_ATOMIC, DET])
+def test_logit_scale_matches_the_scaled_oracle(wl, mode, sm_scale):
+    """index_score from the forward with the logit scale inside the ReLU; the
+    backward with that scale against the oracle's scaled definitions."""
+    x = synth.make_inputs(wl)
+    if wl.dense:
+        x["I"] = oracle.forward_dense(x["q"], x["k"], x["w"], sm_scale).astype(np.float32)
+        dI = oracle.score_grad_dense(x["I"], x["attn"])
+        ref = oracle.gemm_dense(x["q"], x["k"], x["w"], dI, sm_scale)
+    else:
+        x["I"] = oracle.forward_sparse(x["q"], x["k"], x["w"], x["idx"], wl.S_k, sm_scale).astype(np.float32)
+        dI = oracle.score_grad_sparse(x["I"], x["attn"], x["idx"], wl.S_k)
+        ref = oracle.gemm_sparse(x["q"], x["k"], x["w"], dI, x["idx"], wl.S_k, sm_scale)
+    attn, dq, dw, dk = run(wl, x, mode=mode, sm_scale=sm_scale)
+    assert_close(dq.cpu().numpy(), dw.cpu().numpy(), dk.cpu().numpy(), ref, tag=f"sm_scale {sm_scale}")
+    # and the unscaled call on the same I differs by exactly the factor's effect
+    if sm_scale == 0.5 and mode == DET:
+        _, dq1, dw1, dk1 = run(wl, x, mode=mode)
+        assert torch.equal(dq.view(torch.int32), (0.5 * dq1).view(torch.int32))
+        assert torch.equal(dk.view(torch.int32), (0.5 * dk1).view(torch.int32))
+        assert torch.equal(dw.view(torch.int32), (0.5 * dw1).view(torch.int32))
