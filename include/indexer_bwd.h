@@ -33,9 +33,12 @@
  *    2^-14 <= |x| <= 65504 and to fp16 subnormals (absolute error at most
  *    2^-25) below that.  A larger or non-finite entry is reported as
  *    IBWD_ERR_RANGE by indexer_bwd_last_device_status.
- *  - The library allocates no memory on the compute path.  The deterministic
- *    mode uses the caller's workspace.  One 4-byte device status word per
- *    device is allocated on first use and kept until process exit.
+ *  - The library allocates no memory on the compute path: every scratch
+ *    buffer is in the caller's workspace.  Per device, one 4-byte status
+ *    word, one internal stream and two events (the gemm stage builds its q
+ *    copies on that stream, forked from and joined back to the caller's
+ *    stream within each call) are created on first use and kept until
+ *    process exit.
  */
 #ifndef INDEXER_BWD_H
 #define INDEXER_BWD_H
@@ -85,17 +88,20 @@ IBWD_API int indexer_bwd_score_grad(const float* index_score, float* attn_score,
                            int B, int S_q, int S_k, int topk, float grad_scale, float* dk_to_zero,
                            int D, void* stream);
 
-/* Bytes of device workspace indexer_bwd_gemm needs (always > 0): a 256-byte
- * block of counters; an fp16 copy of k, 256 bytes per key row plus one zero
- * row per batch; and, since the gemm stage takes the query rows in blocks of
- * four (nb = B * ceil(S_q / 4) blocks) against the union of their keys,
- * per block 20 bytes and ceil(min(S_k, 4*topk) / 128) tile records of 2560
- * bytes.  The deterministic mode adds 512 bytes per record and per-entry dK
- * rows, 4*D bytes for each of nb * min(S_k, 4*topk) entries, plus its key
- * sort (4*S_k bytes per two blocks).  The dense variant has no records; its
- * deterministic mode has one dK row per (block, causal key).  The workspace
- * is rewritten by every call: calls that may overlap on the GPU need
- * separate workspaces.  0 for unsupported arguments. */
+/* Bytes of device workspace indexer_bwd_gemm needs (always > 0).  The gemm
+ * stage takes the query rows in blocks of four (nb = B * ceil(S_q / 4)
+ * blocks) against the union of their keys; the workspace holds, each part
+ * rounded up to 256 bytes: a 256-byte block of counters; an fp16 copy of k,
+ * 256 bytes per key row plus one zero row per batch; per block a 64 KB fp16
+ * copy of its q rows laid out as the tensor-core operand and 16 bytes of
+ * block data; for the sparse variant per block 4 bytes of ordering and
+ * ceil(min(S_k, 4*topk) / 128) tile records of 2560 bytes.  The
+ * deterministic mode adds 512 bytes per record, one dK row (4*D bytes) per
+ * (block, key) entry -- nb * min(S_k, 4*topk) of them, or for the dense
+ * variant one per (block, causal key) -- its key sort (4*S_k bytes per two
+ * blocks) and 4*(B*S_k + 1) bytes of key offsets.  The workspace is
+ * rewritten by every call: calls that may overlap on the GPU need separate
+ * workspaces.  0 for unsupported arguments. */
 IBWD_API size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk,
                                        int dk_mode);
 
@@ -110,7 +116,9 @@ IBWD_API size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, 
  *   dq     fp32 [B,S_q,H,D], fully written;  dw fp32 [B,S_q,H], fully written
  *   dk     fp32 [B,S_k,D]: IBWD_DK_ATOMIC accumulates into it (zero it first,
  *          e.g. through indexer_bwd_score_grad's dk_to_zero);
- *          IBWD_DK_DETERMINISTIC overwrites it.
+ *          IBWD_DK_DETERMINISTIC overwrites it: each (block, key) row of
+ *          contributions is stored at its place in key order and every
+ *          key's rows are summed in a fixed order.
  *   workspace  device memory of at least indexer_bwd_gemm_workspace_size bytes
  * dq and dw are bitwise reproducible run to run in both modes.
  */

@@ -12,6 +12,10 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   unsigned* status = nullptr;  // one device word, allocated once
+  // a second stream for work that runs beside the caller's stream within one
+  // call (the gemm stage's q images), and the events that fork and join it
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -33,6 +37,10 @@ int device_info(DeviceInfo** out) {
     if (d.supported) {
       if (cudaMalloc(&d.status, sizeof(unsigned)) != cudaSuccess) return IBWD_ERR_CUDA;
       if (cudaMemset(d.status, 0, sizeof(unsigned)) != cudaSuccess) return IBWD_ERR_CUDA;
+      if (cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess)
+        return IBWD_ERR_CUDA;
     }
     d.ready = true;
   }
@@ -169,6 +177,9 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.ws_bytes = ws_bytes;
   a.status = dv->status;
   a.num_sms = dv->num_sms;
+  a.side = dv->side;
+  a.ev_fork = dv->fork;
+  a.ev_join = dv->join;
   if (I) {
     rc = score_grad_common(I, const_cast<float*>(dI), idx, need_idx, B, S_q, S_k, L, grad_scale,
                            mode == IBWD_DK_ATOMIC ? dk : nullptr, D, stream, a.ids_global);

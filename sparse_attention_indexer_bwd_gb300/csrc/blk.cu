@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   int* ids_s = reinterpret_cast<int*>(drow + R * p.dcap);  // staged: [4][Lp] ids, then [4][Lp] dI
   float* dI_s = reinterpret_cast<float*>(ids_s + R * Lp);
   __shared__ int s_cnt[5], s_kmin[4], s_kmax[4];
-  __shared__ float s_wmax[4], s_wmin[4], s_dmax[4][R];
+  __shared__ float s_wmax[4], s_dmax[4][R];
   __shared__ int s_last;
   griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -112,15 +112,13 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   const float* dr_in = p.staged ? dI_s + warp * Lp : p.dI + (own ? (row0 + warp) * p.L : 0);
   if (p.staged) stage_rows(smem_u32(ids_s), p.idx, row0, Rb, p.L, Lp);
 
-  float wmax = 0.f, wmin = 3.0e38f;  // over the row's heads; wmin stays large for rows past the block
+  float wmax = 0.f;  // over the row's heads
   if (own) {
     for (int h = lane; h < p.H; h += 32) {
       const float a = fabsf(__ldg(p.w + (row0 + warp) * p.H + h));
       wmax = fmaxf(wmax, a);
-      wmin = fminf(wmin, a);
     }
     wmax = warp_max(wmax);
-    wmin = -warp_max(-wmin);
   }
   if (p.staged) {
     cp_async_wait_all();
@@ -152,7 +150,6 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   }
   if (lane == 0) {
     s_wmax[warp] = wmax;
-    s_wmin[warp] = wmin;
   }
   __syncthreads();
   if (p.S_k > p.W) {
@@ -268,14 +265,12 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   }
   __syncthreads();
   if (tid == 0) {
-    float m = 0.f, wx = 0.f, wn = 3.0e38f;
+    float m = 0.f;
     for (int r = 0; r < R; ++r) {
       const float d = fmaxf(fmaxf(s_dmax[0][r], s_dmax[1][r]), fmaxf(s_dmax[2][r], s_dmax[3][r]));
       m = fmaxf(m, d * s_wmax[r]);
-      wx = fmaxf(wx, s_wmax[r]);
-      wn = fminf(wn, s_wmin[r]);
     }
-    p.binfo[b] = make_int4(ntiles, dz_scale_exponent(m), U, direct_dw(wn, wx));
+    p.binfo[b] = make_int4(ntiles, dz_scale_exponent(m), U, 0);
     __threadfence();
     s_last = atomicAdd(p.done, 1u) == (unsigned)(p.nblocks - 1);
   }
@@ -309,6 +304,79 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   __syncthreads();
   for (long long x = tid; x < p.nblocks; x += UT)
     p.border[atomicAdd(&cur[min(NBUCKET - 1, __ldcg(&p.binfo[x].x))], 1)] = (int)x;
+}
+
+struct QImg {  // the Q operand images of every block
+  const uint16_t* q;
+  uint8_t* img;
+  long long nblocks;
+  int S_q, H, D, nbpb;
+};
+
+// Chunk x of the images (16 bytes; 4096 per block); returns the fp16-range flag.
+__device__ __forceinline__ bool q_image_at(const QImg& qi, long long x) {
+  const long long blk = x / (NR * 16);
+  const int within = (int)(x % (NR * 16));
+  const int batch = (int)(blk / qi.nbpb), t0 = (int)(blk % qi.nbpb) * R;
+  return q_image_chunk(qi.q, qi.img + blk * QIMG_BYTES, (long long)batch * qi.S_q + t0, min(R, qi.S_q - t0), qi.H,
+                       qi.D, within >> 4, within & 15);
+}
+
+// The q images, on the side stream beside the union pass (or the dense
+// scale pass).
+__global__ void q_image_kernel(const QImg qi, unsigned* __restrict__ status) {
+  const long long nq = qi.nblocks * (NR * 16);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  bool bad = false;
+  long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  for (; x + 3 * stride < nq; x += 4 * stride) {  // four chunks in flight per thread
+#pragma unroll
+    for (int k = 0; k < 4; ++k) bad |= q_image_at(qi, x + k * stride);
+  }
+  for (; x < nq; x += stride) bad |= q_image_at(qi, x);
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, DEV_FP16_RANGE);
+}
+
+// Dense blocks: block b holds keys [0, t0 + Rb); its dz scale exponent from
+// max |dI| over each row's causal keys and max |w|, written to binfo (the
+// gemm kernel's scan reads it).  One CTA of four warps per block, warp r on
+// row r.
+__global__ void __launch_bounds__(128) dense_scale_kernel(const float* __restrict__ dI, const float* __restrict__ w,
+                                                          int4* __restrict__ binfo, int S, int H, int nbpb) {
+  __shared__ float s_m[4];
+  griddep_launch_dependents();
+  griddep_wait();  // dI is the score-grad's output
+  const long long b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int batch = (int)(b / nbpb), t0 = (int)(b % nbpb) * R;
+  const int Rb = min(R, S - t0);
+  float m = 0.f;
+  if (warp < Rb) {
+    const long long row = (long long)batch * S + t0 + warp;
+    const float* dr = dI + row * S;
+    const int n = t0 + warp + 1;  // causal keys 0 .. t
+    float mx = 0.f;
+    if ((S & 3) == 0) {
+      const float4* d4 = reinterpret_cast<const float4*>(dr);
+      for (int v = lane; v < (n >> 2); v += 32) {
+        const float4 x = __ldg(d4 + v);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+      }
+      for (int j = ((n >> 2) << 2) + lane; j < n; j += 32) mx = fmaxf(mx, fabsf(__ldg(dr + j)));
+    } else {
+      for (int j = lane; j < n; j += 32) mx = fmaxf(mx, fabsf(__ldg(dr + j)));
+    }
+    float wm = 0.f;
+    for (int h = lane; h < H; h += 32) wm = fmaxf(wm, fabsf(__ldg(w + row * H + h)));
+    m = warp_max(mx) * warp_max(wm);
+  }
+  if (lane == 0) s_m[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float mb = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+    const int U = t0 + Rb;
+    binfo[b] = make_int4((U + kBM - 1) / kBM, dz_scale_exponent(mb), U, 0);
+  }
 }
 
 // k (bf16, [B, S_k, D]) -> fp16 [B][S_k + 1][128]: zero padded beyond D, and
@@ -414,12 +482,14 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
   off = up(off + 256);
   w.k16 = off;
   off = up(off + (size_t)B * (S_k + 1) * kDP * 2);
+  w.qimg = off;
+  off = up(off + (size_t)w.nblocks * QIMG_BYTES);
+  w.binfo = off;
+  off = up(off + (size_t)w.nblocks * 16);
   if (!dense) {
     const long long ucap = std::min<long long>(S_k, (long long)R * L);
     w.tcap = (int)std::max<long long>(1, (ucap + kBM - 1) / kBM);
     w.rstride = deterministic ? (int)REC_BYTES : REC_POS;
-    w.binfo = off;
-    off = up(off + (size_t)w.nblocks * 16);
     w.border = off;
     off = up(off + (size_t)w.nblocks * 4);
     w.rec = off;
@@ -454,18 +524,36 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   char* ws = static_cast<char*>(a.ws);
   __half* k16 = reinterpret_cast<__half*>(ws + lay.k16);
   unsigned* sched = reinterpret_cast<unsigned*>(ws + lay.sched);
+  uint8_t* qimg = reinterpret_cast<uint8_t*>(ws + lay.qimg);
+  int4* binfo = reinterpret_cast<int4*>(ws + lay.binfo);
   // programmatic only right after this library's score-grad kernel: the
   // kernel reads k before it waits for its predecessor
   cudaError_t e =
       launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 2, a.status, a.after_score_grad != 0, a.num_sms, st);
   if (e != cudaSuccess) return e;
+  // the q images on the side stream: the union pass (or the dense scale
+  // pass) is latency-bound and leaves the memory system mostly idle, so the
+  // two overlap; the gemm kernel waits for both
+  e = cudaEventRecord(a.ev_fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(a.side, a.ev_fork, 0);
+  if (e != cudaSuccess) return e;
+  {
+    const QImg qi{a.q, qimg, lay.nblocks, a.S_q, a.H, a.D, lay.nbpb};
+    const long long n = lay.nblocks * (NR * 16);
+    // two CTAs per SM: with the union pass's four, the register file holds both
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 2LL * a.num_sms));
+    q_image_kernel<<<blocks, 256, 0, a.side>>>(qi, a.status);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaEventRecord(a.ev_join, a.side);
+    if (e != cudaSuccess) return e;
+  }
   if (!dense) {
     UParams u{};
     u.idx = a.idx;
     u.dI = a.dI;
     u.w = a.w;
     u.rec = ws + lay.rec;
-    u.binfo = reinterpret_cast<int4*>(ws + lay.binfo);
+    u.binfo = binfo;
     u.border = reinterpret_cast<int*>(ws + lay.border);
     u.done = sched + 1;
     u.nblocks = lay.nblocks;
@@ -483,19 +571,25 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     if (!set_smem_attr((const void*)union_kernel, sh, g_attr_union)) return cudaErrorInvalidValue;
     // it reads the ids before its predecessor completes and dI only after
     e = launch_ex(union_kernel, (unsigned)lay.nblocks, (unsigned)UT, sh, st, true, u);
-    if (e != cudaSuccess) return e;
+  } else {
+    e = launch_ex(dense_scale_kernel, (unsigned)lay.nblocks, 128u, 0, st, true, static_cast<const float*>(a.dI), a.w,
+                  binfo, a.S_q, a.H, lay.nbpb);
   }
+  if (e != cudaSuccess) return e;
   if (a.deterministic) {
     e = launch_det_sort(a, lay, st);
     if (e != cudaSuccess) return e;
   }
+  e = cudaStreamWaitEvent(st, a.ev_join, 0);
+  if (e != cudaSuccess) return e;
   BParams p{};
   p.q = a.q;
   p.k16 = k16;
+  p.qimg = qimg;
   p.w = a.w;
   p.dI = a.dI;
   p.rec = dense ? nullptr : ws + lay.rec;
-  p.binfo = dense ? nullptr : reinterpret_cast<const int4*>(ws + lay.binfo);
+  p.binfo = binfo;
   p.border = dense ? nullptr : reinterpret_cast<const int*>(ws + lay.border);
   p.dq = a.dq;
   p.dw = a.dw;

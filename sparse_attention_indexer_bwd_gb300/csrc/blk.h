@@ -41,11 +41,25 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int REC_KEY = 0, REC_DIS = 512, REC_POS = 2560;
 constexpr uint32_t REC_BYTES = 3072;
 
-// Whether a block's dW is summed per key (1) rather than recovered from the
-// dQ accumulator: when the smallest |w| of its heads is zero, below 2^-12 of
-// the largest, or not finite.
-__device__ __forceinline__ int direct_dw(float wmin, float wmax) {
-  return (wmin > 0.f && wmin >= 0x1p-12f * wmax && wmax <= 3.0e38f) ? 0 : 1;
+// A block's q rows as the gemm kernel's Q operand: fp16, [d-half][(r,h) =
+// 64r + h][128 B], each 128-byte row's 16-byte chunks in the 128-byte swizzle
+// (chunk c of row n at (c ^ n % 8) * 16); rows past the block, heads past H
+// and columns past D zero.  Built once per call, copied as it is.
+constexpr uint32_t QIMG_HALF = NR * 128;  // one 64-column half: 32 KB
+constexpr uint32_t QIMG_BYTES = 2 * QIMG_HALF;
+
+// One 16-byte chunk of a block's image: chunk c (0..15, 8 columns each) of
+// (r,h) row n (0..255), converted from the bf16 rows starting at global row
+// row0 (Rb of them).  Returns whether an entry lies outside the fp16 range.
+__device__ __forceinline__ bool q_image_chunk(const uint16_t* __restrict__ q, uint8_t* img, long long row0, int Rb,
+                                              int H, int D, int n, int c) {
+  const int r = n >> 6, h = n & 63;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (r < Rb && h < H && c * 8 < D)
+    v = __ldg(reinterpret_cast<const uint4*>(q + ((row0 + r) * H + h) * D + c * 8));
+  *reinterpret_cast<uint4*>(img + (c >> 3) * QIMG_HALF + n * 128 + (((c & 7) ^ (n & 7)) << 4)) =
+      make_uint4(bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z), bf16x2_to_half2(v.w));
+  return bf16x2_out_of_fp16(v.x) || bf16x2_out_of_fp16(v.y) || bf16x2_out_of_fp16(v.z) || bf16x2_out_of_fp16(v.w);
 }
 
 struct BParams {
@@ -53,8 +67,9 @@ struct BParams {
   const __half* k16;   // [B][S_k + 1][128]; row S_k of each batch is zero
   const float* w;      // [rows, H]
   const float* dI;     // dense: [rows, S] (sparse blocks read their tile records instead)
+  const uint8_t* qimg; // per block: the Q operand image
   const char* rec;     // sparse: tile records
-  const int4* binfo;   // sparse: per block {tiles, c, entries, 0}
+  const int4* binfo;   // per block {tiles, c, entries, 0}
   const int* border;   // sparse: processing order of the blocks
   float* dq;
   float* dw;

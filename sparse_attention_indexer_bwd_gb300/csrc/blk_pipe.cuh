@@ -55,7 +55,7 @@ constexpr int NKQ = 4;  // key quarters of a tile: four dz warps per TMEM lane q
 
 constexpr uint32_t KTILE = kBM * kDP * 2;  // 32 KB: [2 d-halves][128 keys][128 B]
 constexpr uint32_t KHALF = kBM * 128;      // 16 KB
-constexpr uint32_t QDH = NR * 128;         // Q block, one 64-d half: [256 (r,h)][128 B] = 32 KB
+constexpr uint32_t QDH = QIMG_HALF;        // Q block, one 64-d half: [256 (r,h)][128 B] = 32 KB
 constexpr uint32_t DZKC = NR * 128;        // dz tile, one 64-key chunk: [256 (r,h)][128 B] = 32 KB
 
 constexpr uint32_t TM_Z = 0, TM_DK = 128, TM_DQ = 256, TM_COLS = 512;
@@ -69,8 +69,7 @@ struct Hdr {        // per tile, written by the scan
   int c;            // dz scale exponent of the block
   int flags;
   int batch;
-  int direct;       // dW of this block by per-key accumulation (some |w| is zero or tiny)
-  int pad;
+  int pad[2];
 };
 
 struct Bars {
@@ -131,7 +130,7 @@ __device__ __forceinline__ const int* rec_pos(const Ctx& cx, int ms) {
 // first CTAs), compiled only with -DIBWD_TRACE for pipeline analysis.
 enum TraceEv {
   EV_SCAN_PUB, EV_GATHER_ISSUED, EV_MMA_ZA, EV_MMA_ZB, EV_MMA_DQ, EV_MMA_DK, EV_DZ_ZA, EV_DZ_ZB, EV_DZ_DONE,
-  EV_DK_FULL, EV_DK_DONE, EV_Q_START, EV_Q_DONE, EV_COUNT
+  EV_DK_FULL, EV_DK_DONE, EV_Q_START, EV_Q_DONE, EV_EPI_A, EV_EPI_B, EV_EPI_C, EV_COUNT
 };
 #ifdef IBWD_TRACE
 constexpr int TRACE_CTAS = 4, TRACE_TILES = 512;
@@ -192,64 +191,16 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
     const int t0 = jb * R;
     const int Rb = min(R, p.S_q - t0);
     const int row0 = batch * p.S_q + t0;
-    int ntiles, c, U, direct;
-    if (!p.dense) {
-      const int4 bi = __ldg(p.binfo + b);
-      ntiles = bi.x;
-      c = bi.y;
-      U = bi.z;
-      direct = bi.w;
-    } else {
-      // keys [0, t0 + Rb); the scale from max |dI| over each row's causal keys and max |w|
-      U = t0 + Rb;
-      ntiles = (U + kBM - 1) / kBM;
-      float m = 0.f, wx = 0.f, wn = 3.0e38f;
-      for (int r = 0; r < Rb; ++r) {
-        const float* dr = p.dI + (long long)(row0 + r) * p.S_q;
-        const int n = t0 + r + 1;
-        float mx = 0.f;
-        if ((p.S_q & 3) == 0) {
-          const float4* d4 = reinterpret_cast<const float4*>(dr);
-          const int n4 = n >> 2;
-          int v = lane;
-          for (; v + 96 < n4; v += 128) {
-            float4 x[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) x[k] = __ldg(d4 + v + 32 * k);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x[k].x), fabsf(x[k].y)), fmaxf(fabsf(x[k].z), fabsf(x[k].w))));
-          }
-          for (; v < n4; v += 32) {
-            const float4 x = __ldg(d4 + v);
-            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-          }
-          for (int j = 4 * n4 + lane; j < n; j += 32) mx = fmaxf(mx, fabsf(__ldg(dr + j)));
-        } else {
-          for (int j = lane; j < n; j += 32) mx = fmaxf(mx, fabsf(__ldg(dr + j)));
-        }
-        float wm = 0.f, wl = 3.0e38f;
-        for (int h = lane; h < p.H; h += 32) {
-          const float a = fabsf(__ldg(p.w + (long long)(row0 + r) * p.H + h));
-          wm = fmaxf(wm, a);
-          wl = fminf(wl, a);
-        }
-        wm = warp_max(wm);
-        m = fmaxf(m, warp_max(mx) * wm);
-        wx = fmaxf(wx, wm);
-        wn = fminf(wn, -warp_max(-wl));
-      }
-      c = dz_scale_exponent(m);
-      direct = direct_dw(wn, wx);
-    }
+    // tiles, dz scale exponent and entries of the block (the union pass or the
+    // dense scale pass)
+    const int4 bi = __ldg(p.binfo + b);
+    const int ntiles = bi.x, c = bi.y, U = bi.z;
     // publish the block to the Q loader; warm L2 with its q rows
     if (!WAIT(&B->bempty[i % BQ], ((i / BQ) & 1) ^ 1)) return drain_records();
     if (lane == 0) {
-      bq[i % BQ] = make_int4(row0, Rb, 0, 0);
+      bq[i % BQ] = make_int4(row0, Rb, (int)b, 0);
       mbar_arrive(&B->bfull[i % BQ]);
-      const uint32_t qbytes = (uint32_t)Rb * p.H * p.D * 2;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.q + (long long)row0 * p.H * p.D),
-                   "r"(qbytes)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.qimg + b * QIMG_BYTES), "r"(QIMG_BYTES)
                    : "memory");
     }
     unsigned pend = 0;
@@ -268,7 +219,7 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
       uint8_t* rs = cx.smem + OFF_REC + ms * REC_BYTES;
       if (!p.dense) {
         if (lane == 0) {
-          cx.hdr[ms] = Hdr{row0, Rb, max(count, 0), c, flags, batch, direct, 0};
+          cx.hdr[ms] = Hdr{row0, Rb, max(count, 0), c, flags, batch, {0, 0}};
           fence_proxy_async_smem();  // earlier generic reads of the slot precede the async writes
           mbar_arrive_expect_tx(&B->mfull[ms], copy_bytes);
           bulk_g2s(smem_u32(rs), p.rec + ((long long)b * p.tcap + k) * p.rstride, copy_bytes, &B->mfull[ms]);
@@ -296,7 +247,7 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
         }
         __syncwarp();
         if (lane == 0) {
-          cx.hdr[ms] = Hdr{row0, Rb, count, c, flags, batch, direct, 0};
+          cx.hdr[ms] = Hdr{row0, Rb, count, c, flags, batch, {0, 0}};
           mbar_arrive(&B->mfull[ms]);
         }
       }
@@ -335,7 +286,10 @@ __device__ void gather_role(const BParams& p, const Ctx& cx) {
     const __half* kb = p.k16 + (long long)batch * (p.S_k + 1) * kDP + ch * 8;
 #pragma unroll 4
     for (int i2 = 0; i2 < kBM / 8; ++i2) {  // rows rsub + 8*i2 and rsub + 4 + 8*i2
-      const int k0 = keys[rsub + 8 * i2], k1 = keys[rsub + 4 + 8 * i2];  // padding entries hold the zero row S_k
+      // padding entries hold the zero row S_k; the clamp keeps every address
+      // inside k16 whatever a record holds
+      const int k0 = min((unsigned)keys[rsub + 8 * i2], (unsigned)p.S_k);
+      const int k1 = min((unsigned)keys[rsub + 4 + 8 * i2], (unsigned)p.S_k);
       cp_async16(kbase + off0 + i2 * 1024, kb + (long long)k0 * kDP, 16);
       cp_async16(kbase + off1 + i2 * 1024, kb + (long long)k1 * kDP, 16);
     }
@@ -347,54 +301,44 @@ __device__ void gather_role(const BParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------- Q loader ---
-// The block's q rows (bf16) land by cp.async in the fp16 operand's swizzled
-// positions ([d-half][(r,h) = 64r + h][128 B]) and are converted in place
-// (bf16 -> fp16 keeps the element size); rows past the block, heads past H
-// and columns past D are zero.
+// The block's Q operand image (fp16, already swizzled: built by the union
+// pass or the k conversion kernel) arrives by one bulk copy once the previous
+// block's last MMA that reads Q is complete; the loader warps meanwhile put
+// the block's w in shared memory.
 __device__ void q_role(const BParams& p, const Ctx& cx) {
   const int tid = threadIdx.x - W_Q0 * 32;  // 0..95
   Bars* B = cx.bars;
   const int4* bq = reinterpret_cast<const int4*>(cx.smem + OFF_BQ);
   float* w_s = reinterpret_cast<float*>(cx.smem + OFF_W);
+  long long issued = -1;  // the last block whose image copy was issued
+  // before the role returns: that copy has landed (its phase completes once
+  // every loader thread has arrived and the bytes are in)
+  auto drain = [&]() {
+    if (issued >= 0) drain_wait(&B->qfull, (uint32_t)(issued & 1), p.status, p.drain_ns);
+  };
   for (long long i = 0;; ++i) {
-    if (!WAIT(&B->bfull[i % BQ], (i / BQ) & 1)) return;
-    const int row0 = bq[i % BQ].x, Rb = bq[i % BQ].y;
+    if (!WAIT(&B->bfull[i % BQ], (i / BQ) & 1)) return drain();
+    const int row0 = bq[i % BQ].x, Rb = bq[i % BQ].y, blk = bq[i % BQ].z;
     mbar_arrive(&B->bempty[i % BQ]);
-    if (row0 < 0) return;
-    // the previous block's last MMAs that read Q (and its w) are complete
-    if (!WAIT(&B->qempty, (i & 1) ^ 1)) return;
-    if (tid == 0) TRACE(EV_Q_START, (int)i);
-    constexpr int NCHUNK = NR * 16;  // 16-byte chunks of the block
-#pragma unroll 4
-    for (int x = tid; x < NCHUNK; x += NQT) {
-      const int n = x >> 4, c = x & 15, r = n >> 6, h = n & 63;
-      const bool ok = r < Rb && h < p.H && c * 8 < p.D;
-      const uint16_t* src = ok ? p.q + ((long long)(row0 + r) * p.H + h) * p.D + c * 8 : p.q;
-      cp_async16(cx.sbase + OFF_Q + (c >> 3) * QDH + n * 128 + (((c & 7) ^ (n & 7)) << 4), src, ok ? 16u : 0u);
-    }
-    float wv[(NR + NQT - 1) / NQT];  // w of the block, loaded while the copies fly
+    if (row0 < 0) return drain();
+    float wv[(NR + NQT - 1) / NQT];  // w of the block
 #pragma unroll
     for (int k = 0; k < (NR + NQT - 1) / NQT; ++k) {
       const int e = tid + NQT * k, r = e >> 6, h = e & 63;
       wv[k] = (e < NR && r < Rb && h < p.H) ? __ldg(p.w + (long long)(row0 + r) * p.H + h) : 0.f;
     }
-    cp_async_wait_all();
-    bool bad = false;
-#pragma unroll 4
-    for (int x = tid; x < NCHUNK; x += NQT) {
-      const int n = x >> 4, c = x & 15;
-      const uint32_t a = cx.sbase + OFF_Q + (c >> 3) * QDH + n * 128 + (((c & 7) ^ (n & 7)) << 4);
-      uint32_t v0, v1, v2, v3;
-      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3) : "r"(a));
-      bad |= bf16x2_out_of_fp16(v0) || bf16x2_out_of_fp16(v1) || bf16x2_out_of_fp16(v2) || bf16x2_out_of_fp16(v3);
-      st_shared_v4(a, bf16x2_to_half2(v0), bf16x2_to_half2(v1), bf16x2_to_half2(v2), bf16x2_to_half2(v3));
+    // the previous block's last MMAs that read Q (and its w) are complete
+    if (!WAIT(&B->qempty, (i & 1) ^ 1)) return drain();
+    issued = i;
+    if (tid == 0) {
+      TRACE(EV_Q_START, (int)i);
+      mbar_expect_tx(&B->qfull, QIMG_BYTES);
+      bulk_g2s(cx.sbase + OFF_Q, p.qimg + (long long)blk * QIMG_BYTES, QIMG_BYTES, &B->qfull);
     }
-    if (__any_sync(FULL, bad) && (tid & 31) == 0) atomicOr(p.status, DEV_FP16_RANGE);
 #pragma unroll
     for (int k = 0; k < (NR + NQT - 1) / NQT; ++k)
       if (tid + NQT * k < NR) w_s[tid + NQT * k] = wv[k];
-    fence_proxy_async_smem();
-    mbar_arrive(&B->qfull);
+    mbar_arrive(&B->qfull);  // the phase completes when the copy has landed too
     if (tid == 0) TRACE(EV_Q_DONE, (int)i);
   }
 }
@@ -519,83 +463,62 @@ __device__ void gmma_role(const BParams& p, const Ctx& cx) {
 // their z (16 at a time), releases the buffer after the second load, and
 // writes dz = dI w 2^c [z > 0] (fp16) into its 64 bytes of the dz row.
 //
-// dW.  Summing dz z over the keys gives w 2^c dW, and sum_s dz z =
-// q . (sum_s dz k_s) = q . dQraw, the dQ accumulator before its 2^-c scale:
-// so dW = (q . dQraw) / (w 2^c), one dot product per (r,h) at block end.
-// Blocks where some |w| is zero or below 2^-12 of the block's largest (the
-// dz of those heads would lose precision or vanish) accumulate
-// dW = sum_s dI relu(z) per key instead (Hdr::direct).
-__device__ void dz_epilogue(const BParams& p, const Ctx& cx, int row0, int Rb, int c, int direct, int i,
-                            float acc0, float acc1, float wv0, float wv1) {
+// dW = sum_s dI relu(z): each thread sums dI relu(z) over its 32 keys of a
+// tile as it forms dz (two FMAs per pair of keys, no shared memory), over the
+// block's tiles in registers; at block end the four key quarters' partials
+// are added in a fixed order.
+__device__ void dz_epilogue(const BParams& p, const Ctx& cx, int row0, int Rb, int c, int i, float acc0,
+                            float acc1) {
   const int dzw = (threadIdx.x >> 5) - W_DZ0, q = (threadIdx.x >> 5) & 3, kq = dzw >> 2, lane = threadIdx.x & 31;
   const int tdz = threadIdx.x - W_DZ0 * 32;
   float* dwp = reinterpret_cast<float*>(cx.smem + OFF_DWP);
-  if (direct) {  // per-key sums of the four key quarters
-    dwp[kq * NR + 32 * q + lane] = acc0;
-    dwp[kq * NR + 128 + 32 * q + lane] = acc1;
-  }
+  dwp[kq * NR + 32 * q + lane] = acc0;
+  dwp[kq * NR + 128 + 32 * q + lane] = acc1;
   if (!WAIT(&cx.bars->dqfull, i & 1)) return;
+  if (tdz == 0) TRACE(EV_EPI_A, i);
   tc_fence_after();
   const int d = 32 * q + lane;  // TMEM lane = column of dQ
   const float sc = pow2f(-c) * p.sm_scale;  // a power of two times s: exact while it stays normal
   const int r = kq;             // dQ columns 64kq .. 64kq+63: the heads of row kq
-  const bool rowok = r < Rb;
+  const bool ok = r < Rb && d < p.D;
 #pragma unroll 1
-  for (int cc = 0; cc < 4; ++cc) {
-    float v[16];
-    tmem_ld16(cx.tmem + ((uint32_t)(32 * q) << 16) + TM_DQ + 64 * kq + 16 * cc, v);
-    tmem_wait_ld_dep16(v);
-    if (cc == 3) {
+  for (int cp = 0; cp < 2; ++cp) {  // two 16-column loads in flight at a time
+    float v[2][16];
+    const uint32_t ta = cx.tmem + ((uint32_t)(32 * q) << 16) + TM_DQ + 64 * kq + 32 * cp;
+    tmem_ld16(ta, v[0]);
+    tmem_ld16(ta + 16, v[1]);
+    tmem_wait_ld_dep16(v[0]);
+    tmem_wait_ld_dep16(v[1]);
+    if (cp == 1) {
       tc_fence_before();
       mbar_arrive(&cx.bars->dqempty);
     }
-    const int h0 = 16 * cc;
-    const long long e0 = ((long long)(row0 + r) * p.H + h0) * p.D + d;
-    if (rowok && d < p.D) {
-      if (p.dq16) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (h0 + j < p.H) p.dq16[e0 + (long long)j * p.D] = to_bf16(v[j] * sc);
-      } else {
+    for (int u = 0; u < 2; ++u) {
+      const int h0 = 32 * cp + 16 * u;
+      const long long e0 = ((long long)(row0 + r) * p.H + h0) * p.D + d;
+      if (ok) {
+        if (p.dq16) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (h0 + j < p.H) p.dq[e0 + (long long)j * p.D] = v[j] * sc;
-      }
-    }
-    if (!direct) {
-      // q[r,h,d] dQraw[r,h,d] for this lane's d, then summed over the warp's
-      // 32 columns d: four exchange steps and a last add leave head h0 + l
-      // summed in lanes l and l + 16
+          for (int j = 0; j < 16; ++j)
+            if (h0 + j < p.H) p.dq16[e0 + (long long)j * p.D] = to_bf16(v[u][j] * sc);
+        } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const bool on = rowok && d < p.D && h0 + j < p.H;
-        const float qv = on ? __uint_as_float((uint32_t)__ldg(p.q + e0 + (long long)j * p.D) << 16) : 0.f;
-        v[j] *= qv;
-      }
-#pragma unroll
-      for (int step = 0; step < 4; ++step) {
-        const int o = 16 >> step, nn = 8 >> step;
-        const bool upper = (lane & (o >> 1)) != 0;
-#pragma unroll
-        for (int k = 0; k < nn; ++k) {
-          const float send = upper ? v[k] : v[k + nn];
-          const float keep = upper ? v[k + nn] : v[k];
-          v[k] = keep + __shfl_xor_sync(FULL, send, o >> 1);
+          for (int j = 0; j < 16; ++j)
+            if (h0 + j < p.H) p.dq[e0 + (long long)j * p.D] = v[u][j] * sc;
         }
       }
-      v[0] += __shfl_xor_sync(FULL, v[0], 16);
-      if (lane < 16) dwp[q * NR + r * kHP + h0 + lane] = v[0];
     }
   }
   mbar_arrive(&cx.bars->dwbar);
+  if (tdz == 0) TRACE(EV_EPI_B, i);
   if (!WAIT(&cx.bars->dwbar, i & 1)) return;
   if (tdz < NR) {
     const int rr = tdz >> 6, h = tdz & 63;
     if (rr < Rb && h < p.H) {
-      // the four partials in a fixed order
+      // the four key quarters' partials in a fixed order
       const float s4 = ((dwp[tdz] + dwp[NR + tdz]) + dwp[2 * NR + tdz]) + dwp[3 * NR + tdz];
-      // thread tdz holds w of (r,h) = tdz: buffer half tdz / 128
-      const float dwv = (direct ? s4 : s4 / ((tdz < 128 ? wv0 : wv1) * pow2f(c))) * p.sm_scale;
+      const float dwv = s4 * p.sm_scale;
       const long long e = (long long)(row0 + rr) * p.H + h;
       if (p.dw16)
         p.dw16[e] = to_bf16(dwv);
@@ -603,6 +526,7 @@ __device__ void dz_epilogue(const BParams& p, const Ctx& cx, int row0, int Rb, i
         p.dw[e] = dwv;
     }
   }
+  if (tdz == 0) TRACE(EV_EPI_C, i);
 }
 
 __device__ void dz_role(const BParams& p, const Ctx& cx) {
@@ -621,7 +545,7 @@ __device__ void dz_role(const BParams& p, const Ctx& cx) {
   for (int g = 0;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&B->mfull[ms], (g / MST) & 1)) return;
-    const int flags = cx.hdr[ms].flags, c = cx.hdr[ms].c, direct = cx.hdr[ms].direct;
+    const int flags = cx.hdr[ms].flags, c = cx.hdr[ms].c;
     if (flags & F_FIRST) {
       ++i;
       if (!WAIT(&B->qfull, i & 1)) return;
@@ -640,7 +564,7 @@ __device__ void dz_role(const BParams& p, const Ctx& cx) {
       if (tdz == 0) TRACE(x == 0 ? EV_DZ_ZA : EV_DZ_ZB, g);
       tc_fence_after();
       uint32_t pk[16];
-      float ad = 0.f;  // direct dW: this tile's sum
+      float ad = 0.f;  // dW: this tile's sum of dI relu(z)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {  // keys 16hh .. 16hh+15 of the thread's 32
         float z[16];
@@ -661,7 +585,7 @@ __device__ void dz_role(const BParams& p, const Ctx& cx) {
             const float v0 = z0 > 0.f ? __uint_as_float((uint32_t)t2) : 0.f;
             const float v1 = z1 > 0.f ? __uint_as_float((uint32_t)(t2 >> 32)) : 0.f;
             pk[8 * hh + 2 * j4 + e2] = pack_half2(v0, v1);
-            if (direct) ad = fmaf(dA, fmaxf(z0, 0.f), fmaf(dB, fmaxf(z1, 0.f), ad));
+            ad = fmaf(dA, fmaxf(z0, 0.f), fmaf(dB, fmaxf(z1, 0.f), ad));
           }
         }
       }
@@ -685,19 +609,29 @@ __device__ void dz_role(const BParams& p, const Ctx& cx) {
     fence_proxy_async_smem();
     mbar_arrive(&B->dzfull);
     if (tdz == 0) TRACE(EV_DZ_DONE, g);
-    if (flags & F_LAST) dz_epilogue(p, cx, row0, Rb, c, direct, i, acc0, acc1, wv0, wv1);
+    if (flags & F_LAST) dz_epilogue(p, cx, row0, Rb, c, i, acc0, acc1);
     if (flags & F_END) return;
   }
 }
 
 // ------------------------------------------------------------ dK group ----
 // dK warp w (0..7): TMEM lane quarter qw = w % 4 (32 columns d), entries
-// 64*(w/4) .. +63 of the tile in two chunks of 32.
+// 64*(w/4) .. +63 of the tile in two chunks of 32.  (Straight from TMEM,
+// lane l holds column d of each entry, so each entry's 32 columns could go
+// out as one whole-line scalar reduction per warp instruction; built and
+// measured, that made the anchor's gemm stage 1106 us against 854: four
+// times the reduction instructions per tile held back the dK warps.  The
+// transpose through shared memory lets one 16-byte vector reduction per lane
+// cover four whole lines.)
 __device__ void dk_role(const BParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3;
   const int kg = (threadIdx.x - W_DK0 * 32) >> 7;
   float* stage = reinterpret_cast<float*>(cx.smem + OFF_DKST) + ((threadIdx.x >> 5) - W_DK0) * 512;
   Bars* B = cx.bars;
+  // the ids' bound: rows of u (deterministic mode) or keys of a batch
+  const int idmax = p.u ? (int)(p.dense ? (long long)p.B * p.dense_batch_entries - 1
+                                        : p.nblocks * min((long long)p.S_k, (long long)R * p.L) - 1)
+                        : p.S_k - 1;
   for (long long g = 0;; ++g) {
     const int ms = (int)(g % MST);
     if (!WAIT(&B->mfull[ms], (g / MST) & 1)) return;
@@ -714,9 +648,9 @@ __device__ void dk_role(const BParams& p, const Ctx& cx) {
       if (ch * 32 >= count) break;  // uniform: the remaining entries are padding
       const int nrow = min(32, count - ch * 32);
       if (p.u)
-        dk_chunk_tmem<false>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage);
+        dk_chunk_tmem<false>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage, idmax);
       else
-        dk_chunk_tmem<true>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage);
+        dk_chunk_tmem<true>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage, idmax);
     }
     tc_fence_before();
     mbar_arrive(&B->dkempty);

@@ -53,6 +53,8 @@ struct GemmArgs {
   uint16_t* dw16;        // if set: dw likewise
   uint16_t* dk16;        // if set: bf16 copy of the final dk, written after it
   float sm_scale;        // logit scale s (> 0; 0 reads as 1): dq, dw, dk are s times the unscaled results
+  cudaStream_t side;     // a second stream of the device, forked from and joined to the call's stream
+  cudaEvent_t ev_fork, ev_join;
 };
 
 // Workspace of the gemm stage (indexer_bwd_gemm and the one-call forms).
@@ -61,11 +63,13 @@ struct GemmArgs {
 // stored as tile records of 128 entries:
 //   int key[128] | float dis[kBlkRows][128] | int pos[128] (deterministic)
 // (dis[r][e]: the sum of dI over row r's slots selecting key e, 0 when row r
-// does not select it; padding entries have key S_k and dis 0).
+// does not select it; padding entries have key S_k and dis 0; pos[e]: the
+// entry's row of u in key order).
 struct WsLayout {
   size_t sched;      // 256 bytes: [0] the gemm kernel's block counter, [1] the union pass's CTA counter
   size_t k16;        // fp16 copy of k, [B, S_k + 1, 128]
-  size_t binfo;      // sparse: int4 per block {tiles, dz scale exponent, entries, 0}
+  size_t qimg;       // per block: its q rows as the gemm kernel's fp16 Q operand image (64 KB)
+  size_t binfo;      // int4 per block {tiles, dz scale exponent, entries, 0}
   size_t border;     // sparse: the blocks in descending tile count (processing order)
   size_t rec;        // sparse: tile records [nblocks][tcap][rstride bytes]
   size_t u;          // deterministic: per-entry dK rows [entries_cap, D] fp32, in key order
@@ -81,8 +85,9 @@ struct WsLayout {
 };
 WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic, int dense);
 
-// The blocked gemm stage (blk.cu): fp16 copy of k, the union pass (sparse),
-// the deterministic sort (det.cu), the gemm kernel, the segment sum.
+// The blocked gemm stage (blk.cu): fp16 copy of k, the q images, the union
+// pass (sparse) or the scale pass (dense), the deterministic sort (det.cu),
+// the gemm kernel, the segment sum.
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 
 // Deterministic mode (det.cu): the key sort of the blocks' entries (sparse) or

@@ -1,6 +1,6 @@
 // Device and host helpers shared by the gemm-stage kernels (the blocked
-// kernel in blk.cu and the per-row kernel in gemm.cu): bounded-wait macros,
-// scale helpers, the transposed dK reduction and the launch wrapper.
+// kernel in blk_pipe.cuh and the per-row kernel in gemm.cu): scale helpers,
+// the drain wait, the transposed dK reduction and the launch wrapper.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -82,10 +82,11 @@ __device__ __forceinline__ void dk_chunk(float* base, const int* ids, const floa
 
 // The same for 32 entries read straight from TMEM, 16 columns at a time (half
 // the live registers of dk_chunk): ta addresses the warp's lane quarter at
-// the chunk's first column.
+// the chunk's first column; the ids are clamped to idmax, so every address
+// stays inside the destination whatever a record holds.
 template <bool RED>
 __device__ __forceinline__ void dk_chunk_tmem(float* base, const int* ids, uint32_t ta, int nrow, float sc, int D,
-                                              int dblk, float* stage) {
+                                              int dblk, float* stage, int idmax) {
   const int lane = threadIdx.x & 31;
   const int rsub = lane >> 3, c4 = (lane & 7) * 4;
   const bool con = dblk + c4 < D;
@@ -96,7 +97,7 @@ __device__ __forceinline__ void dk_chunk_tmem(float* base, const int* ids, uint3
     tmem_ld16(ta + hf * 16, v);
     int idv[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) idv[k] = ids[hf * 16 + rsub + 4 * k];
+    for (int k = 0; k < 4; ++k) idv[k] = min((unsigned)ids[hf * 16 + rsub + 4 * k], (unsigned)idmax);
     tmem_wait_ld_dep16(v);
 #pragma unroll
     for (int e = 0; e < 16; ++e) stage[e * 32 + lane] = v[e] * sc;

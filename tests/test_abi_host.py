@@ -49,15 +49,19 @@ def test_status_strings(lib):
 def test_workspace_sizes(lib):
     a = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_ATOMIC)
     nb, tcap = 8192 // 4, 4096 // 128       # blocks of four query rows; records per block (min(S_k, 4*topk) keys)
-    # counters + fp16 copy of k (+ a zero row) + per-block info and order + the tile records
-    assert a == 256 + 4097 * 128 * 2 + nb * 16 + nb * 4 + nb * tcap * 2560
+    qimg = nb * 65536                        # per block: its q rows as the fp16 Q operand image
+    # counters + fp16 copy of k (+ a zero row) + q images + per-block info and order + the tile records
+    assert a == 256 + 4097 * 128 * 2 + qimg + nb * 16 + nb * 4 + nb * tcap * 2560
     d = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_DETERMINISTIC)
     u = nb * 4096 * 128 * 4                  # one dK row per (block, key) entry at most
-    assert d == a + nb * tcap * 512 + u + (nb // 2) * 4096 * 4 + ((4096 + 1) * 4 + 255) // 256 * 256
-    assert ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 0) == 256 + 4097 * 128 * 2
+    keyoff = ((4096 + 1) * 4 + 255) // 256 * 256
+    assert d == a + nb * tcap * 512 + u + (nb // 2) * 4096 * 4 + keyoff
+    dnb = 4096 // 4
+    dense = 256 + 4097 * 128 * 2 + dnb * 65536 + dnb * 16
+    assert ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 0) == dense
     # dense deterministic: block j holds keys [0, 4j + 4): sum over j of 4(j + 1) dK rows
     dd = ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 1)
-    assert dd == 256 + 4097 * 128 * 2 + 4 * (1024 * 1025 // 2) * 128 * 4 + ((4096 + 1) * 4 + 255) // 256 * 256
+    assert dd == dense + 4 * (1024 * 1025 // 2) * 128 * 4 + keyoff
     # unsupported shapes report 0
     assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 65, 128, 4, 0) == 0
     assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 4, 12, 4, 0) == 0

@@ -1,6 +1,7 @@
 """Full-size workloads (the shapes the benchmark times, in the same launch
-configuration) against the full fp64 oracle: every element of dI, dQ, dW and
-dK is compared.  The oracle's forward supplies index_score."""
+configuration, and two points of the top-k sweep with uniform lengths)
+against the full fp64 oracle: every element of dI, dQ, dW and dK is
+compared.  The oracle's forward supplies index_score."""
 import time
 
 import numpy as np
@@ -27,7 +28,8 @@ def full_case(name):
     return _cache[name]
 
 
-@pytest.mark.parametrize("name", ["sq4096_topk512", "anchor", "window_topk2048", "dense_s4096"])
+@pytest.mark.parametrize("name", ["sq4096_topk512", "anchor", "window_topk2048", "dense_s4096", "uniform_topk128",
+                                  "uniform_topk384"])
 def test_full_size_matches_oracle(name):
     wl, x, ref, secs = full_case(name)
     modes = [ibwd.IBWD_DK_ATOMIC, ibwd.IBWD_DK_DETERMINISTIC]

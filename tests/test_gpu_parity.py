@@ -110,19 +110,49 @@ def test_whole_call_equals_the_pair_of_calls(cases, name):
         assert np.array_equal(u.view(np.int32), v.view(np.int32))
 
 
-@pytest.mark.parametrize("topk", [1364, 1368])
-def test_deterministic_layouts_at_the_stage_limit(topk):
-    # 12 bytes a slot (ids, dI, sorted positions) fill the gemm kernel's 16 KB
-    # row stage at topk 1364: the dK rows go to u in key order (position
-    # mode); at 1368 they go by slot and are summed through the key-order slot
-    # list (slot mode).  Both against the oracle, both bitwise run to run.
-    wl = W(f"det_layout_{topk}", 1, 4, 32, 48, 4096, topk, "causal", 23)
+@pytest.mark.parametrize("mode", [ibwd.IBWD_DK_ATOMIC, ibwd.IBWD_DK_DETERMINISTIC])
+def test_dk_across_a_wide_dynamic_range(mode):
+    # Rows 0..191 select keys below 160 only and carry dI at 2^-24 of the
+    # other rows', which select keys from 256 up; the dz scale is per block,
+    # so the small rows' keys keep their own relative accuracy, element by
+    # element, in both dK modes.
+    wl = W("fixed_range", 1, 8, 64, 512, 512, 64, "causal", 29)
     x = case_inputs(wl)
-    ref = oracle_all(wl, x)
-    runs = [gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_DETERMINISTIC) for _ in range(2)]
-    assert_close(*runs[0][1:], ref[1:], tag=f"det topk {topk}")
-    for a, b in zip(runs[0], runs[1]):
-        assert np.array_equal(a.view(np.int32), b.view(np.int32))
+    rng = np.random.default_rng(29)
+    small = np.arange(wl.S_q) < 192
+    idx = np.where(small[:, None], rng.integers(0, 160, (wl.S_q, wl.topk)),
+                   rng.integers(256, wl.S_k, (wl.S_q, wl.topk))).astype(np.int32)[None]
+    x["idx"] = idx
+    x["I"] = oracle.forward_sparse(x["q"], x["k"], x["w"], idx, wl.S_k).astype(np.float32)
+    dI = oracle.score_grad_sparse(x["I"], x["attn"], idx, wl.S_k).astype(np.float32)
+    dI[0, small] *= np.float32(2.0 ** -24)
+    ref = oracle.gemm_sparse(x["q"], x["k"], x["w"], dI.astype(np.float64), idx, wl.S_k)
+    dq, dw, dk = gpu_gemm(wl, x, dI, mode, idx=idx)
+    keys = np.unique(idx[0, small])
+    assert keys.max() < 160 and keys.size > 100
+    ks, rk = dk[0, keys], ref[2][0, keys]
+    assert np.abs(ks - rk).max() <= 1e-3 * np.abs(rk).max()
+    assert_close(dq, dw, dk, ref, tag="wide range")
+
+
+@pytest.mark.parametrize("mode", [ibwd.IBWD_DK_ATOMIC, ibwd.IBWD_DK_DETERMINISTIC])
+def test_dk_with_large_q_and_dI(mode):
+    # q entries near the fp16 limit and a large dI: the fp16 operands and the
+    # dz scale keep every value in range, the results within the tolerance
+    wl = W("fixed_large", 1, 16, 64, 200, 300, 96, "causal", 30)
+    x = case_inputs(wl)
+    q = synth.bf16_to_f32(x["q"]).astype(np.float32)
+    q[0, 7, 3, :8] = 60000.0
+    x["q"] = f32_to_bf16_bits(q)
+    dI = (oracle.score_grad_sparse(x["I"], x["attn"], x["idx"], wl.S_k) * 1e6).astype(np.float32)
+    ref = oracle.gemm_sparse(x["q"], x["k"], x["w"], dI.astype(np.float64), x["idx"], wl.S_k)
+    dq, dw, dk = gpu_gemm(wl, x, dI, mode)
+    assert_close(dq, dw, dk, ref, tag="large q and dI")
+
+
+def f32_to_bf16_bits(x):
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
 
 
 @pytest.mark.parametrize("name", ["multi_tile_ragged", "window_small", "odd_shapes", "dense_small", "dense_odd",
