@@ -49,6 +49,8 @@ METRIC = "indexer-bwd kernel µs & TFLOP/s (frac of bf16 peak), H64 D128 Sq8192 
 GEMM_FILES = ("blk.cu", "blk.h", "blk_pipe.cuh", "blk_pipe.cu", "kcommon.cuh", "ptx.cuh", "internal.h")
 SCORE_GRAD_FILES = ("score_grad.cu",)
 PROFILED_TRAFFIC = {
+    # k_to_f16 + union + q_image + blk kernels of one gemm-stage call
+    ("anchor", "atomic", "gemm_stage"): ("c7be96e67eacd994b938375dc80eddddb7643259fe956bafa42f79b0cc9225a8", 1.06e6 + 83.91e6 + 222.07e6 + 423.15e6),
     ("anchor", "atomic", "score_grad"): ("32716e0bdb141dfa50987a5d3f34f07eb40acf8a602b202185531f24332fc497", 100.694528e6 + 4.471808e6),
 }
 
