@@ -5,6 +5,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdlib>
+#include <cstring>
 
 #include "blk.h"
 
@@ -30,6 +31,7 @@ struct UParams {
   int W;       // key window per pass (multiple of 1024)
   int dcap;    // per-row capacity of the dedup arrays: min(L, W)
   int staged;  // the block's ids and dI rows are copied into shared memory (Lp = L rounded up to 4)
+  const unsigned* select;  // if set: the pass runs only when *select == 0 (1 selects the per-row kernel)
 };
 
 // Exclusive prefix of the popcounts of n words (n a multiple of 32), by one
@@ -99,6 +101,10 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   __shared__ float s_wmax[4], s_dmax[4][R];
   __shared__ int s_last;
   griddep_launch_dependents();
+  if (p.select) {  // the flag is written by the kernel before
+    griddep_wait();
+    if (__ldcg(p.select) != 0u) return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long b = blockIdx.x;
   const int bb = (int)(b / p.nbpb), jb = (int)(b % p.nbpb);
@@ -306,6 +312,86 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
     p.border[atomicAdd(&cur[min(NBUCKET - 1, __ldcg(&p.binfo[x].x))], 1)] = (int)x;
 }
 
+// Words of the per-call counter block used by the kernel choice.
+constexpr int SEL_FLAG = 2;      // 1: the per-row kernel serves the call, 0: the blocked one
+constexpr int SEL_DONE = 3;      // CTA counter of select_kernel
+constexpr int SEL_SUMS = 4;      // three 64-bit sums: union tiles, row tiles, rows
+constexpr int SCHED_ZERO = 10;   // words the k conversion kernel zeroes
+
+// Cost model of the two gemm paths, in thousands of cycles per SM, fitted to
+// their measured times (uniform top-k 128 ... 2048 over 4096 keys, the causal
+// top-1024 rows over 4096 keys, causal top-512 rows on S_q = S_k = 4096): the
+// blocked path pays per block of four rows (its union pass, Q copy,
+// block-end epilogue) plus per 128-key union tile; the per-row kernel pays
+// per row plus per 128-slot tile of the row.  Its dK reductions collide when
+// rows share keys (causal prefixes), which the per-tile costs do not see: it
+// is chosen only when its estimate is below the blocked one by a margin (the
+// causal top-512 rows lose to the blocked kernel at an estimate 13 % lower;
+// uniform top-128 rows win at 18 % lower).
+constexpr double COST_BLOCK = 30.0, COST_UNION_TILE = 7.82, COST_ROW = 9.08, COST_ROW_TILE = 3.9;
+constexpr double ROWS_MARGIN = 1.15;
+
+// Which gemm kernel serves an atomic call without options: on a strided
+// sample of blocks, the union's tiles against the rows' own tiles, through
+// the cost model above.  One CTA of four warps per sampled block (warp r on
+// row r), a bitmap of the keys in shared memory (S_k <= 65536); the last CTA
+// writes the choice.  force >= 0 imposes it (a test switch).
+__global__ void __launch_bounds__(128) select_kernel(const int32_t* __restrict__ idx, int S_q, int S_k, int L,
+                                                     int nbpb, long long stride, unsigned* __restrict__ sched,
+                                                     int force) {
+  extern __shared__ uint32_t sbm[];  // ceil(S_k / 32) words
+  __shared__ unsigned s_cnt[4], s_pop[4];
+  griddep_wait();  // the counter block is zeroed by the kernel before
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int words = (S_k + 31) >> 5;
+  for (int i = tid; i < words; i += 128) sbm[i] = 0u;
+  __syncthreads();
+  const long long b = blockIdx.x * stride;
+  const int batch = (int)(b / nbpb), t0 = (int)(b % nbpb) * R;
+  const int Rb = min(R, S_q - t0);
+  unsigned cnt = 0;
+  if (warp < Rb) {
+    const int32_t* ir = idx + ((long long)batch * S_q + t0 + warp) * L;
+    for (int j = lane; j < L; j += 32) {
+      const int s = __ldg(ir + j);
+      if ((unsigned)s < (unsigned)S_k) {
+        atomicOr(&sbm[s >> 5], 1u << (s & 31));
+        ++cnt;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(FULL, cnt, o);
+  __syncthreads();
+  unsigned pop = 0;
+  for (int i = tid; i < words; i += 128) pop += __popc(sbm[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) pop += __shfl_xor_sync(FULL, pop, o);
+  if (lane == 0) {
+    s_cnt[warp] = cnt;
+    s_pop[warp] = pop;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned U = s_pop[0] + s_pop[1] + s_pop[2] + s_pop[3];
+    unsigned long long row_tiles = 0;
+    for (int r = 0; r < Rb; ++r) row_tiles += max(1u, (s_cnt[r] + 127u) / 128u);
+    unsigned long long* sums = reinterpret_cast<unsigned long long*>(sched + SEL_SUMS);
+    atomicAdd(sums, (unsigned long long)max(1u, (U + 127u) / 128u));
+    atomicAdd(sums + 1, row_tiles);
+    atomicAdd(sums + 2, (unsigned long long)Rb);
+    __threadfence();
+    if (atomicAdd(sched + SEL_DONE, 1u) == gridDim.x - 1) {
+      __threadfence();
+      const double ut = (double)__ldcg(sums), rt = (double)__ldcg(sums + 1), nr = (double)__ldcg(sums + 2);
+      const double t_blocked = gridDim.x * COST_BLOCK + ut * COST_UNION_TILE;
+      const double t_rows = nr * COST_ROW + rt * COST_ROW_TILE;
+      sched[SEL_FLAG] = force >= 0 ? (unsigned)force : (ROWS_MARGIN * t_rows < t_blocked ? 1u : 0u);
+    }
+  }
+  griddep_launch_dependents();
+}
+
 struct QImg {  // the Q operand images of every block
   const uint16_t* q;
   uint8_t* img;
@@ -324,7 +410,8 @@ __device__ __forceinline__ bool q_image_at(const QImg& qi, long long x) {
 
 // The q images, on the side stream beside the union pass (or the dense
 // scale pass).
-__global__ void q_image_kernel(const QImg qi, unsigned* __restrict__ status) {
+__global__ void q_image_kernel(const QImg qi, unsigned* __restrict__ status, const unsigned* __restrict__ select) {
+  if (select && __ldcg(select) != 0u) return;  // the per-row kernel serves this call
   const long long nq = qi.nblocks * (NR * 16);
   const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
@@ -462,6 +549,17 @@ bool test_shallow_pipeline() {
   return v && v[0] == '1';
 }
 
+// Test of both gemm kernels on calls the choice covers:
+// IBWD_TEST_GEMM_PATH=rows imposes the per-row kernel, =blocked the blocked
+// one (no choice is made).  -1: the cost model decides; 0: blocked; 1: rows.
+int test_gemm_path() {
+  const char* v = std::getenv("IBWD_TEST_GEMM_PATH");
+  if (!v) return -1;
+  if (std::strcmp(v, "rows") == 0) return 1;
+  if (std::strcmp(v, "blocked") == 0) return 0;
+  return -1;
+}
+
 }  // namespace
 
 cudaError_t launch_k_to_f16(const uint16_t* k, __half* k16, int B, int S_k, int D, unsigned* sched, int nsched,
@@ -526,11 +624,26 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   unsigned* sched = reinterpret_cast<unsigned*>(ws + lay.sched);
   uint8_t* qimg = reinterpret_cast<uint8_t*>(ws + lay.qimg);
   int4* binfo = reinterpret_cast<int4*>(ws + lay.binfo);
+  // The per-row kernel can serve atomic sparse calls without options (and
+  // keys that fit select_kernel's bitmap); select_kernel chooses on the
+  // device, and every kernel of the path that is not chosen exits at once.
+  const int forced = test_gemm_path();
+  const bool choose = !a.deterministic && !dense && !a.ids_global && !a.dq16 && !a.dw16 && !a.dk16 &&
+                      a.sm_scale == 1.f && a.S_k <= 65536 && forced != 0;
+  const unsigned* select = choose ? sched + SEL_FLAG : nullptr;
   // programmatic only right after this library's score-grad kernel: the
   // kernel reads k before it waits for its predecessor
-  cudaError_t e =
-      launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 2, a.status, a.after_score_grad != 0, a.num_sms, st);
+  cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, SCHED_ZERO, a.status, a.after_score_grad != 0,
+                                  a.num_sms, st);
   if (e != cudaSuccess) return e;
+  if (choose) {
+    const long long nsample = std::min<long long>(lay.nblocks, 256);
+    const long long stride = lay.nblocks / nsample;
+    const size_t sh = (size_t)((a.S_k + 31) / 32) * 4;
+    e = launch_ex(select_kernel, (unsigned)nsample, 128u, sh, st, true, static_cast<const int32_t*>(a.idx), a.S_q,
+                  a.S_k, a.L, lay.nbpb, stride, sched, forced);
+    if (e != cudaSuccess) return e;
+  }
   // the q images on the side stream: the union pass (or the dense scale
   // pass) is latency-bound and leaves the memory system mostly idle, so the
   // two overlap; the gemm kernel waits for both
@@ -542,7 +655,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     const long long n = lay.nblocks * (NR * 16);
     // two CTAs per SM: with the union pass's four, the register file holds both
     const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 2LL * a.num_sms));
-    q_image_kernel<<<blocks, 256, 0, a.side>>>(qi, a.status);
+    q_image_kernel<<<blocks, 256, 0, a.side>>>(qi, a.status, select);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaEventRecord(a.ev_join, a.side);
     if (e != cudaSuccess) return e;
@@ -565,6 +678,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     u.tcap = lay.tcap;
     u.rstride = lay.rstride;
     u.ids_global = a.ids_global;
+    u.select = select;
     union_geometry(a.S_k, a.L, u.W, u.dcap, u.staged);
     const size_t sh = union_smem_bytes(u.W, u.dcap, a.L, u.staged);
     // (its static arrays come on top of the dynamic bytes: always raise the limit)
@@ -605,6 +719,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const unsigned long long test_ns = test_timeout_ns();
   p.wait_ns = test_ns ? test_ns : 2000000000ull;
   p.test_stall = test_ns != 0;
+  p.select = select;
   p.B = a.B;
   p.S_q = a.S_q;
   p.S_k = a.S_k;
@@ -619,6 +734,12 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const int grid = (int)std::min<long long>(a.num_sms, lay.nblocks);
   e = test_shallow_pipeline() ? launch_blk_pipe<1, 2>(p, grid, st) : launch_blk_pipe<2, 4>(p, grid, st);
   if (e != cudaSuccess) return e;
+  if (choose) {
+    // the per-row kernel: runs only if chosen (then the blocked kernel has
+    // exited at once); the row counter is the block counter's word
+    e = launch_gemm_rows_kernel(a, k16, sched, select, st);
+    if (e != cudaSuccess) return e;
+  }
   if (a.deterministic) {
     e = launch_det_segsum(a, lay, st);
     if (e != cudaSuccess) return e;

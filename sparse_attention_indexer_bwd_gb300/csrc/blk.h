@@ -84,6 +84,7 @@ struct BParams {
   unsigned long long drain_ns;  // limit of the drains of issued copies and MMAs before exit
   float sm_scale;               // logit scale s > 0: every output is s times the unscaled one
   int test_stall;               // test of the timeout path: the record producer publishes nothing
+  const unsigned* select;       // if set: the kernel runs only when *select == 0 (1 selects the per-row kernel)
   int B, S_q, S_k, H, D, L;
   int dense, nbpb, tcap, rstride;
   long long dense_batch_entries;  // deterministic dense: entries (rows of u) per batch

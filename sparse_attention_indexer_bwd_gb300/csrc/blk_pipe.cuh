@@ -713,8 +713,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
   // dependent launch); the inputs it wrote are read only from here on
   griddep_wait();
   if (threadIdx.x == 0) TRACE_CTA(0, clock64());
+  const bool run = p.select == nullptr || __ldcg(p.select) == 0u;
 
-  if (warp < W_SCAN) {
+  if (!run) {
+    // the per-row kernel serves this call
+  } else if (warp < W_SCAN) {
     gather_role(p, cx);
   } else if (warp == W_SCAN) {
     scan_role(p, cx);

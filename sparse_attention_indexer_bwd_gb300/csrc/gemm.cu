@@ -109,6 +109,7 @@ struct KParams {
   unsigned long long wait_ns;
   int B, S_q, S_k, H, D, L;
   int staged;  // rows are staged in shared memory by bulk copies
+  const unsigned* select;  // if set: the kernel runs only when *select == 1 (written by an earlier kernel)
 };
 
 __device__ __forceinline__ long long row_of(long long u, const KParams& p) {
@@ -672,8 +673,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
   tc_fence_after();
   cx.tmem = *tmem_slot;
   griddep_wait();  // the fp16 copy of k is written by the kernel before
+  const bool run = p.select == nullptr || __ldcg(p.select) == 1u;
 
-  if (warp < W_SCAN) {
+  if (!run) {
+    // another kernel serves this call
+  } else if (warp < W_SCAN) {
     gather_role(p, cx);
   } else if (warp == W_SCAN) {
     scan_role(p, cx);
@@ -733,10 +737,16 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t st) {
   char* ws = static_cast<char*>(a.ws);
   unsigned* sched = reinterpret_cast<unsigned*>(ws);
   __half* k16 = reinterpret_cast<__half*>(ws + 256);
+  cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 1, a.status, false, a.num_sms, st);
+  if (e != cudaSuccess) return e;
+  return launch_gemm_rows_kernel(a, k16, sched, nullptr, st);
+}
+
+cudaError_t launch_gemm_rows_kernel(const GemmArgs& a, const __half* k16, unsigned* counter, const unsigned* select,
+                                    cudaStream_t st) {
   cudaError_t e = prepare_gemm_rows();
   if (e != cudaSuccess) return e;
-  e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, 1, a.status, false, a.num_sms, st);
-  if (e != cudaSuccess) return e;
+  unsigned* sched = counter;
   KParams p{};
   p.q = a.q;
   p.k16 = k16;
@@ -760,6 +770,7 @@ cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t st) {
   // rows are staged in shared memory when they fit and are 16-byte aligned
   p.staged = 2 * (size_t)a.L * 4 <= ROW_BYTES && a.L % 4 == 0 && (uintptr_t)a.dI % 16 == 0 &&
              (uintptr_t)a.idx % 16 == 0;
+  p.select = select;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
   return launch_ex(gemm_rows_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
 }

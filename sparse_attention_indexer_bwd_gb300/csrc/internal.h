@@ -108,6 +108,11 @@ cudaError_t launch_k_to_f16(const uint16_t* k, __half* k16, int B, int S_k, int 
 size_t rows_workspace_bytes(int B, int S_k);
 cudaError_t prepare_gemm_rows();  // per device: the kernel's shared-memory attribute
 cudaError_t launch_gemm_rows(const GemmArgs& a, cudaStream_t st);
+// The per-row kernel alone on an fp16 copy of k made by the caller, its row
+// counter zeroed by the caller; with select set it runs only when *select
+// is 1 at its start (otherwise it exits at once).
+cudaError_t launch_gemm_rows_kernel(const GemmArgs& a, const __half* k16, unsigned* counter, const unsigned* select,
+                                    cudaStream_t st);
 
 struct FwdArgs {
   const uint16_t* q;     // bf16 [rows, H, D]

@@ -2,6 +2,9 @@
 through the C ABI, the oracle side, and the acceptance metrics."""
 from __future__ import annotations
 
+import contextlib
+import os
+
 import numpy as np
 import torch
 
@@ -31,6 +34,21 @@ def rms_rel(got, ref):
 
 def dev():
     return torch.device("cuda:0")
+
+
+@contextlib.contextmanager
+def gemm_path(path):
+    """Imposes the gemm kernel on calls the device-side choice covers (atomic,
+    sparse, no options): "rows" (the per-row kernel) or "blocked"."""
+    old = os.environ.get("IBWD_TEST_GEMM_PATH")
+    os.environ["IBWD_TEST_GEMM_PATH"] = path
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["IBWD_TEST_GEMM_PATH"]
+        else:
+            os.environ["IBWD_TEST_GEMM_PATH"] = old
 
 
 def t_bf16(bits):

@@ -16,7 +16,7 @@ import pytest
 
 import synth
 import sparse_attention_indexer_bwd_gb300 as ibwd
-from gpu_util import TOL_DK, assert_close, case_inputs, gpu_gemm, oracle_all, rms_rel
+from gpu_util import TOL_DK, assert_close, case_inputs, gemm_path, gpu_gemm, oracle_all, rms_rel
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +42,9 @@ def test_shallow_pipeline_is_bitwise_the_production_one(wl, mode):
     x = case_inputs(wl)
     ref = oracle_all(wl, x)
     dI = ref[0].astype(np.float32)
-    deep = gpu_gemm(wl, x, dI, dk_mode=mode)
-    flat = shallow(gpu_gemm, wl, x, dI, dk_mode=mode)
+    with gemm_path("blocked"):
+        deep = gpu_gemm(wl, x, dI, dk_mode=mode)
+        flat = shallow(gpu_gemm, wl, x, dI, dk_mode=mode)
     np.testing.assert_array_equal(flat[0].view(np.int32), deep[0].view(np.int32))
     np.testing.assert_array_equal(flat[1].view(np.int32), deep[1].view(np.int32))
     if mode == ibwd.IBWD_DK_DETERMINISTIC:

@@ -18,7 +18,7 @@ import torch
 import synth
 import sparse_attention_indexer_bwd_gb300 as ibwd
 import oracle
-from gpu_util import assert_close, case_inputs, gpu_gemm, t_bf16, t_f32, t_i32
+from gpu_util import assert_close, case_inputs, gemm_path, gpu_gemm, t_bf16, t_f32, t_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,8 @@ def test_role_wait_timeout_is_reported_and_the_next_call_is_correct(mode):
     x, dI, ref = inputs(wl)
     os.environ["IBWD_TEST_TIMEOUT_NS"] = "1000000"
     try:
-        st = raw_gemm(wl, x, dI, mode)
+        with gemm_path("blocked"):  # the switch stalls the blocked kernel's record producer
+            st = raw_gemm(wl, x, dI, mode)
     finally:
         del os.environ["IBWD_TEST_TIMEOUT_NS"]
     assert st == ibwd.IBWD_ERR_TIMEOUT, ibwd.status_string(st)
