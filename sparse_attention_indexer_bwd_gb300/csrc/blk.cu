@@ -28,6 +28,8 @@ struct UParams {
   unsigned* done;      // CTA counter, zeroed by the k conversion kernel
   long long nblocks;
   int S_q, S_k, H, L, nbpb, tcap, rstride, ids_global;
+  int* hist;   // deterministic mode: per (sort chunk, key) counts of the chunk's blocks holding the key, or nullptr
+  int cpb;     // deterministic mode: sort chunks per batch
   int W;       // key window per pass (multiple of 1024)
   int dcap;    // per-row capacity of the dedup arrays: min(L, W)
   int staged;  // the block's ids and dI rows are copied into shared memory (Lp = L rounded up to 4)
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
       const int ug = base + pf[4 * WW + i] + __popc(m & below);
       char* rb = p.rec + ((long long)b * p.tcap + (ug >> 7)) * p.rstride;
       reinterpret_cast<int*>(rb + REC_KEY)[ug & 127] = w0 + 32 * i + lane;
+      if (p.hist) atomicAdd(p.hist + ((long long)bb * p.cpb + jb / kSortBlocks) * p.S_k + w0 + 32 * i + lane, 1);
       float* dd = reinterpret_cast<float*>(rb + REC_DIS);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
 constexpr int SEL_FLAG = 2;      // 1: the per-row kernel serves the call, 0: the blocked one
 constexpr int SEL_DONE = 3;      // CTA counter of select_kernel
 constexpr int SEL_SUMS = 4;      // three 64-bit sums: union tiles, row tiles, rows
-constexpr int SCHED_ZERO = 10;   // words the k conversion kernel zeroes
+constexpr int SCHED_ZERO = kSchedWords;  // words the k conversion kernel zeroes
 
 // Cost model of the two gemm paths, in thousands of cycles per SM, fitted to
 // their measured times (uniform top-k 128 ... 2048 over 4096 keys, the causal
@@ -472,7 +475,8 @@ __global__ void __launch_bounds__(128) dense_scale_kernel(const float* __restric
 // k nor the workspace), it runs alongside it and waits for it before exiting,
 // so that its own completion implies the score-grad's.
 __global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restrict__ k16, int B, int S_k, int D,
-                                unsigned* __restrict__ sched, int nsched, unsigned* __restrict__ status) {
+                                unsigned* __restrict__ sched, int nsched, unsigned* __restrict__ status,
+                                int* __restrict__ zero32, long long nzero32) {
   griddep_launch_dependents();  // the next kernel may start its prologue
   if (blockIdx.x == 0 && threadIdx.x < nsched) sched[threadIdx.x] = 0u;  // the following kernels' counters
   const long long rows = (long long)B * (S_k + 1);
@@ -491,6 +495,10 @@ __global__ void k_to_f16_kernel(const uint16_t* __restrict__ k, __half* __restri
     *reinterpret_cast<uint4*>(k16 + row * kDP + ch * 8) =
         make_uint4(bf16x2_to_half2(val.x), bf16x2_to_half2(val.y), bf16x2_to_half2(val.z), bf16x2_to_half2(val.w));
   }
+  // the deterministic sort's per-chunk key counts start at zero
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < nzero32;
+       x += (long long)gridDim.x * blockDim.x)
+    zero32[x] = 0;
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, DEV_FP16_RANGE);
   griddep_wait();
 }
@@ -563,10 +571,11 @@ int test_gemm_path() {
 }  // namespace
 
 cudaError_t launch_k_to_f16(const uint16_t* k, __half* k16, int B, int S_k, int D, unsigned* sched, int nsched,
-                            unsigned* status, bool pdl, int num_sms, cudaStream_t st) {
-  const long long n = (long long)B * (S_k + 1) * (kDP / 8);
+                            unsigned* status, bool pdl, int num_sms, cudaStream_t st, int* zero32, long long nzero32) {
+  const long long n = std::max<long long>((long long)B * (S_k + 1) * (kDP / 8), nzero32);
   const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 8LL * num_sms));
-  return launch_ex(k_to_f16_kernel, (unsigned)blocks, 256u, 0, st, pdl, k, k16, B, S_k, D, sched, nsched, status);
+  return launch_ex(k_to_f16_kernel, (unsigned)blocks, 256u, 0, st, pdl, k, k16, B, S_k, D, sched, nsched, status,
+                   zero32, nzero32);
 }
 
 WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic, int dense) {
@@ -633,8 +642,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   const unsigned* select = choose ? sched + SEL_FLAG : nullptr;
   // programmatic only right after this library's score-grad kernel: the
   // kernel reads k before it waits for its predecessor
+  int* hist = (a.deterministic && !dense) ? reinterpret_cast<int*>(ws + lay.hist) : nullptr;
   cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, SCHED_ZERO, a.status, a.after_score_grad != 0,
-                                  a.num_sms, st);
+                                  a.num_sms, st, hist, hist ? lay.nchunks * a.S_k : 0LL);
   if (e != cudaSuccess) return e;
   if (choose) {
     const long long nsample = std::min<long long>(lay.nblocks, 256);
@@ -678,6 +688,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     u.nbpb = lay.nbpb;
     u.tcap = lay.tcap;
     u.rstride = lay.rstride;
+    u.hist = hist;
+    u.cpb = (lay.nbpb + kSortBlocks - 1) / kSortBlocks;
     u.ids_global = a.ids_global;
     u.select = select;
     union_geometry(a.S_k, a.L, u.W, u.dcap, u.staged);

@@ -11,17 +11,16 @@
 // the entry's row there, and
 //   segsum:  dK[s] = sum of the key's rows, in that order.
 // Sparse: per chunk of kSortBlocks blocks, per-key counts (a key appears at
-// most once per block), an exclusive scan over the chunks and over the keys
-// (no position atomics, so the order is fixed), then the positions, written
-// into the tile records.  Dense: block j of a batch holds keys [0, 4j + Rb),
+// most once per block; the union pass counts them as it writes the records),
+// an exclusive scan over the chunks and over the keys (no position atomics,
+// so the order is fixed), then the positions, written into the tile records.  Dense: block j of a batch holds keys [0, 4j + Rb),
 // so the positions have a closed form (the gemm kernel computes them) and
 // only the CSR offsets are filled here.
 // The result is bitwise identical run to run and overwrites dK.
 #include <algorithm>
 #include <atomic>
 
-#include "internal.h"
-#include "ptx.cuh"
+#include "kcommon.cuh"
 
 namespace ibwd {
 namespace {
@@ -40,21 +39,31 @@ __device__ __forceinline__ int* rec_field(const DetP& d, long long b, int e, int
   return reinterpret_cast<int*>(d.rec + (b * d.tcap + (e >> 7)) * d.rstride + off) + (e & 127);
 }
 
-// Counts, per chunk of CB blocks, how many of its blocks hold each key.
-__global__ void __launch_bounds__(256) hist_kernel(const DetP d, int* __restrict__ hist) {
-  extern __shared__ int sh[];
-  const int cpb = (d.nbpb + CB - 1) / CB;  // chunks per batch
-  const long long chunk = blockIdx.x;
-  const int bb = (int)(chunk / cpb), j0 = (int)(chunk % cpb) * CB;
-  for (int s = threadIdx.x; s < d.S_k; s += blockDim.x) sh[s] = 0;
+// Exclusive scan of the per-key totals into CSR offsets, by one CTA of 1024
+// threads (the totals were written by other CTAs: read past L1).
+__device__ __forceinline__ void keyscan(int* __restrict__ key_start, long long n) {
+  __shared__ int part[1024];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  for (int jb = j0; jb < min(d.nbpb, j0 + CB); ++jb) {
-    const long long b = (long long)bb * d.nbpb + jb;
-    const int U = __ldg(&d.binfo[b].z);
-    for (int e = threadIdx.x; e < U; e += blockDim.x) atomicAdd(&sh[*rec_field(d, b, e, REC_KEY)], 1);
+  for (long long base = 0; base < n; base += 1024) {
+    const long long i = base + threadIdx.x;
+    const int v = i < n ? __ldcg(key_start + i) : 0;
+    part[threadIdx.x] = v;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+      const int add = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+      __syncthreads();
+      part[threadIdx.x] += add;
+      __syncthreads();
+    }
+    const int excl = part[threadIdx.x] - v + carry;
+    if (i < n) key_start[i] = excl;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = excl + v;
+    __syncthreads();
   }
-  __syncthreads();
-  for (int s = threadIdx.x; s < d.S_k; s += blockDim.x) hist[chunk * d.S_k + s] = sh[s];
+  if (threadIdx.x == 0) key_start[n] = carry;
 }
 
 // For each (batch, key): exclusive prefix of the counts over the batch's
@@ -62,9 +71,14 @@ __global__ void __launch_bounds__(256) hist_kernel(const DetP d, int* __restrict
 // keys; its 32 warps split the batch's chunks into 32 contiguous segments
 // (lane = key, so every access is a coalesced 128-byte row piece): segment
 // sums, a scan over the segments, then the prefixes within each segment.
+// The counts come from the union pass (one per block entry).  The last CTA
+// to finish turns every batch's key totals into CSR offsets.
 __global__ void __launch_bounds__(1024) colscan_kernel(int* __restrict__ hist, int* __restrict__ key_start, int S_k,
-                                                      int cpb) {
+                                                      int cpb, int B, unsigned* __restrict__ done) {
   __shared__ int seg[32][33];
+  __shared__ int s_last;
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int kpb = (S_k + 31) / 32;  // key blocks per batch
   const int b = (int)(blockIdx.x / kpb);
@@ -97,32 +111,15 @@ __global__ void __launch_bounds__(1024) colscan_kernel(int* __restrict__ hist, i
       run += v;
     }
   }
-}
-
-// Exclusive scan of the per-key totals into CSR offsets (one block).
-__global__ void __launch_bounds__(1024) keyscan_kernel(int* __restrict__ key_start, long long n) {
-  __shared__ int part[1024];
-  __shared__ int carry;
-  if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  for (long long base = 0; base < n; base += 1024) {
-    const long long i = base + threadIdx.x;
-    const int v = i < n ? key_start[i] : 0;
-    part[threadIdx.x] = v;
-    __syncthreads();
-    for (int o = 1; o < 1024; o <<= 1) {
-      const int add = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
-      __syncthreads();
-      part[threadIdx.x] += add;
-      __syncthreads();
-    }
-    const int excl = part[threadIdx.x] - v + carry;
-    if (i < n) key_start[i] = excl;
-    __syncthreads();
-    if (threadIdx.x == 1023) carry = excl + v;
-    __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(done, 1u) == gridDim.x - 1;
   }
-  if (threadIdx.x == 0) key_start[n] = carry;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  keyscan(key_start, (long long)B * S_k);
 }
 
 // Positions of a chunk's entries: each key's cursor starts at its CSR offset
@@ -132,6 +129,8 @@ __global__ void __launch_bounds__(1024) keyscan_kernel(int* __restrict__ key_sta
 __global__ void __launch_bounds__(256) place_kernel(const DetP d, const int* __restrict__ hist,
                                                    const int* __restrict__ key_start) {
   extern __shared__ int cursor[];
+  griddep_launch_dependents();
+  griddep_wait();  // the offsets come from the column scan
   const int cpb = (d.nbpb + CB - 1) / CB;
   const long long chunk = blockIdx.x;
   const int bb = (int)(chunk / cpb), j0 = (int)(chunk % cpb) * CB;
@@ -156,6 +155,8 @@ __global__ void __launch_bounds__(256) place_kernel(const DetP d, const int* __r
 // the keys before it hold s*nbpb - sum_{s'<s} floor(s'/4) entries.
 __global__ void dense_keystart_kernel(int* __restrict__ key_start, int B, int S, int nbpb, long long per_batch) {
   const long long n = (long long)B * S;
+  griddep_launch_dependents();
+  griddep_wait();
   for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x <= n; x += (long long)gridDim.x * blockDim.x) {
     const long long bb = x / S, s = x % S;
     const long long a = s >> 2, c = s & 3;
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const float* __r
                                                                const int* __restrict__ key_start,
                                                                float* __restrict__ dk, int D) {
   __shared__ float4 part[SEG_WARPS][32];
+  griddep_wait();  // the u rows come from the gemm kernel
   const long long gk = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int beg = key_start[gk], end = key_start[gk + 1];
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const float* __r
   }
 }
 
-std::atomic<int> g_attr_hist[64], g_attr_place[64];
+std::atomic<int> g_attr_place[64];
 
 bool raise_smem(const void* fn, size_t bytes, std::atomic<int>* done) {
   int dev = 0;
@@ -233,8 +235,8 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   if (!a.idx) {
     const long long n = (long long)a.B * a.S_k + 1;
     const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 4LL * a.num_sms));
-    dense_keystart_kernel<<<blocks, 256, 0, st>>>(key_start, a.B, a.S_k, lay.nbpb, lay.entries_cap / a.B);
-    return cudaGetLastError();
+    return launch_ex(dense_keystart_kernel, (unsigned)blocks, 256u, 0, st, true, key_start, a.B, a.S_k, lay.nbpb,
+                     lay.entries_cap / a.B);
   }
   DetP d{};
   d.rec = ws + lay.rec;
@@ -246,14 +248,14 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
   d.rstride = lay.rstride;
   int* hist = reinterpret_cast<int*>(ws + lay.hist);
   const size_t sh = (size_t)a.S_k * sizeof(int);  // per-key counters or cursors
-  if (!raise_smem((const void*)hist_kernel, sh, g_attr_hist) || !raise_smem((const void*)place_kernel, sh, g_attr_place))
-    return cudaErrorInvalidValue;
+  if (!raise_smem((const void*)place_kernel, sh, g_attr_place)) return cudaErrorInvalidValue;
   const int cpb = (lay.nbpb + CB - 1) / CB;
-  hist_kernel<<<(unsigned)lay.nchunks, 256, sh, st>>>(d, hist);
-  colscan_kernel<<<(unsigned)(a.B * ((a.S_k + 31) / 32)), 1024, 0, st>>>(hist, key_start, a.S_k, cpb);
-  keyscan_kernel<<<1, 1024, 0, st>>>(key_start, (long long)a.B * a.S_k);
-  place_kernel<<<(unsigned)lay.nchunks, 256, sh, st>>>(d, hist, key_start);
-  return cudaGetLastError();
+  unsigned* done = reinterpret_cast<unsigned*>(ws + lay.sched) + kSchedDetScan;  // zeroed by the k copy
+  cudaError_t e = launch_ex(colscan_kernel, (unsigned)(a.B * ((a.S_k + 31) / 32)), 1024u, 0, st, true, hist,
+                            key_start, a.S_k, cpb, a.B, done);
+  if (e != cudaSuccess) return e;
+  return launch_ex(place_kernel, (unsigned)lay.nchunks, 256u, sh, st, true, static_cast<const DetP>(d),
+                   static_cast<const int*>(hist), static_cast<const int*>(key_start));
 }
 
 cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st) {
@@ -261,8 +263,7 @@ cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream
   const float* u = reinterpret_cast<const float*>(ws + lay.u);
   const int* key_start = reinterpret_cast<const int*>(ws + lay.key_start);
   const long long nk = (long long)a.B * a.S_k;
-  segsum_kernel<<<(unsigned)nk, SEG_WARPS * 32, 0, st>>>(u, key_start, a.dk, a.D);
-  return cudaGetLastError();
+  return launch_ex(segsum_kernel, (unsigned)nk, (unsigned)(SEG_WARPS * 32), 0, st, true, u, key_start, a.dk, a.D);
 }
 
 }  // namespace ibwd

@@ -14,6 +14,11 @@ constexpr int kDP = 128;  // head dim padded to 128 (the MMA M dimension for dQ 
 constexpr int kHP = 64;   // indexer heads padded to 64
 constexpr int kBlkRows = 4;     // query rows per block of the gemm stage
 constexpr int kSortBlocks = 2;  // blocks per chunk of the deterministic mode's key sort
+// The per-call counter block (256 bytes at the start of the gemm stage's
+// workspace): words the k conversion kernel zeroes, and the deterministic
+// sort's CTA counter among them.
+constexpr int kSchedWords = 11;
+constexpr int kSchedDetScan = 10;
 
 struct ScoreGradArgs {
   const float* index_score;  // [rows, L]
@@ -97,11 +102,13 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
 cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st);
 
 // fp16 copy of k into k16 ([B][S_k+1][128], zero padded, row S_k zero) that
-// also zeroes nsched words of the counters at sched and raises the
-// fp16-range bit of *status for an entry outside the fp16 range.  pdl: launched
-// programmatically behind this library's score-grad kernel.
+// also zeroes nsched words of the counters at sched and nzero32 ints at
+// zero32, and raises the fp16-range bit of *status for an entry outside the
+// fp16 range.  pdl: launched programmatically behind this library's
+// score-grad kernel.
 cudaError_t launch_k_to_f16(const uint16_t* k, __half* k16, int B, int S_k, int D, unsigned* sched, int nsched,
-                            unsigned* status, bool pdl, int num_sms, cudaStream_t st);
+                            unsigned* status, bool pdl, int num_sms, cudaStream_t st, int* zero32 = nullptr,
+                            long long nzero32 = 0);
 
 // The per-row gemm kernel (gemm.cu), atomic dK and no options: served to the
 // allocation-free entry point, whose only scratch is its fp16 copy of k.
