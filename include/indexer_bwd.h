@@ -96,10 +96,12 @@ IBWD_API int indexer_bwd_score_grad(const float* index_score, float* attn_score,
  * copy of its q rows laid out as the tensor-core operand and 16 bytes of
  * block data; for the sparse variant per block 4 bytes of ordering and
  * ceil(min(S_k, 4*topk) / 128) tile records of 2560 bytes.  The
- * deterministic mode adds 512 bytes per record, one dK row (4*D bytes) per
- * (block, key) entry -- nb * min(S_k, 4*topk) of them, or for the dense
- * variant one per (block, causal key) -- its key sort (4*S_k bytes per two
- * blocks) and 4*(B*S_k + 1) bytes of key offsets.  The workspace is
+ * deterministic mode adds 512 bytes per record, per (block, key) entry
+ * -- nb * min(S_k, 4*topk) of them, or for the dense variant one per
+ * (block, causal key) -- a scaled fp16 dK row (2*D bytes rounded up to a
+ * multiple of 32, then 32 bytes holding its factor), its key sort (4*S_k
+ * bytes per two blocks, sparse variant only) with 4 bytes per block, and
+ * 4*(B*S_k + 1) bytes of key offsets.  The workspace is
  * rewritten by every call: calls that may overlap on the GPU need separate
  * workspaces.  0 for unsupported arguments. */
 IBWD_API size_t indexer_bwd_gemm_workspace_size(int B, int S_q, int S_k, int H, int D, int topk,

@@ -15,7 +15,7 @@ namespace {
 
 
 // ------------------------------------------------------------ union pass --
-constexpr int UT = 128;        // threads: warp r handles row r of the block
+constexpr int UT = 256;        // threads: warps r and r + 4 handle row r of the block
 constexpr int NBUCKET = 1024;  // tile-count buckets of the block order
 
 struct UParams {
@@ -90,7 +90,7 @@ __device__ __forceinline__ void stage_rows(uint32_t dst, const void* src_base, l
 // sums.  The largest |dis| * |w| of the block fixes its dz scale.  The last
 // CTA to finish orders all blocks by descending tile count (a processing
 // order for the gemm kernel; it affects no result).
-__global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
+__global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
   extern __shared__ __align__(16) uint32_t us[];
   const int WW = p.W >> 5;
   const int Lp = (p.L + 3) & ~3;
@@ -99,31 +99,30 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   float* drow = reinterpret_cast<float*>(us + 10 * WW);   // [4][dcap]
   int* ids_s = reinterpret_cast<int*>(drow + R * p.dcap);  // staged: [4][Lp] ids, then [4][Lp] dI
   float* dI_s = reinterpret_cast<float*>(ids_s + R * Lp);
-  __shared__ int s_cnt[5], s_kmin[4], s_kmax[4];
-  __shared__ float s_wmax[4], s_dmax[4][R];
+  constexpr int NW = UT / 32;
+  __shared__ int s_cnt[5], s_kmin[NW], s_kmax[NW], s_dup[NW];
+  __shared__ float s_wmax[R], s_dmax[NW][R];
   __shared__ int s_last;
   griddep_launch_dependents();
-  if (p.select) {  // the flag is written by the kernel before
-    griddep_wait();
-    if (__ldcg(p.select) != 0u) return;
-  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // warp w: row w % 4, and of its slots the 32-slot steps of parity w / 4
+  const int row = warp & 3, hlf = warp >> 2;
   const long long b = blockIdx.x;
   const int bb = (int)(b / p.nbpb), jb = (int)(b % p.nbpb);
   const int t0 = jb * R;
   const int Rb = min(R, p.S_q - t0);
   const long long row0 = (long long)bb * p.S_q + t0;
   const unsigned off = p.ids_global ? (unsigned)bb * (unsigned)p.S_k : 0u;  // rows < 2^31
-  const bool own = warp < Rb;
+  const bool own = row < Rb;
   // this warp's row: in shared memory when staged, else global
-  const int32_t* ir = p.staged ? ids_s + warp * Lp : p.idx + (own ? (row0 + warp) * p.L : 0);
-  const float* dr_in = p.staged ? dI_s + warp * Lp : p.dI + (own ? (row0 + warp) * p.L : 0);
+  const int32_t* ir = p.staged ? ids_s + row * Lp : p.idx + (own ? (row0 + row) * p.L : 0);
+  const float* dr_in = p.staged ? dI_s + row * Lp : p.dI + (own ? (row0 + row) * p.L : 0);
   if (p.staged) stage_rows(smem_u32(ids_s), p.idx, row0, Rb, p.L, Lp);
 
   float wmax = 0.f;  // over the row's heads
-  if (own) {
+  if (own && hlf == 0) {
     for (int h = lane; h < p.H; h += 32) {
-      const float a = fabsf(__ldg(p.w + (row0 + warp) * p.H + h));
+      const float a = fabsf(__ldg(p.w + (row0 + row) * p.H + h));
       wmax = fmaxf(wmax, a);
     }
     wmax = warp_max(wmax);
@@ -138,7 +137,7 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
     kmin = INT_MAX;
     kmax = -1;
     if (own) {
-      for (int j = lane; j < p.L; j += 32) {
+      for (int j = lane + 32 * hlf; j < p.L; j += 64) {
         const int s = (int)((unsigned)ir[j] - off);
         if ((unsigned)s < (unsigned)p.S_k) {
           kmin = min(kmin, s);
@@ -156,16 +155,18 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
       s_kmax[warp] = kmax;
     }
   }
-  if (lane == 0) {
-    s_wmax[warp] = wmax;
-  }
+  if (lane == 0 && hlf == 0) s_wmax[row] = wmax;
   __syncthreads();
   if (p.S_k > p.W) {
-    kmin = min(min(s_kmin[0], s_kmin[1]), min(s_kmin[2], s_kmin[3]));
-    kmax = max(max(s_kmax[0], s_kmax[1]), max(s_kmax[2], s_kmax[3]));
+    for (int x = 0; x < NW; ++x) {
+      kmin = min(kmin, s_kmin[x]);
+      kmax = max(kmax, s_kmax[x]);
+    }
   }
-  // dI is written by the kernel before this one (score-grad)
+  // dI is written by an earlier kernel (score-grad), the choice of gemm
+  // kernel by the one before (its launch lets this one start early)
   griddep_wait();
+  if (p.select && __ldcg(p.select) != 0u) return;  // the per-row kernel serves this call
   if (p.staged) {
     stage_rows(smem_u32(dI_s), p.dI, row0, Rb, p.L, Lp);
     cp_async_wait_all();
@@ -180,18 +181,21 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
     __syncthreads();
     bool dup = false;
     if (own) {
-      for (int j = lane; j < p.L; j += 32) {
+      for (int j = lane + 32 * hlf; j < p.L; j += 64) {
         const int s = (int)((unsigned)ir[j] - off);
         const unsigned x = (unsigned)(s - w0);
         if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
           const uint32_t bit = 1u << (x & 31);
-          const uint32_t old = atomicOr(&bm[warp * WW + (x >> 5)], bit);
+          const uint32_t old = atomicOr(&bm[row * WW + (x >> 5)], bit);
           dup |= (old & bit) != 0u;
         }
       }
     }
     dup = __any_sync(FULL, dup);
+    if (lane == 0) s_dup[warp] = dup;
     __syncthreads();
+    // a key set twice in a row, by either of its warps
+    dup = s_dup[row] | s_dup[row + 4];
     for (int i = tid; i < WW; i += UT) bm[4 * WW + i] = bm[i] | bm[WW + i] | bm[2 * WW + i] | bm[3 * WW + i];
     __syncthreads();
     for (int x = warp; x < 5; x += UT / 32) {
@@ -199,15 +203,18 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
       if (lane == 0) s_cnt[x] = n;
     }
     __syncthreads();
-    if (own) {
-      float* drr = drow + warp * p.dcap;
-      const uint32_t* bmr = bm + warp * WW;
-      const int* pfr = pf + warp * WW;
+    // a row without repeated keys: each of its warps stores its own slots'
+    // dI at their ranks; a row with repeats: its first warp alone adds the
+    // row's values per key in slot order
+    if (own && (!dup || hlf == 0)) {
+      float* drr = drow + row * p.dcap;
+      const uint32_t* bmr = bm + row * WW;
+      const int* pfr = pf + row * WW;
       if (dup) {
-        for (int i = lane; i < s_cnt[warp]; i += 32) drr[i] = 0.f;
+        for (int i = lane; i < s_cnt[row]; i += 32) drr[i] = 0.f;
         __syncwarp();
       }
-      for (int j0 = 0; j0 < p.L; j0 += 32) {
+      for (int j0 = dup ? 0 : 32 * hlf; j0 < p.L; j0 += dup ? 32 : 64) {
         const int j = j0 + lane;
         int rank = -1;
         float v = 0.f;
@@ -276,8 +283,9 @@ __global__ void __launch_bounds__(UT) union_kernel(const UParams p) {
   if (tid == 0) {
     float m = 0.f;
     for (int r = 0; r < R; ++r) {
-      const float d = fmaxf(fmaxf(s_dmax[0][r], s_dmax[1][r]), fmaxf(s_dmax[2][r], s_dmax[3][r]));
-      m = fmaxf(m, d * s_wmax[r]);
+      float d = 0.f;
+      for (int x = 0; x < NW; ++x) d = fmaxf(d, s_dmax[x][r]);
+      m = fmaxf(m, d * (r < Rb ? s_wmax[r] : 0.f));
     }
     p.binfo[b] = make_int4(ntiles, dz_scale_exponent(m), U, 0);
     __threadfence();
@@ -344,7 +352,9 @@ __global__ void __launch_bounds__(128) select_kernel(const int32_t* __restrict__
                                                      int force) {
   extern __shared__ uint32_t sbm[];  // ceil(S_k / 32) words
   __shared__ unsigned s_cnt[4], s_pop[4];
-  griddep_wait();  // the counter block is zeroed by the kernel before
+  // the union pass may start now: it waits for this kernel's completion
+  // before it reads the choice
+  griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int words = (S_k + 31) >> 5;
   for (int i = tid; i < words; i += 128) sbm[i] = 0u;
@@ -355,11 +365,17 @@ __global__ void __launch_bounds__(128) select_kernel(const int32_t* __restrict__
   unsigned cnt = 0;
   if (warp < Rb) {
     const int32_t* ir = idx + ((long long)batch * S_q + t0 + warp) * L;
-    for (int j = lane; j < L; j += 32) {
-      const int s = __ldg(ir + j);
-      if ((unsigned)s < (unsigned)S_k) {
-        atomicOr(&sbm[s >> 5], 1u << (s & 31));
-        ++cnt;
+    constexpr int NB = 16;  // ids in flight per lane
+    for (int j0 = lane; j0 < L; j0 += 32 * NB) {
+      int sv[NB];
+#pragma unroll
+      for (int k = 0; k < NB; ++k) sv[k] = j0 + 32 * k < L ? __ldg(ir + j0 + 32 * k) : -1;
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        if ((unsigned)sv[k] < (unsigned)S_k) {
+          atomicOr(&sbm[sv[k] >> 5], 1u << (sv[k] & 31));
+          ++cnt;
+        }
       }
     }
   }
@@ -375,6 +391,7 @@ __global__ void __launch_bounds__(128) select_kernel(const int32_t* __restrict__
     s_pop[warp] = pop;
   }
   __syncthreads();
+  griddep_wait();  // the counter block is zeroed by the kernel before
   if (tid == 0) {
     const unsigned U = s_pop[0] + s_pop[1] + s_pop[2] + s_pop[3];
     unsigned long long row_tiles = 0;
@@ -392,18 +409,18 @@ __global__ void __launch_bounds__(128) select_kernel(const int32_t* __restrict__
       sched[SEL_FLAG] = force >= 0 ? (unsigned)force : (ROWS_MARGIN * t_rows < t_blocked ? 1u : 0u);
     }
   }
-  griddep_launch_dependents();
 }
 
 struct QImg {  // the Q operand images of every block
   const uint16_t* q;
   uint8_t* img;
+  unsigned* qmax;  // if set: per block, max |q| as bf16 bits (zeroed before)
   long long nblocks;
   int S_q, H, D, nbpb;
 };
 
-// Chunk x of the images (16 bytes; 4096 per block); returns the fp16-range flag.
-__device__ __forceinline__ bool q_image_at(const QImg& qi, long long x) {
+// Chunk x of the images (16 bytes; 4096 per block).
+__device__ __forceinline__ QChunk q_image_at(const QImg& qi, long long x) {
   const long long blk = x / (NR * 16);
   const int within = (int)(x % (NR * 16));
   const int batch = (int)(blk / qi.nbpb), t0 = (int)(blk % qi.nbpb) * R;
@@ -412,18 +429,39 @@ __device__ __forceinline__ bool q_image_at(const QImg& qi, long long x) {
 }
 
 // The q images, on the side stream beside the union pass (or the dense
-// scale pass).
+// scale pass).  A thread loads QIMG_ILP chunks before it stores any: the
+// stores could alias q as far as the compiler knows, so loads interleaved
+// with stores would be issued one at a time.
+constexpr int QIMG_ILP = 4;
 __global__ void q_image_kernel(const QImg qi, unsigned* __restrict__ status, const unsigned* __restrict__ select) {
   if (select && __ldcg(select) != 0u) return;  // the per-row kernel serves this call
   const long long nq = qi.nblocks * (NR * 16);
   const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
-  long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  for (; x + 3 * stride < nq; x += 4 * stride) {  // four chunks in flight per thread
+  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < nq; x += QIMG_ILP * stride) {
+    QChunk ch[QIMG_ILP];
+    uint4 v[QIMG_ILP];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) bad |= q_image_at(qi, x + k * stride);
+    for (int k = 0; k < QIMG_ILP; ++k) {
+      const long long y = x + k * stride;
+      ch[k] = y < nq ? q_image_at(qi, y) : QChunk{nullptr, nullptr};
+    }
+#pragma unroll
+    for (int k = 0; k < QIMG_ILP; ++k) v[k] = ch[k].src ? __ldg(ch[k].src) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < QIMG_ILP; ++k)
+      if (ch[k].dst) bad |= q_image_put(ch[k].dst, v[k]);
+    if (qi.qmax) {
+      // a warp's 32 chunks are consecutive and lie in one block (4096 chunks
+      // per block, 32-aligned): one maximum per warp and chunk step
+#pragma unroll
+      for (int k = 0; k < QIMG_ILP; ++k) {
+        const unsigned m = __reduce_max_sync(0xffffffffu, bf16x8_abs_max(v[k]));
+        const long long y = x + k * stride;
+        if ((threadIdx.x & 31) == 0 && y < nq && m != 0u) atomicMax(qi.qmax + y / (NR * 16), m);
+      }
+    }
   }
-  for (; x < nq; x += stride) bad |= q_image_at(qi, x);
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, DEV_FP16_RANGE);
 }
 
@@ -613,11 +651,12 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
       w.nchunks = (long long)B * ((w.nbpb + kSortBlocks - 1) / kSortBlocks);
     }
     w.u = off;
-    off = up(off + (size_t)w.entries_cap * D * 4);
-    if (!dense) {
-      w.hist = off;
-      off = up(off + (size_t)w.nchunks * S_k * 4);
-    }
+    off = up(off + (size_t)w.entries_cap * u_row_bytes(D));
+    // the key counts and the q maxima are contiguous: one zeroing covers both
+    w.hist = off;
+    if (!dense) off += (size_t)w.nchunks * S_k * 4;
+    w.qmax = off;
+    off = up(off + (size_t)w.nblocks * 4);
     w.key_start = off;
     off = up(off + ((size_t)B * S_k + 1) * 4);
   }
@@ -643,8 +682,12 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   // programmatic only right after this library's score-grad kernel: the
   // kernel reads k before it waits for its predecessor
   int* hist = (a.deterministic && !dense) ? reinterpret_cast<int*>(ws + lay.hist) : nullptr;
+  unsigned* qmax = a.deterministic ? reinterpret_cast<unsigned*>(ws + lay.qmax) : nullptr;
+  // deterministic mode: the key counts and the q maxima (contiguous) start at zero
+  const long long nzero = a.deterministic ? (hist ? lay.nchunks * a.S_k : 0LL) + lay.nblocks : 0LL;
   cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, SCHED_ZERO, a.status, a.after_score_grad != 0,
-                                  a.num_sms, st, hist, hist ? lay.nchunks * a.S_k : 0LL);
+                                  a.num_sms, st, a.deterministic ? reinterpret_cast<int*>(ws + lay.hist) : nullptr,
+                                  nzero);
   if (e != cudaSuccess) return e;
   if (choose) {
     const long long nsample = std::min<long long>(lay.nblocks, 256);
@@ -661,7 +704,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaStreamWaitEvent(a.side, a.ev_fork, 0);
   if (e != cudaSuccess) return e;
   {
-    const QImg qi{a.q, qimg, lay.nblocks, a.S_q, a.H, a.D, lay.nbpb};
+    const QImg qi{a.q, qimg, qmax, lay.nblocks, a.S_q, a.H, a.D, lay.nbpb};
     const long long n = lay.nblocks * (NR * 16);
     // four CTAs per SM: the union pass keeps three of its four while both run
     // (measured: 30 us faster than two CTAs per SM at the anchor)
@@ -721,7 +764,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.dq = a.dq;
   p.dw = a.dw;
   p.dk = a.dk;
-  p.u = a.deterministic ? reinterpret_cast<float*>(ws + lay.u) : nullptr;
+  p.u = a.deterministic ? ws + lay.u : nullptr;
+  p.qmax = qmax;
   p.dq16 = a.dq16;
   p.dw16 = a.dw16;
   p.sched = sched;

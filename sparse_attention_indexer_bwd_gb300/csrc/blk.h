@@ -49,16 +49,26 @@ constexpr uint32_t QIMG_HALF = NR * 128;  // one 64-column half: 32 KB
 constexpr uint32_t QIMG_BYTES = 2 * QIMG_HALF;
 
 // One 16-byte chunk of a block's image: chunk c (0..15, 8 columns each) of
-// (r,h) row n (0..255), converted from the bf16 rows starting at global row
-// row0 (Rb of them).  Returns whether an entry lies outside the fp16 range.
-__device__ __forceinline__ bool q_image_chunk(const uint16_t* __restrict__ q, uint8_t* img, long long row0, int Rb,
-                                              int H, int D, int n, int c) {
+// (r,h) row n (0..255) of the block whose first q row is global row row0
+// (Rb rows).  Its source in q (nullptr: a zero chunk) and its place in img.
+struct QChunk {
+  const uint4* src;
+  uint4* dst;
+};
+__device__ __forceinline__ QChunk q_image_chunk(const uint16_t* q, uint8_t* img, long long row0, int Rb, int H, int D,
+                                                int n, int c) {
   const int r = n >> 6, h = n & 63;
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (r < Rb && h < H && c * 8 < D)
-    v = __ldg(reinterpret_cast<const uint4*>(q + ((row0 + r) * H + h) * D + c * 8));
-  *reinterpret_cast<uint4*>(img + (c >> 3) * QIMG_HALF + n * 128 + (((c & 7) ^ (n & 7)) << 4)) =
-      make_uint4(bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z), bf16x2_to_half2(v.w));
+  QChunk o;
+  o.src = (r < Rb && h < H && c * 8 < D) ? reinterpret_cast<const uint4*>(q + ((row0 + r) * H + h) * D + c * 8)
+                                         : nullptr;
+  o.dst = reinterpret_cast<uint4*>(img + (c >> 3) * QIMG_HALF + n * 128 + (((c & 7) ^ (n & 7)) << 4));
+  return o;
+}
+
+// Writes the fp16 form of eight bf16 values; returns whether one lies
+// outside the fp16 range.
+__device__ __forceinline__ bool q_image_put(uint4* dst, uint4 v) {
+  *dst = make_uint4(bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z), bf16x2_to_half2(v.w));
   return bf16x2_out_of_fp16(v.x) || bf16x2_out_of_fp16(v.y) || bf16x2_out_of_fp16(v.z) || bf16x2_out_of_fp16(v.w);
 }
 
@@ -74,7 +84,8 @@ struct BParams {
   float* dq;
   float* dw;
   float* dk;           // [B, S_k, D] (atomic mode)
-  float* u;            // deterministic: per-entry dK rows in key order, or nullptr
+  char* u;             // deterministic: per-entry dK rows in key order (u_row_bytes(D) each), or nullptr
+  const unsigned* qmax;  // deterministic: per block, max |q| as bf16 bits
   uint16_t* dq16;      // bf16 outputs instead of dq / dw when set
   uint16_t* dw16;
   unsigned* sched;     // block counter, zeroed by the k conversion kernel

@@ -69,7 +69,8 @@ struct Hdr {        // per tile, written by the scan
   int c;            // dz scale exponent of the block
   int flags;
   int batch;
-  int pad[2];
+  int qe;           // deterministic mode: max |q| of the block < 2^qe
+  int pad;
 };
 
 struct Bars {
@@ -195,6 +196,7 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
     // dense scale pass)
     const int4 bi = __ldg(p.binfo + b);
     const int ntiles = bi.x, c = bi.y, U = bi.z;
+    const int qe = p.qmax ? q_exponent(__ldcg(p.qmax + b)) : 0;
     // publish the block to the Q loader; warm L2 with its q rows
     if (!WAIT(&B->bempty[i % BQ], ((i / BQ) & 1) ^ 1)) return drain_records();
     if (lane == 0) {
@@ -219,7 +221,7 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
       uint8_t* rs = cx.smem + OFF_REC + ms * REC_BYTES;
       if (!p.dense) {
         if (lane == 0) {
-          cx.hdr[ms] = Hdr{row0, Rb, max(count, 0), c, flags, batch, {0, 0}};
+          cx.hdr[ms] = Hdr{row0, Rb, max(count, 0), c, flags, batch, qe, 0};
           fence_proxy_async_smem();  // earlier generic reads of the slot precede the async writes
           mbar_arrive_expect_tx(&B->mfull[ms], copy_bytes);
           bulk_g2s(smem_u32(rs), p.rec + ((long long)b * p.tcap + k) * p.rstride, copy_bytes, &B->mfull[ms]);
@@ -247,7 +249,7 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
         }
         __syncwarp();
         if (lane == 0) {
-          cx.hdr[ms] = Hdr{row0, Rb, count, c, flags, batch, {0, 0}};
+          cx.hdr[ms] = Hdr{row0, Rb, count, c, flags, batch, qe, 0};
           mbar_arrive(&B->mfull[ms]);
         }
       }
@@ -636,19 +638,26 @@ __device__ void dk_role(const BParams& p, const Ctx& cx) {
     const int ms = (int)(g % MST);
     if (!WAIT(&B->mfull[ms], (g / MST) & 1)) return;
     const int flags = cx.hdr[ms].flags, c = cx.hdr[ms].c, count = cx.hdr[ms].count, batch = cx.hdr[ms].batch;
-    float* base = p.u ? p.u : p.dk + (long long)batch * p.S_k * p.D;
+    const int qe = cx.hdr[ms].qe;
+    float* base = p.dk + (long long)batch * p.S_k * p.D;
     const int* ids = p.u ? rec_pos(cx, ms) : rec_key(cx, ms);
     if (!WAIT(&B->dkfull, g & 1)) return;
     if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_FULL, (int)g);
     tc_fence_after();
     const float sc = pow2f(-c) * p.sm_scale;
+    // deterministic rows: |dK^T| < 256 * 2^14 * 2^qe (256 products of
+    // |dz| < 2^14 and |q| < 2^qe), so 2^-(7+qe) keeps them below 2^15 in
+    // fp16; the factor restores the scale (saturated at the largest float,
+    // so that a zero row stays zero)
+    const float su = pow2f(-7 - qe);
+    const float fu = fminf(ldexpf(p.sm_scale, 7 + qe - c), 3.4028235e38f);
     const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK;
 #pragma unroll 1
     for (int ch = kg * 2; ch < kg * 2 + 2; ++ch) {
       if (ch * 32 >= count) break;  // uniform: the remaining entries are padding
       const int nrow = min(32, count - ch * 32);
       if (p.u)
-        dk_chunk_tmem<false>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage, idmax);
+        dk_chunk_u16(p.u, ids + ch * 32, ta + ch * 32, nrow, su, fu, p.D, qw * 32, stage, idmax, qw == 0);
       else
         dk_chunk_tmem<true>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage, idmax);
     }

@@ -8,14 +8,19 @@
 // (block, key) entry (the four rows' contributions already summed by the
 // tensor core).  Here every entry gets a position such that each key's
 // entries are contiguous and in ascending block order; the gemm kernel stores
-// the entry's row there, and
-//   segsum:  dK[s] = sum of the key's rows, in that order.
+// the entry's row there, in fp16 under a power-of-two scale bounded from the
+// block's largest |q| and dz scale (no row can reach the fp16 limit; the
+// rounding is 2^-12 of the row's own values), with its restoring factor, and
+//   segsum:  dK[s] = sum of the key's rows times their factors, in that order.
+// fp16 rows halve the traffic of the mode's HBM-bound part (the rows are
+// written once and read once).
 // Sparse: per chunk of kSortBlocks blocks, per-key counts (a key appears at
 // most once per block; the union pass counts them as it writes the records),
 // an exclusive scan over the chunks and over the keys (no position atomics,
-// so the order is fixed), then the positions, written into the tile records.  Dense: block j of a batch holds keys [0, 4j + Rb),
-// so the positions have a closed form (the gemm kernel computes them) and
-// only the CSR offsets are filled here.
+// so the order is fixed), then the positions, written into the tile records.
+// Dense: block j of a batch holds keys [0, 4j + Rb), so the positions have
+// a closed form (the gemm kernel computes them) and only the CSR offsets are
+// filled here.
 // The result is bitwise identical run to run and overwrites dK.
 #include <algorithm>
 #include <atomic>
@@ -165,12 +170,13 @@ __global__ void dense_keystart_kernel(int* __restrict__ key_start, int B, int S,
 }
 
 // One block of eight warps per key: dK[key] = sum of the key's u rows, which
-// the gemm kernel stored contiguously in position order.  Warp w sums rows
-// w, w + 8, w + 16, ... of the segment in order (the block reads eight
-// consecutive rows per step, four steps in flight), then the eight partial
-// sums are added in warp order: a fixed order, so dK is bitwise reproducible.
+// the gemm kernel stored contiguously in position order as fp16 rows, each
+// with its restoring factor.  Warp w sums rows w, w + 8, w + 16, ... of the
+// segment in order (the block reads eight consecutive rows per step, NF steps
+// in flight), then the eight partial sums are added in warp order: a fixed
+// order, so dK is bitwise reproducible.
 constexpr int SEG_WARPS = 8;
-__global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const float* __restrict__ u,
+__global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const char* __restrict__ u,
                                                                const int* __restrict__ key_start,
                                                                float* __restrict__ dk, int D) {
   __shared__ float4 part[SEG_WARPS][32];
@@ -180,23 +186,29 @@ __global__ void __launch_bounds__(SEG_WARPS * 32) segsum_kernel(const float* __r
   const int beg = key_start[gk], end = key_start[gk + 1];
   const int d = lane * 4;
   const bool on = d < D;
+  const int rb = u_row_bytes(D), fsec = rb - 32;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int NF = 4;  // steps in flight per warp
+  constexpr int NF = 8;  // steps in flight per warp
   for (int p0 = beg + w; p0 < end; p0 += NF * SEG_WARPS) {
-    float4 v[NF];
+    uint2 v[NF];
+    float f[NF];
 #pragma unroll
     for (int k = 0; k < NF; ++k) {
       const int pr = p0 + k * SEG_WARPS;
-      v[k] = (on && pr < end) ? __ldcs(reinterpret_cast<const float4*>(u + (long long)pr * D + d))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool in = pr < end;
+      const char* row = u + (long long)pr * rb;
+      v[k] = (on && in) ? __ldcs(reinterpret_cast<const uint2*>(row + 2 * d)) : make_uint2(0u, 0u);
+      f[k] = in ? __ldcs(reinterpret_cast<const float*>(row + fsec)) : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < NF; ++k) {
       if (p0 + k * SEG_WARPS < end) {
-        acc.x += v[k].x;
-        acc.y += v[k].y;
-        acc.z += v[k].z;
-        acc.w += v[k].w;
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&v[k].x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&v[k].y));
+        acc.x += lo.x * f[k];
+        acc.y += lo.y * f[k];
+        acc.z += hi.x * f[k];
+        acc.w += hi.y * f[k];
       }
     }
   }
@@ -260,7 +272,7 @@ cudaError_t launch_det_sort(const GemmArgs& a, const WsLayout& lay, cudaStream_t
 
 cudaError_t launch_det_segsum(const GemmArgs& a, const WsLayout& lay, cudaStream_t st) {
   char* ws = static_cast<char*>(a.ws);
-  const float* u = reinterpret_cast<const float*>(ws + lay.u);
+  const char* u = ws + lay.u;
   const int* key_start = reinterpret_cast<const int*>(ws + lay.key_start);
   const long long nk = (long long)a.B * a.S_k;
   return launch_ex(segsum_kernel, (unsigned)nk, (unsigned)(SEG_WARPS * 32), 0, st, true, u, key_start, a.dk, a.D);

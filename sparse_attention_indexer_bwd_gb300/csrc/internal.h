@@ -14,6 +14,11 @@ constexpr int kDP = 128;  // head dim padded to 128 (the MMA M dimension for dQ 
 constexpr int kHP = 64;   // indexer heads padded to 64
 constexpr int kBlkRows = 4;     // query rows per block of the gemm stage
 constexpr int kSortBlocks = 2;  // blocks per chunk of the deterministic mode's key sort
+// Bytes of one deterministic-mode dK row: D fp16 values padded to whole
+// 32-byte sectors, then one sector whose first word is the row's fp32
+// restoring factor (the rest zero).  The gemm kernel writes every byte of a
+// row at once, so no sector is left partly written.
+__host__ __device__ constexpr int u_row_bytes(int D) { return ((2 * D + 31) & ~31) + 32; }
 // The per-call counter block (256 bytes at the start of the gemm stage's
 // workspace): words the k conversion kernel zeroes, and the deterministic
 // sort's CTA counter among them.
@@ -77,8 +82,9 @@ struct WsLayout {
   size_t binfo;      // int4 per block {tiles, dz scale exponent, entries, 0}
   size_t border;     // sparse: the blocks in descending tile count (processing order)
   size_t rec;        // sparse: tile records [nblocks][tcap][rstride bytes]
-  size_t u;          // deterministic: per-entry dK rows [entries_cap, D] fp32, in key order
+  size_t u;          // deterministic: per-entry dK rows [entries_cap][u_row_bytes(D)], in key order
   size_t hist;       // deterministic sparse: per-chunk key counts [nchunks, S_k] int32
+  size_t qmax;       // deterministic: per block, max |q| as bf16 bits (right after hist: zeroed with it)
   size_t key_start;  // deterministic: CSR offsets into u [B*S_k + 1] int32
   size_t total;
   long long nblocks;      // B * nbpb

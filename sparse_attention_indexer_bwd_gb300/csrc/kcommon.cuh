@@ -119,6 +119,63 @@ __device__ __forceinline__ void dk_chunk_tmem(float* base, const int* ids, uint3
   }
 }
 
+// Exponent qe with max |q| < 2^qe, from the largest |q| of a block as bf16
+// bits (the q images hold fp16, where magnitudes below 2^-25 are zero, so
+// qe >= -24 covers every nonzero operand; non-finite q raises the range
+// status and takes the top value).
+__device__ __forceinline__ int q_exponent(unsigned bits) {
+  if (bits == 0u) return 0;
+  if (bits >= 0x7F80u) return 17;
+  int e;
+  frexpf(__uint_as_float(bits << 16), &e);
+  return max(-24, min(17, e));
+}
+
+// The deterministic mode's form of dk_chunk_tmem: 32 entries' dK rows stored
+// at their sorted positions as u rows (u_row_bytes(D) each: D fp16 values,
+// each scaled by su, then the factor sector).  The warp that holds columns
+// 0..31 (own_f) also writes each entry's factor sector: f and zeros, 32
+// bytes from two lanes.  The caller picks su so that every value stays below
+// 2^15.
+__device__ __forceinline__ void dk_chunk_u16(char* u, const int* ids, uint32_t ta, int nrow, float su, float f, int D,
+                                             int dblk, float* stage, int idmax, bool own_f) {
+  const int lane = threadIdx.x & 31;
+  const int rsub = lane >> 3, c4 = (lane & 7) * 4;
+  const bool con = dblk + c4 < D;
+  const int rb = u_row_bytes(D), fsec = rb - 32;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    if (hf * 16 >= nrow) break;  // uniform
+    float v[16];
+    tmem_ld16(ta + hf * 16, v);
+    int idv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) idv[k] = min((unsigned)ids[hf * 16 + rsub + 4 * k], (unsigned)idmax);
+    tmem_wait_ld_dep16(v);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) stage[e * 32 + lane] = v[e] * su;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = rsub + 4 * k;
+      if (hf * 16 + e < nrow) {
+        char* row = u + (long long)idv[k] * rb;
+        if (con) {
+          const float4 x = *reinterpret_cast<const float4*>(stage + e * 32 + c4);
+          const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
+          uint2 h;
+          h.x = *reinterpret_cast<const uint32_t*>(&lo);
+          h.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(row + 2 * (dblk + c4)) = h;
+        }
+        if (own_f && c4 < 8)
+          *reinterpret_cast<uint4*>(row + fsec + 4 * c4) = make_uint4(c4 == 0 ? __float_as_uint(f) : 0u, 0u, 0u, 0u);
+      }
+    }
+    __syncwarp();  // the stage is rewritten by the next half
+  }
+}
+
 // Launch with programmatic stream serialization when pdl is set: the kernel
 // may start before the previous one on the stream completes and must call
 // griddep_wait() before reading what that one writes.

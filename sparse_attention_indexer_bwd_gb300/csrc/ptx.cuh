@@ -377,6 +377,13 @@ __device__ __forceinline__ bool bf16x2_out_of_fp16(uint32_t v) {
   return (v & 0x7FFFu) > 0x477Fu || ((v >> 16) & 0x7FFFu) > 0x477Fu;
 }
 
+// The largest magnitude among eight bf16 (a uint4), as bf16 bits: for
+// finite values the bits of |x| order as the magnitudes do.
+__device__ __forceinline__ unsigned bf16x8_abs_max(uint4 v) {
+  auto m2 = [](uint32_t x) { return max(x & 0x7FFFu, (x >> 16) & 0x7FFFu); };
+  return max(max(m2(v.x), m2(v.y)), max(m2(v.z), m2(v.w)));
+}
+
 __device__ __forceinline__ uint32_t bf16x2_to_half2(uint32_t v) {
   float lo = __uint_as_float(v << 16);
   float hi = __uint_as_float(v & 0xFFFF0000u);

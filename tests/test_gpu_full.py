@@ -51,8 +51,10 @@ def test_full_size_matches_oracle(name):
             a = gpu_all(wl, x, dk_mode=ibwd.IBWD_DK_ATOMIC)[1:]
     assert np.array_equal(a[0], d[0]) and np.array_equal(a[1], d[1])
     assert np.array_equal(again[1], d[0]) and np.array_equal(again[2], d[1]) and np.array_equal(again[3], d[2])
-    # atomic vs deterministic dK: both summations of the same fp32 terms
-    assert rms_rel(a[2], d[2]) < 1e-5
+    # atomic vs deterministic dK: the same terms, the deterministic mode's
+    # summed from fp16 partial rows (each rounded within 2^-12 of its own
+    # values: about 2e-4 relative RMS at these sizes)
+    assert rms_rel(a[2], d[2]) < 5e-4
 
 
 def test_anchor_homogeneity_identity():
