@@ -127,10 +127,17 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
     }
     wmax = warp_max(wmax);
   }
+  // dI is written by an earlier kernel (score-grad), the choice of gemm
+  // kernel by the one before (its launch lets this one start early); the
+  // dI copy then joins the ids copy in flight
+  griddep_wait();
+  const bool rows_path = p.select && __ldcg(p.select) != 0u;  // the per-row kernel serves this call
   if (p.staged) {
+    if (!rows_path) stage_rows(smem_u32(dI_s), p.dI, row0, Rb, p.L, Lp);
     cp_async_wait_all();
     __syncthreads();
   }
+  if (rows_path) return;
   // key range of the block's valid slots (one window covers every key when S_k <= W)
   int kmin = 0, kmax = p.S_k - 1;
   if (p.S_k > p.W) {
@@ -163,16 +170,6 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
       kmax = max(kmax, s_kmax[x]);
     }
   }
-  // dI is written by an earlier kernel (score-grad), the choice of gemm
-  // kernel by the one before (its launch lets this one start early)
-  griddep_wait();
-  if (p.select && __ldcg(p.select) != 0u) return;  // the per-row kernel serves this call
-  if (p.staged) {
-    stage_rows(smem_u32(dI_s), p.dI, row0, Rb, p.L, Lp);
-    cp_async_wait_all();
-    __syncthreads();
-  }
-
   float dmax[R] = {0.f, 0.f, 0.f, 0.f};
   int base = 0;
   for (long long w0l = kmin; w0l <= kmax; w0l += p.W) {  // no pass when the block has no valid slot

@@ -24,7 +24,7 @@
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
 //   0-3   gather;  4 scan (row ids and dI staged by bulk copies one row
 //   ahead, compaction into tile metadata);  5 MMA issuer and TMEM owner;
-//   6-7   Q loader;  8-15 dz (two groups of four for heads 0-31 / 32-63: dW
+//   6-7   Q loader (the row's q by one bulk copy, then fp16 conversion);  8-15 dz (two groups of four for heads 0-31 / 32-63: dW
 //   partials, fp16 dz tile, dW reduction and the dQ epilogue);  16-23 dK
 //   (fp32 red.global.add of the transposed tile rows).
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
@@ -37,7 +37,7 @@
 namespace ibwd {
 namespace {
 
-constexpr int KST = 3;  // K-tile stages
+constexpr int KST = 2;  // K-tile stages
 constexpr int MST = 8;  // tile-metadata ring (deep enough to hide the per-row scan)
 constexpr int RQ = 16;  // row-order ring: the scan runs at most ~MST + 2 rows ahead of the Q loader
 constexpr int NTHREADS = 768;
@@ -69,6 +69,7 @@ struct Bars {
   uint64_t mfull[MST], mempty[MST];
   uint64_t rowfull[2];
   uint64_t qfull[2];
+  uint64_t qraw[2];
   uint64_t zfull[2], zempty[2];
   uint64_t dzfull[2], dzempty[2];
   uint64_t dkfull[2], dkempty[2];
@@ -81,7 +82,8 @@ struct Bars {
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_Q = OFF_K + KST * KTILE_BYTES;
 constexpr uint32_t OFF_DZ = OFF_Q + 2 * QTILE_BYTES;
-constexpr uint32_t OFF_ROW = OFF_DZ + 2 * DZTILE_BYTES;
+constexpr uint32_t OFF_QRAW = OFF_DZ + 2 * DZTILE_BYTES;  // two rows of q as they are (bf16 [H][D])
+constexpr uint32_t OFF_ROW = OFF_QRAW + 2 * QTILE_BYTES;
 constexpr uint32_t OFF_META = OFF_ROW + 2 * ROW_BYTES;
 constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
 constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
@@ -134,46 +136,89 @@ struct Ctx {
 #define WAIT(bar, par) __all_sync(0xffffffffu, mbar_wait((bar), (par), cx.abort, p.status, p.wait_ns))
 #define WAITW(bar, par) WAIT(bar, par)
 
+// Optional per-tile timeline (clock64 stamps of each role's progress in the
+// first CTAs), compiled only with -DIBWD_TRACE for pipeline analysis.
+enum RowTraceEv {
+  RV_SCAN_PUB, RV_GATHER, RV_Q_START, RV_Q_FREE, RV_Q_DONE, RV_MMA_Z, RV_MMA_DK, RV_MMA_DQ, RV_DZ_START,
+  RV_DZ_DONE, RV_EPI_DONE, RV_DW_DONE, RV_DK_START, RV_DK_DONE, RV_COUNT
+};
+#ifdef IBWD_TRACE
+constexpr int RTRACE_CTAS = 4, RTRACE_TILES = 256;
+__device__ unsigned long long g_rtrace[RTRACE_CTAS][RV_COUNT][RTRACE_TILES];
+#define RTRACE(ev, g)                                                                                       \
+  do {                                                                                                      \
+    if (blockIdx.x < RTRACE_CTAS && (g) >= 0 && (g) < RTRACE_TILES && (threadIdx.x & 31) == 0)             \
+      g_rtrace[blockIdx.x][ev][g] = clock64();                                                              \
+  } while (0)
+#else
+#define RTRACE(ev, g) \
+  do {                \
+  } while (0)
+#endif
+
 // ------------------------------------------------------------ Q loader ----
+// A row's q (H*D bf16, contiguous) arrives by one bulk copy into a raw
+// buffer, issued a row ahead; the loader threads then convert it into the
+// fp16, 128-byte-swizzled Q operand once that buffer is free.  The copy's
+// latency stays off the MMA chain.
 __device__ void q_role(const KParams& p, const Ctx& cx) {
   const int tid = threadIdx.x - W_Q0 * 32;  // 0..63
-  for (long long i = 0;; ++i) {
+  const uint32_t rowq_bytes = (uint32_t)(p.H * p.D * 2);
+  long long issued = -1, landed = -1;  // last rows whose raw copy was issued / waited for
+  auto issue_raw = [&](long long i, long long r) {
+    if (tid == 0) {
+      const int b = (int)(i & 1);
+      mbar_arrive_expect_tx(&cx.bars->qraw[b], rowq_bytes);
+      bulk_g2s(cx.sbase + OFF_QRAW + b * QTILE_BYTES, p.q + r * p.H * p.D, rowq_bytes, &cx.bars->qraw[b]);
+    }
+    issued = i;
+  };
+  // copies still in flight (at most two) must land before the CTA can exit
+  auto drain = [&]() {
+    if (tid == 0)
+      for (long long j = landed + 1; j <= issued; ++j)
+        drain_wait(&cx.bars->qraw[j & 1], (uint32_t)((j >> 1) & 1), p.status, p.wait_ns);
+  };
+  if (!WAIT(&cx.bars->rowid[0], 0u)) return;
+  long long r = cx.rowq[0];
+  if (r >= 0) issue_raw(0, r);
+  for (long long i = 0; r >= 0; ++i) {
     const int qb = (int)(i & 1);
-    // the scan publishes the CTA's rows in order; -1 ends the list
-    if (!WAIT(&cx.bars->rowid[i % RQ], (uint32_t)((i / RQ) & 1))) return;
-    const long long r = cx.rowq[i % RQ];
-    if (r < 0) return;
+    // the next row's copy into the other raw buffer, once both loader warps
+    // have converted row i - 1 out of it (their qfull arrivals)
+    if (!WAIT(&cx.bars->rowid[(i + 1) % RQ], (uint32_t)(((i + 1) / RQ) & 1))) return drain();
+    const long long rn = cx.rowq[(i + 1) % RQ];
+    if (i >= 1 && !WAIT(&cx.bars->qfull[(i + 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) return drain();
+    if (rn >= 0) issue_raw(i + 1, rn);
+    if (tid == 0) RTRACE(RV_Q_START, (int)i);
+    const float wv = tid < p.H ? __ldg(p.w + r * p.H + tid) : 0.f;
+    if (!WAIT(&cx.bars->qraw[qb], (uint32_t)((i >> 1) & 1))) return drain();
+    landed = i;
     // buffer qb was last used by row i-2: all its MMAs and dz reads are done
     // once that row's dQ accumulator is complete
-    if (i >= 2 && !WAIT(&cx.bars->dqfull[qb], (uint32_t)(((i - 2) >> 1) & 1))) return;
-    const uint16_t* qr = p.q + r * p.H * p.D;
+    if (i >= 2 && !WAIT(&cx.bars->dqfull[qb], (uint32_t)(((i - 2) >> 1) & 1))) return drain();
+    if (tid == 0) RTRACE(RV_Q_FREE, (int)i);
+    const uint8_t* raw = cx.smem + OFF_QRAW + qb * QTILE_BYTES;
     const uint32_t qs = cx.sbase + OFF_Q + qb * QTILE_BYTES;
     bool bad = false;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 v[8];
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int x = tid + (half * 8 + it) * NQT;  // 16-byte chunk: head h, column chunk ch
-        const int h = x >> 4, ch = x & 15;
-        v[it] = make_uint4(0u, 0u, 0u, 0u);
-        if (h < p.H && ch * 8 < p.D) v[it] = __ldg(reinterpret_cast<const uint4*>(qr + h * p.D + ch * 8));
-      }
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int x = tid + (half * 8 + it) * NQT;
-        const int h = x >> 4, ch = x & 15;
-        const uint32_t dst = qs + (ch >> 3) * QHALF_BYTES + h * 128 + (((ch & 7) ^ (h & 7)) << 4);
-        bad |= bf16x2_out_of_fp16(v[it].x) || bf16x2_out_of_fp16(v[it].y) || bf16x2_out_of_fp16(v[it].z) ||
-               bf16x2_out_of_fp16(v[it].w);
-        st_shared_v4(dst, bf16x2_to_half2(v[it].x), bf16x2_to_half2(v[it].y), bf16x2_to_half2(v[it].z),
-                     bf16x2_to_half2(v[it].w));
-      }
+#pragma unroll 4
+    for (int it = 0; it < 16; ++it) {
+      const int x = tid + it * NQT;  // 16-byte chunk: head h, column chunk ch
+      const int h = x >> 4, ch = x & 15;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (h < p.H && ch * 8 < p.D) v = *reinterpret_cast<const uint4*>(raw + (h * p.D + ch * 8) * 2);
+      const uint32_t dst = qs + (ch >> 3) * QHALF_BYTES + h * 128 + (((ch & 7) ^ (h & 7)) << 4);
+      bad |= bf16x2_out_of_fp16(v.x) || bf16x2_out_of_fp16(v.y) || bf16x2_out_of_fp16(v.z) ||
+             bf16x2_out_of_fp16(v.w);
+      st_shared_v4(dst, bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z), bf16x2_to_half2(v.w));
     }
     if (__any_sync(0xffffffffu, bad) && (tid & 31) == 0) atomicOr(p.status, DEV_FP16_RANGE);
-    cx.w_s[qb * kHP + tid] = tid < p.H ? __ldg(p.w + r * p.H + tid) : 0.f;
+    cx.w_s[qb * kHP + tid] = wv;
+    // the raw buffer's generic reads precede the next copy into it (async)
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->qfull[qb]);
+    if (tid == 0) RTRACE(RV_Q_DONE, (int)i);
+    r = rn;
   }
 }
 
@@ -326,6 +371,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
         }
         __syncwarp();
         mbar_arrive(&cx.bars->mfull[ms]);
+        RTRACE(RV_SCAN_PUB, g);
       }
     }
     __syncwarp();
@@ -365,6 +411,7 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
 #pragma unroll
     for (int i = 0; i < kBM / 8; ++i) cp_async16(kbase + i * 1024, kb + (long long)key[i] * kDP, 16);
     cp_async_mbar_arrive_noinc(&cx.bars->kfull[st]);
+    if (x == 0) RTRACE(RV_GATHER, g);
     if (flags & F_END) break;
   }
   // copies in flight must land before the CTA can exit
@@ -418,6 +465,7 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
     tc_fence_after();
     mma_z(cx, 0, 0);
     umma_commit_elect(&B->zfull[0]);
+    RTRACE(RV_MMA_Z, 0);
     for (;;) {
       int nflags = 0;
       long long niq = iq;
@@ -427,6 +475,7 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
       tc_fence_after();
       mma_dk(cx, g, (int)(iq & 1));
       umma_commit_elect(&B->dkfull[g & 1]);
+      RTRACE(RV_MMA_DK, g);
       if (!(flags & F_END)) {
         // then Z of tile g+1
         const int g1 = g + 1;
@@ -442,10 +491,12 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
         tc_fence_after();
         mma_z(cx, g1, (int)(niq & 1));
         umma_commit_elect(&B->zfull[g1 & 1]);
+        RTRACE(RV_MMA_Z, g1);
       }
       if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
       tc_fence_after();
       mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
+      RTRACE(RV_MMA_DQ, g);
       umma_commit_elect(&B->kempty[g % KST]);
       umma_commit_elect(&B->dzempty[g & 1]);
       if (flags & F_LAST) umma_commit_elect(&B->dqfull[iq & 1]);
@@ -520,6 +571,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
     if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
     tc_fence_after();
+    if (tdz == 0) RTRACE(RV_DZ_START, g);
     const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
     const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
 #pragma unroll
@@ -552,9 +604,11 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     }
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
+    if (tdz == 0) RTRACE(RV_DZ_DONE, g);
     if ((flags & F_FIRST) && ep_r >= 0) {
       dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
       ep_r = -1;
+      if (tdz == 0) RTRACE(RV_EPI_DONE, g);
     }
     if (flags & F_LAST) {
       // dW[t,h] = 2^-c sum over the 128 tile rows of acc[h]: a butterfly
@@ -580,6 +634,7 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
           p.dw[(long long)r * p.H + tdz] =
               (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
       }
+      if (tdz == 0) RTRACE(RV_DW_DONE, g);
       ep_r = r;
       ep_c = c;
       ep_iq = iq;
@@ -604,6 +659,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
     float* base = p.dk + (long long)(r / p.S_q) * p.S_k * p.D;
     if (!WAIT(&cx.bars->dkfull[g & 1], (uint32_t)((g >> 1) & 1))) return;
     tc_fence_after();
+    if (threadIdx.x == W_DK0 * 32) RTRACE(RV_DK_START, g);
     const float sc = pow2f(-c);
     const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DK + (uint32_t)(g & 1) * 128;
 #pragma unroll 1
@@ -617,6 +673,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
     tc_fence_before();
     mbar_arrive(&cx.bars->dkempty[g & 1]);
     mbar_arrive(&cx.bars->mempty[ms]);
+    if (threadIdx.x == W_DK0 * 32) RTRACE(RV_DK_DONE, g);
     if (flags & F_END) return;
   }
 }
@@ -649,6 +706,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->rowfull[i], 1);
       mbar_init(&B->qfull[i], NQT);
+      mbar_init(&B->qraw[i], 1);
       mbar_init(&B->zfull[i], 1);
       mbar_init(&B->zempty[i], NDZT);
       mbar_init(&B->dzfull[i], NDZT);
@@ -774,5 +832,11 @@ cudaError_t launch_gemm_rows_kernel(const GemmArgs& a, const __half* k16, unsign
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
   return launch_ex(gemm_rows_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
 }
+
+#ifdef IBWD_TRACE
+extern "C" __attribute__((visibility("default"))) int ibwd_rtrace_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_rtrace, bytes < sizeof(g_rtrace) ? bytes : sizeof(g_rtrace));
+}
+#endif
 
 }  // namespace ibwd
