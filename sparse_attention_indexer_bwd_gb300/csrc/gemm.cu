@@ -24,9 +24,10 @@
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
 //   0-3   gather;  4 scan (row ids and dI staged by bulk copies one row
 //   ahead, compaction into tile metadata);  5 MMA issuer and TMEM owner;
-//   6-7   Q loader (the row's q by one bulk copy, then fp16 conversion);  8-15 dz (two groups of four for heads 0-31 / 32-63: dW
-//   partials, fp16 dz tile, dW reduction and the dQ epilogue);  16-23 dK
-//   (fp32 red.global.add of the transposed tile rows).
+//   6-7   Q loader (the row's q by one bulk copy, then fp16 conversion);
+//   8-15 dz (two groups of four for heads 0-31 / 32-63: dW partials, fp16
+//   dz tile, dW reduction and the dQ epilogue);  16-23 dK (fp32
+//   red.global.add of the transposed tile rows).
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
 #include <algorithm>
