@@ -44,14 +44,14 @@ METRIC = "indexer-bwd kernel µs & TFLOP/s (frac of bf16 peak), H64 D128 Sq8192 
 # of the source files of the kernels it measured; a change to any of those
 # files makes the figure stale and the benchmark then reports null.  The
 # captures and their commands are summarised under profiles/.
-# the gemm stage's kernels (k conversion, union pass, blocked kernel) and the
-# code they include
-GEMM_FILES = ("blk.cu", "blk.h", "blk_pipe.cuh", "blk_pipe.cu", "kcommon.cuh", "ptx.cuh", "internal.h")
+# the gemm stage's kernels (k conversion, kernel choice, union pass, q images,
+# blocked kernel, the per-row kernel's empty launch) and the code they include
+GEMM_FILES = ("blk.cu", "blk.h", "blk_pipe.cuh", "blk_pipe.cu", "gemm.cu", "kcommon.cuh", "ptx.cuh", "internal.h")
 SCORE_GRAD_FILES = ("score_grad.cu",)
 PROFILED_TRAFFIC = {
-    # k_to_f16 + union + q_image + blk kernels of one gemm-stage call
-    ("anchor", "atomic", "gemm_stage"): ("c7be96e67eacd994b938375dc80eddddb7643259fe956bafa42f79b0cc9225a8", 1.06e6 + 83.91e6 + 222.07e6 + 423.15e6),
-    ("anchor", "atomic", "score_grad"): ("32716e0bdb141dfa50987a5d3f34f07eb40acf8a602b202185531f24332fc497", 100.694528e6 + 4.471808e6),
+    # k_to_f16 + select + union + q_image + blk + (exiting) per-row kernels of one gemm-stage call
+    ("anchor", "atomic", "gemm_stage"): ("23025c9338639c9e9a537b92cf1605f2006a5808bb1ea348993a8de1bebf0e13", 1.063e6 + 4.212e6 + 84.177e6 + 218.841e6 + 423.780e6 + 0.071e6),
+    ("anchor", "atomic", "score_grad"): ("32716e0bdb141dfa50987a5d3f34f07eb40acf8a602b202185531f24332fc497", 100.692e6 + 2.113e6),
 }
 
 
