@@ -659,7 +659,7 @@ __device__ void dk_role(const BParams& p, const Ctx& cx) {
       if (p.u)
         dk_chunk_u16(p.u, ids + ch * 32, ta + ch * 32, nrow, su, fu, p.D, qw * 32, stage, idmax, qw == 0);
       else
-        dk_chunk_tmem<true>(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage, idmax);
+        dk_chunk_tmem(base, ids + ch * 32, ta + ch * 32, nrow, sc, p.D, qw * 32, stage, idmax);
     }
     tc_fence_before();
     mbar_arrive(&B->dkempty);

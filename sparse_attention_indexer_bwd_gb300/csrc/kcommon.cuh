@@ -81,10 +81,10 @@ __device__ __forceinline__ void dk_chunk(float* base, const int* ids, const floa
 }
 
 // The same for 32 entries read straight from TMEM, 16 columns at a time (half
-// the live registers of dk_chunk): ta addresses the warp's lane quarter at
-// the chunk's first column; the ids are clamped to idmax, so every address
-// stays inside the destination whatever a record holds.
-template <bool RED>
+// the live registers of dk_chunk), as fp32 reductions into base: ta
+// addresses the warp's lane quarter at the chunk's first column; the ids are
+// clamped to idmax, so every address stays inside the destination whatever a
+// record holds.
 __device__ __forceinline__ void dk_chunk_tmem(float* base, const int* ids, uint32_t ta, int nrow, float sc, int D,
                                               int dblk, float* stage, int idmax) {
   const int lane = threadIdx.x & 31;
@@ -108,11 +108,8 @@ __device__ __forceinline__ void dk_chunk_tmem(float* base, const int* ids, uint3
       if (hf * 16 + e < nrow && con) {
         const float4 x = *reinterpret_cast<const float4*>(stage + e * 32 + c4);
         float* dst = base + (long long)idv[k] * D + dblk + c4;
-        if (RED)
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x), "f"(x.y), "f"(x.z),
-                       "f"(x.w));
-        else
-          *reinterpret_cast<float4*>(dst) = x;
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x), "f"(x.y), "f"(x.z),
+                     "f"(x.w));
       }
     }
     __syncwarp();  // the stage is rewritten by the next half
