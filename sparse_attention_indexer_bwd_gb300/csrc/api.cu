@@ -13,7 +13,9 @@ struct DeviceInfo {
   int num_sms = 0;
   unsigned* status = nullptr;  // one device word, allocated once
   // a second stream for work that runs beside the caller's stream within one
-  // call (the gemm stage's q images), and the events that fork and join it
+  // call (the gemm stage's q images), and the events that fork and join it;
+  // at the highest priority, so that the images (the later of the two to
+  // finish otherwise) take the SMs first as the union pass's CTAs retire
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
@@ -37,7 +39,9 @@ int device_info(DeviceInfo** out) {
     if (d.supported) {
       if (cudaMalloc(&d.status, sizeof(unsigned)) != cudaSuccess) return IBWD_ERR_CUDA;
       if (cudaMemset(d.status, 0, sizeof(unsigned)) != cudaSuccess) return IBWD_ERR_CUDA;
-      if (cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) != cudaSuccess ||
+      int least = 0, greatest = 0;
+      if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+          cudaStreamCreateWithPriority(&d.side, cudaStreamNonBlocking, greatest) != cudaSuccess ||
           cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess)
         return IBWD_ERR_CUDA;
