@@ -61,3 +61,43 @@ def test_the_choice_follows_the_key_overlap():
         picks[wl.name] = [p for p in outs if np.array_equal(outs[p], dq)]
     assert picks["low_overlap"] == ["rows"]
     assert picks["high_overlap"] == ["blocked"]
+
+
+def test_alternating_choices_on_one_workspace():
+    # Consecutive calls on one workspace whose ids pick different kernels:
+    # every kernel that reads the choice must read this call's, not the one
+    # an earlier call left in the workspace.
+    import torch
+    from gpu_util import dev, gpu_gemm, t_bf16, t_f32, t_i32
+    import oracle
+    wl = W("alternating", 1, 16, 64, 256, 4096, 384, "uniform", 22)
+    x = case_inputs(wl)
+    t = np.arange(wl.S_q)[:, None]
+    window = ((t + np.arange(wl.topk)[None, :]) % wl.S_k).astype(np.int32)[None]  # neighbours share keys
+    cases = {}
+    for name, ids in (("uniform", x["idx"]), ("window", window)):
+        I = oracle.forward_sparse(x["q"], x["k"], x["w"], ids, wl.S_k)
+        dI = oracle.score_grad_sparse(I, x["attn"], ids, wl.S_k)
+        cases[name] = (ids, dI.astype(np.float32), oracle.gemm_sparse(x["q"], x["k"], x["w"], dI, ids, wl.S_k))
+    ws = torch.empty(ibwd.indexer_bwd_gemm_workspace_size(1, wl.S_q, wl.S_k, wl.H, wl.D, wl.topk, 0),
+                     dtype=torch.uint8, device=dev())
+    q, k, w = t_bf16(x["q"]), t_bf16(x["k"]), t_f32(x["w"])
+    for name in ("uniform", "window", "uniform", "window", "window", "uniform"):
+        ids, dI, ref = cases[name]
+        dq = torch.full((1, wl.S_q, wl.H, wl.D), float("nan"), device=dev())
+        dw = torch.full((1, wl.S_q, wl.H), float("nan"), device=dev())
+        dk = torch.zeros((1, wl.S_k, wl.D), device=dev())
+        ibwd.indexer_bwd_gemm(q, k, w, t_f32(dI), t_i32(ids), dq, dw, dk, ibwd.IBWD_DK_ATOMIC, ws)
+        assert ibwd.indexer_bwd_last_device_status() == ibwd.IBWD_OK
+        assert_close(dq.cpu().numpy(), dw.cpu().numpy(), dk.cpu().numpy(), ref, tag=name)
+    # the two id sets do take different kernels
+    picks = {}
+    for name in ("uniform", "window"):
+        ids, dI, _ = cases[name]
+        outs = {}
+        for path in ("rows", "blocked"):
+            with gemm_path(path):
+                outs[path] = gpu_gemm(wl, x, dI, idx=ids)[0]
+        dq = gpu_gemm(wl, x, dI, idx=ids)[0]
+        picks[name] = [p for p in outs if np.array_equal(outs[p], dq)]
+    assert picks == {"uniform": ["rows"], "window": ["blocked"]}
