@@ -32,7 +32,8 @@ struct UParams {
   int cpb;     // deterministic mode: sort chunks per batch
   int W;       // key window per pass (multiple of 1024)
   int dcap;    // per-row capacity of the dedup arrays: min(L, W)
-  int staged;  // the block's ids and dI rows are copied into shared memory (Lp = L rounded up to 4)
+  int staged;    // the block's id rows are copied into shared memory (Lp = L rounded up to 4)
+  int staged_dI;  // and its dI rows after them (read once each: not for long rows, where shared memory sets the occupancy)
   const unsigned* select;  // if set: the pass runs only when *select == 0 (1 selects the per-row kernel)
 };
 
@@ -85,7 +86,8 @@ __device__ __forceinline__ void stage_rows(uint32_t dst, const void* src_base, l
 // and of their union; popcount prefixes give every key its rank (row-local
 // and union); each row's dI is summed per distinct key in slot order (rows
 // with repeated ids: lanes holding the same key in one 32-slot step add their
-// values in lane order, steps in slot order, so the sum is fixed); then the
+// values in lane order, steps in slot order, so the sum is fixed; a step
+// takes as many shuffle rounds as its largest group of equal keys); then the
 // union's entries are written in ascending key order with the four rows'
 // sums.  The largest |dis| * |w| of the block fixes its dz scale.  The last
 // CTA to finish orders all blocks by descending tile count (a processing
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
   const bool own = row < Rb;
   // this warp's row: in shared memory when staged, else global
   const int32_t* ir = p.staged ? ids_s + row * Lp : p.idx + (own ? (row0 + row) * p.L : 0);
-  const float* dr_in = p.staged ? dI_s + row * Lp : p.dI + (own ? (row0 + row) * p.L : 0);
+  const float* dr_in = p.staged_dI ? dI_s + row * Lp : p.dI + (own ? (row0 + row) * p.L : 0);
   if (p.staged) stage_rows(smem_u32(ids_s), p.idx, row0, Rb, p.L, Lp);
 
   float wmax = 0.f;  // over the row's heads
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
   griddep_wait();
   const bool rows_path = p.select && __ldcg(p.select) != 0u;  // the per-row kernel serves this call
   if (p.staged) {
-    if (!rows_path) stage_rows(smem_u32(dI_s), p.dI, row0, Rb, p.L, Lp);
+    if (!rows_path && p.staged_dI) stage_rows(smem_u32(dI_s), p.dI, row0, Rb, p.L, Lp);
     cp_async_wait_all();
     __syncthreads();
   }
@@ -220,17 +222,24 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
           const unsigned x = (unsigned)(s - w0);
           if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
             rank = pfr[x >> 5] + __popc(bmr[x >> 5] & ((1u << (x & 31)) - 1u));
-            v = dr_in[j];
+            v = p.staged_dI ? dr_in[j] : __ldg(dr_in + j);
           }
         }
         if (!dup) {
           if (rank >= 0) drr[rank] = v;
         } else {
+          // the lanes of each lane's group (same key) in lane order: as many
+          // shuffle rounds as the largest group of the step
           const unsigned grp = __match_any_sync(FULL, rank >= 0 ? rank : -1 - lane);
+          const int rounds = (int)__reduce_max_sync(FULL, (unsigned)__popc(grp));
+          unsigned rest = grp;
           float sum = 0.f;
-          for (int l = 0; l < 32; ++l) {
-            const float y = __shfl_sync(FULL, v, l);
-            if ((grp >> l) & 1u) sum += y;
+          for (int k = 0; k < rounds; ++k) {
+            const float y = __shfl_sync(FULL, v, rest ? __ffs(rest) - 1 : lane);
+            if (rest) {
+              sum += y;
+              rest &= rest - 1u;
+            }
           }
           if (rank >= 0 && (grp & ((1u << lane) - 1u)) == 0u) drr[rank] += sum;
           __syncwarp();
@@ -556,16 +565,17 @@ __global__ void dk_to_bf16_kernel(const float* __restrict__ dk, uint16_t* __rest
 // Key window of the union pass and the dedup capacity per row (both bounded
 // so that its shared memory stays under ~104 KB for any shape), and whether
 // the block's rows are staged in shared memory (rows of up to 2048 slots).
-void union_geometry(int S_k, int L, int& W, int& dcap, int& staged) {
+void union_geometry(int S_k, int L, int& W, int& dcap, int& staged, int& staged_dI) {
   const long long skr = ((long long)S_k + 1023) / 1024 * 1024;
   W = (int)std::min<long long>(skr, L <= 4096 ? 32768 : 4096);
   dcap = std::min(L, W);
   staged = L <= 2048 ? 1 : 0;
+  staged_dI = L <= 1024 ? 1 : 0;
 }
 
-size_t union_smem_bytes(int W, int dcap, int L, int staged) {
+size_t union_smem_bytes(int W, int dcap, int L, int staged, int staged_dI) {
   size_t s = (size_t)10 * (W / 32) * 4 + (size_t)R * dcap * 4;
-  if (staged) s += (size_t)2 * R * ((L + 3) & ~3) * 4;
+  if (staged) s += (size_t)(staged_dI ? 2 : 1) * R * ((L + 3) & ~3) * 4;
   return std::max<size_t>(s, 2 * NBUCKET * 4);
 }
 
@@ -732,8 +742,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     u.cpb = (lay.nbpb + kSortBlocks - 1) / kSortBlocks;
     u.ids_global = a.ids_global;
     u.select = select;
-    union_geometry(a.S_k, a.L, u.W, u.dcap, u.staged);
-    const size_t sh = union_smem_bytes(u.W, u.dcap, a.L, u.staged);
+    union_geometry(a.S_k, a.L, u.W, u.dcap, u.staged, u.staged_dI);
+    const size_t sh = union_smem_bytes(u.W, u.dcap, a.L, u.staged, u.staged_dI);
     // (its static arrays come on top of the dynamic bytes: always raise the limit)
     if (!set_smem_attr((const void*)union_kernel, sh, g_attr_union)) return cudaErrorInvalidValue;
     // it reads the ids before its predecessor completes and dI only after
