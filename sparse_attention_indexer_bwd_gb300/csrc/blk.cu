@@ -213,8 +213,15 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
         for (int i = lane; i < s_cnt[row]; i += 32) drr[i] = 0.f;
         __syncwarp();
       }
-      for (int j0 = dup ? 0 : 32 * hlf; j0 < p.L; j0 += dup ? 32 : 64) {
+      // dI read from global memory one step ahead (the steps of a row with
+      // repeats run in order)
+      const int jstep = dup ? 32 : 64;
+      auto dI_at = [&](int j) { return j < p.L ? (p.staged_dI ? dr_in[j] : __ldg(dr_in + j)) : 0.f; };
+      float vnext = dI_at((dup ? 0 : 32 * hlf) + lane);
+      for (int j0 = dup ? 0 : 32 * hlf; j0 < p.L; j0 += jstep) {
         const int j = j0 + lane;
+        const float vj = vnext;
+        vnext = dI_at(j + jstep);
         int rank = -1;
         float v = 0.f;
         if (j < p.L) {
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
           const unsigned x = (unsigned)(s - w0);
           if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
             rank = pfr[x >> 5] + __popc(bmr[x >> 5] & ((1u << (x & 31)) - 1u));
-            v = p.staged_dI ? dr_in[j] : __ldg(dr_in + j);
+            v = vj;
           }
         }
         if (!dup) {
