@@ -213,43 +213,52 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
         for (int i = lane; i < s_cnt[row]; i += 32) drr[i] = 0.f;
         __syncwarp();
       }
-      // dI read from global memory one step ahead (the steps of a row with
-      // repeats run in order)
+      // NBT steps at a time: their ids, ranks and dI (from global memory for
+      // long rows) are all read before any is used, so the loads overlap;
+      // the steps are then taken in order (a row with repeats sums in slot
+      // order)
+      constexpr int NBT = 4;
       const int jstep = dup ? 32 : 64;
-      auto dI_at = [&](int j) { return j < p.L ? (p.staged_dI ? dr_in[j] : __ldg(dr_in + j)) : 0.f; };
-      float vnext = dI_at((dup ? 0 : 32 * hlf) + lane);
-      for (int j0 = dup ? 0 : 32 * hlf; j0 < p.L; j0 += jstep) {
-        const int j = j0 + lane;
-        const float vj = vnext;
-        vnext = dI_at(j + jstep);
-        int rank = -1;
-        float v = 0.f;
-        if (j < p.L) {
-          const int s = (int)((unsigned)ir[j] - off);
-          const unsigned x = (unsigned)(s - w0);
-          if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
-            rank = pfr[x >> 5] + __popc(bmr[x >> 5] & ((1u << (x & 31)) - 1u));
-            v = vj;
-          }
-        }
-        if (!dup) {
-          if (rank >= 0) drr[rank] = v;
-        } else {
-          // the lanes of each lane's group (same key) in lane order: as many
-          // shuffle rounds as the largest group of the step
-          const unsigned grp = __match_any_sync(FULL, rank >= 0 ? rank : -1 - lane);
-          const int rounds = (int)__reduce_max_sync(FULL, (unsigned)__popc(grp));
-          unsigned rest = grp;
-          float sum = 0.f;
-          for (int k = 0; k < rounds; ++k) {
-            const float y = __shfl_sync(FULL, v, rest ? __ffs(rest) - 1 : lane);
-            if (rest) {
-              sum += y;
-              rest &= rest - 1u;
+      for (int j0 = dup ? 0 : 32 * hlf; j0 < p.L; j0 += NBT * jstep) {
+        int rk[NBT];
+        float vv[NBT];
+#pragma unroll
+        for (int t = 0; t < NBT; ++t) {
+          const int j = j0 + t * jstep + lane;
+          rk[t] = -1;
+          vv[t] = 0.f;
+          if (j < p.L) {
+            const int s = (int)((unsigned)ir[j] - off);
+            const unsigned x = (unsigned)(s - w0);
+            if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
+              rk[t] = pfr[x >> 5] + __popc(bmr[x >> 5] & ((1u << (x & 31)) - 1u));
+              vv[t] = p.staged_dI ? dr_in[j] : __ldg(dr_in + j);
             }
           }
-          if (rank >= 0 && (grp & ((1u << lane) - 1u)) == 0u) drr[rank] += sum;
-          __syncwarp();
+        }
+#pragma unroll
+        for (int t = 0; t < NBT; ++t) {
+          const int rank = rk[t];
+          const float v = vv[t];
+          if (!dup) {
+            if (rank >= 0) drr[rank] = v;
+          } else {
+            // the lanes of each lane's group (same key) in lane order: as
+            // many shuffle rounds as the largest group of the step
+            const unsigned grp = __match_any_sync(FULL, rank >= 0 ? rank : -1 - lane);
+            const int rounds = (int)__reduce_max_sync(FULL, (unsigned)__popc(grp));
+            unsigned rest = grp;
+            float sum = 0.f;
+            for (int k = 0; k < rounds; ++k) {
+              const float y = __shfl_sync(FULL, v, rest ? __ffs(rest) - 1 : lane);
+              if (rest) {
+                sum += y;
+                rest &= rest - 1u;
+              }
+            }
+            if (rank >= 0 && (grp & ((1u << lane) - 1u)) == 0u) drr[rank] += sum;
+            __syncwarp();
+          }
         }
       }
     }
