@@ -236,27 +236,42 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
             }
           }
         }
+        if (!dup) {
 #pragma unroll
-        for (int t = 0; t < NBT; ++t) {
-          const int rank = rk[t];
-          const float v = vv[t];
-          if (!dup) {
-            if (rank >= 0) drr[rank] = v;
-          } else {
-            // the lanes of each lane's group (same key) in lane order: as
-            // many shuffle rounds as the largest group of the step
-            const unsigned grp = __match_any_sync(FULL, rank >= 0 ? rank : -1 - lane);
-            const int rounds = (int)__reduce_max_sync(FULL, (unsigned)__popc(grp));
-            unsigned rest = grp;
-            float sum = 0.f;
-            for (int k = 0; k < rounds; ++k) {
-              const float y = __shfl_sync(FULL, v, rest ? __ffs(rest) - 1 : lane);
-              if (rest) {
-                sum += y;
-                rest &= rest - 1u;
+          for (int t = 0; t < NBT; ++t)
+            if (rk[t] >= 0) drr[rk[t]] = vv[t];
+        } else {
+          // per step, the lanes of each lane's group (same key) in lane
+          // order: as many shuffle rounds as the step's largest group; the
+          // steps' groups are independent, their additions into the sums
+          // are made in step order
+          unsigned grp[NBT];
+#pragma unroll
+          for (int t = 0; t < NBT; ++t) grp[t] = __match_any_sync(FULL, rk[t] >= 0 ? rk[t] : -1 - lane);
+          int rounds = 0;
+#pragma unroll
+          for (int t = 0; t < NBT; ++t) rounds = max(rounds, __popc(grp[t]));
+          rounds = (int)__reduce_max_sync(FULL, (unsigned)rounds);
+          float sum[NBT];
+          unsigned rest[NBT];
+#pragma unroll
+          for (int t = 0; t < NBT; ++t) {
+            sum[t] = 0.f;
+            rest[t] = grp[t];
+          }
+          for (int k = 0; k < rounds; ++k) {
+#pragma unroll
+            for (int t = 0; t < NBT; ++t) {
+              const float y = __shfl_sync(FULL, vv[t], rest[t] ? __ffs(rest[t]) - 1 : lane);
+              if (rest[t]) {
+                sum[t] += y;
+                rest[t] &= rest[t] - 1u;
               }
             }
-            if (rank >= 0 && (grp & ((1u << lane) - 1u)) == 0u) drr[rank] += sum;
+          }
+#pragma unroll
+          for (int t = 0; t < NBT; ++t) {
+            if (rk[t] >= 0 && (grp[t] & ((1u << lane) - 1u)) == 0u) drr[rk[t]] += sum[t];
             __syncwarp();
           }
         }
