@@ -180,14 +180,25 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
     __syncthreads();
     bool dup = false;
     if (own) {
-      for (int j = lane + 32 * hlf; j < p.L; j += 64) {
-        const int s = (int)((unsigned)ir[j] - off);
-        const unsigned x = (unsigned)(s - w0);
-        if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) {
-          const uint32_t bit = 1u << (x & 31);
-          const uint32_t old = atomicOr(&bm[row * WW + (x >> 5)], bit);
-          dup |= (old & bit) != 0u;
+      // four slots' atomics in flight at a time
+      for (int j0 = lane + 32 * hlf; j0 < p.L; j0 += 4 * 64) {
+        unsigned xs[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int j = j0 + 64 * t;
+          xs[t] = 0xFFFFFFFFu;
+          if (j < p.L) {
+            const int s = (int)((unsigned)ir[j] - off);
+            const unsigned x = (unsigned)(s - w0);
+            if ((unsigned)s < (unsigned)p.S_k && x < (unsigned)p.W) xs[t] = x;
+          }
         }
+        uint32_t old[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          old[t] = xs[t] != 0xFFFFFFFFu ? atomicOr(&bm[row * WW + (xs[t] >> 5)], 1u << (xs[t] & 31)) : 0u;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) dup |= xs[t] != 0xFFFFFFFFu && ((old[t] >> (xs[t] & 31)) & 1u);
       }
     }
     dup = __any_sync(FULL, dup);
@@ -281,21 +292,34 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
     // the union's entries of this window, in ascending key order: a warp
     // takes one bitmap word at a time and lane l its bit l, so the set lanes
     // write consecutive entries
+    // (every shared read of a word comes before its global stores, so the
+    // reads overlap)
     for (int i = warp; i < WW; i += UT / 32) {
       const uint32_t m = bm[4 * WW + i];
-      if (!((m >> lane) & 1u)) continue;
+      const bool on = (m >> lane) & 1u;
       const uint32_t below = (1u << lane) - 1u;
-      const int ug = base + pf[4 * WW + i] + __popc(m & below);
+      const int pu = pf[4 * WW + i];
+      uint32_t mr[R];
+      int pr[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        mr[r] = bm[r * WW + i];
+        pr[r] = pf[r * WW + i];
+      }
+      float d[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        d[r] = (on && ((mr[r] >> lane) & 1u)) ? drow[r * p.dcap + pr[r] + __popc(mr[r] & below)] : 0.f;
+      if (!on) continue;
+      const int ug = base + pu + __popc(m & below);
       char* rb = p.rec + ((long long)b * p.tcap + (ug >> 7)) * p.rstride;
       reinterpret_cast<int*>(rb + REC_KEY)[ug & 127] = w0 + 32 * i + lane;
       if (p.hist) atomicAdd(p.hist + ((long long)bb * p.cpb + jb / kSortBlocks) * p.S_k + w0 + 32 * i + lane, 1);
       float* dd = reinterpret_cast<float*>(rb + REC_DIS);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const uint32_t mr = bm[r * WW + i];
-        const float d = ((mr >> lane) & 1u) ? drow[r * p.dcap + pf[r * WW + i] + __popc(mr & below)] : 0.f;
-        dd[r * 128 + (ug & 127)] = d;
-        dmax[r] = fmaxf(dmax[r], fabsf(d));
+        dd[r * 128 + (ug & 127)] = d[r];
+        dmax[r] = fmaxf(dmax[r], fabsf(d[r]));
       }
     }
     base += s_cnt[4];
