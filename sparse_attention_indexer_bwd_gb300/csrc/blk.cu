@@ -619,7 +619,8 @@ __global__ void dk_to_bf16_kernel(const float* __restrict__ dk, uint16_t* __rest
 
 // Key window of the union pass and the dedup capacity per row (both bounded
 // so that its shared memory stays under ~104 KB for any shape), and whether
-// the block's rows are staged in shared memory (rows of up to 2048 slots).
+// the block's id rows (rows of up to 2048 slots) and dI rows (up to 1024) are
+// staged in shared memory.
 void union_geometry(int S_k, int L, int& W, int& dcap, int& staged, int& staged_dI) {
   const long long skr = ((long long)S_k + 1023) / 1024 * 1024;
   W = (int)std::min<long long>(skr, L <= 4096 ? 32768 : 4096);
