@@ -22,12 +22,13 @@
 // leaves TMEM transposed (lane = column d) for full-line reductions.
 //
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
-//   0-3   gather;  4 scan (row ids and dI staged by bulk copies one row
-//   ahead, compaction into tile metadata);  5 MMA issuer and TMEM owner;
-//   6-7   Q loader (the row's q by one bulk copy, then fp16 conversion);
-//   8-15 dz (two groups of four for heads 0-31 / 32-63: dW partials, fp16
-//   dz tile, dW reduction and the dQ epilogue);  16-23 dK (fp32
-//   red.global.add of the transposed tile rows).
+//   0-3   gather, and each row's dQ epilogue (the dz warps' when every row
+//   is one tile);  4 scan (row ids and dI
+//   staged by bulk copies one row ahead, compaction into tile metadata);
+//   5 MMA issuer and TMEM owner;  6-7 Q loader (the row's q by one bulk
+//   copy, then fp16 conversion);  8-15 dz (two groups of four for heads
+//   0-31 / 32-63: dW partials, fp16 dz tile, dW reduction);  16-23 dK
+//   (fp32 red.global.add of the transposed tile rows).
 // Every mbarrier wait is bounded: on expiry the kernel raises a status bit,
 // all roles unwind, in-flight copies and MMAs are drained and TMEM is freed.
 #include <algorithm>
@@ -384,23 +385,81 @@ done:
     drain_wait(&cx.bars->rowfull[staged_wait & 1], (uint32_t)((staged_wait >> 1) & 1), p.status, p.wait_ns);
 }
 
+// ------------------------------------------------------- dQ epilogue ----
+// Row `iq` of this CTA (query row r, scale 2^c) leaves its dQ accumulator:
+// a group of four warps (warp w reads TMEM lanes 32w .. 32w+31, the columns
+// d of dQ) stores heads h0 .. h0 + NH - 1 as dQ[r, h, d] = acc * 2^-c, one
+// 128-byte line per head and warp: the four gather warps all 64 heads (NH =
+// 64, in loads of 32 columns), or each of the two dz groups its 32 (NH = 32,
+// in loads of 16).
+template <int NH>
+__device__ __forceinline__ bool dq_epilogue(const KParams& p, const Ctx& cx, long long iq, int r, int c, int h0) {
+  constexpr int NL = NH / 2;  // columns per TMEM load
+  const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return false;
+  tc_fence_after();
+  const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + h0;
+  const float sc = pow2f(-c);
+  const int d = qw * 32 + lane;  // TMEM lane = column of dQ
+  float* dst = p.dq + (long long)r * p.H * p.D + d;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float v[NL];
+    if constexpr (NL == 32) {
+      tmem_ld32(ta + half * NL, v);
+      tmem_wait_ld_dep(v);
+    } else {
+      tmem_ld16(ta + half * NL, v);
+      tmem_wait_ld_dep16(v);
+    }
+    if (half == 1) {
+      tc_fence_before();
+      mbar_arrive(&cx.bars->dqempty[iq & 1]);
+    }
+    if (d < p.D) {
+#pragma unroll
+      for (int h = 0; h < NL; ++h) {
+        const int hh = h0 + half * NL + h;
+        if (hh < p.H) dst[(long long)hh * p.D] = v[h] * sc;
+      }
+    }
+  }
+  return true;
+}
+
 // --------------------------------------------------------------- gather ---
 // Thread x copies chunk (x % 16) of rows (x / 16) + 8i, i = 0..15: every warp
 // instruction moves two whole 256-byte key rows.  Row r of the tile lands in
 // the 128-byte-swizzle layout: half (chunk / 8), XOR (chunk % 8) ^ (r % 8).
 // Each thread's copies arrive on the stage barrier when they land.
+// Unless every row is one tile (kOneTile: the dz warps store dQ then), the
+// same warps store each row's dQ: once tile g's K stage is free again, the dQ
+// MMA of tile g - KST has completed, and if that tile ended its row the row's
+// accumulator is complete; its store overlaps tile g's copies.
+template <bool kOneTile>
 __device__ void gather_role(const KParams& p, const Ctx& cx) {
   const int x = threadIdx.x - W_GATHER0 * 32;  // 0..127
   const int rsub = x >> 4, ch = x & 15;
   const uint32_t dst_off = (ch >> 3) * KHALF_BYTES + rsub * 128 + (((ch & 7) ^ rsub) << 4);
-  for (int g = 0;; ++g) {
+  // the last KST tiles, oldest first: query row, scale exponent, row-end
+  // flag, row number in this CTA
+  int hr[KST], hc[KST];
+  bool hlast[KST];
+  long long hiq[KST];
+#pragma unroll
+  for (int i = 0; i < KST; ++i) hlast[i] = false;
+  long long iq = -1;
+  bool ok = true;
+  int g = 0;
+  for (;; ++g) {
     const int ms = g % MST;
-    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) break;
+    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) { ok = false; break; }
     const TileMeta& M = cx.meta[ms];
     const int count = M.count, flags = M.flags;
     const long long b = M.r / p.S_q;
+    if (flags & F_FIRST) ++iq;
     const int st = g % KST;
-    if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) break;
+    if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) { ok = false; break; }
     const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES + dst_off;
     const __half* kb = p.k16 + b * (p.S_k + 1) * kDP + ch * 8;
     int key[kBM / 8];
@@ -413,7 +472,30 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
     for (int i = 0; i < kBM / 8; ++i) cp_async16(kbase + i * 1024, kb + (long long)key[i] * kDP, 16);
     cp_async_mbar_arrive_noinc(&cx.bars->kfull[st]);
     if (x == 0) RTRACE(RV_GATHER, g);
+    // tile g - KST: its row's dQ, if it ended the row (the history is a
+    // shift register, so that it stays in registers)
+    if (!kOneTile && hlast[0]) {
+      if (!dq_epilogue<64>(p, cx, hiq[0], hr[0], hc[0], 0)) { ok = false; break; }
+      if (x == 0) RTRACE(RV_EPI_DONE, g - KST);
+    }
+#pragma unroll
+    for (int i = 0; i + 1 < KST; ++i) {
+      hr[i] = hr[i + 1];
+      hc[i] = hc[i + 1];
+      hlast[i] = hlast[i + 1];
+      hiq[i] = hiq[i + 1];
+    }
+    hr[KST - 1] = M.r;
+    hc[KST - 1] = M.c;
+    hlast[KST - 1] = (flags & F_LAST) != 0;
+    hiq[KST - 1] = iq;
     if (flags & F_END) break;
+  }
+  // the rows of the last KST tiles, in order
+  if (!kOneTile && ok) {
+#pragma unroll
+    for (int i = 0; i < KST; ++i)
+      if (hlast[i] && !dq_epilogue<64>(p, cx, hiq[i], hr[i], hc[i], 0)) break;
   }
   // copies in flight must land before the CTA can exit
   cp_async_wait_all();
@@ -452,60 +534,82 @@ __device__ __forceinline__ void mma_dq(const Ctx& cx, int g, int qd, bool first)
     umma_f16_elect(d, a0 + ((k * 2048) >> 4), b0 + ((k * 2048) >> 4), ID_DQ, (first && k == 0) ? 0u : 1u);
 }
 
+// Tile g's MMAs are dK then dQ; Z of tile g+1 goes into the other Z buffer.
+// That Z is issued as soon as its inputs (tile metadata, K tile, the row's
+// Q operand, a free Z buffer) are ready: before tile g's dK when they already
+// are, so the dz warps find it waiting, else between dK and dQ, else after
+// dQ.  So tile g's dQ, and the release of its K stage, dz tile and (for the
+// row's last tile) Q buffer behind it, never wait on the next tile's inputs:
+// with one-tile rows those inputs are what that release makes room for.
 __device__ void mma_role(const KParams& p, const Ctx& cx) {
   Bars* B = cx.bars;
   int g = 0;
   long long iq = 0;
-  if (!WAITW(&B->mfull[0], 0)) goto drain;
-  {
-    int flags = cx.meta[0].flags;
-    if (!WAITW(&B->qfull[0], 0) || !WAITW(&B->kfull[0], 0)) goto drain;
+  int flags = 0, nflags = 0;
+  long long niq = 0;
+  bool zn = false;  // Z of tile g+1 issued
+  // Z of tile g1 = g + 1 when its inputs are ready; `block` waits for them,
+  // otherwise a test that does not wait.  Returns -1 once a wait gave up.
+  auto try_z = [&](bool block) -> int {
+    const int g1 = g + 1;
+    if (block) {
+      if (!WAITW(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) return -1;
+    } else if (!__all_sync(0xffffffffu, mbar_test(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1)))) {
+      return 0;
+    }
+    const int nf = cx.meta[g1 % MST].flags;
+    const long long ni = iq + ((nf & F_FIRST) ? 1 : 0);
+    auto ready = [&](uint64_t* bar, uint32_t par) -> int {
+      if (block) return WAITW(bar, par) ? 1 : -1;
+      return __all_sync(0xffffffffu, mbar_test(bar, par)) ? 1 : 0;
+    };
+    int st = (nf & F_FIRST) ? ready(&B->qfull[ni & 1], (uint32_t)((ni >> 1) & 1)) : 1;
+    if (st == 1) st = ready(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1));
+    if (st == 1) st = ready(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1));
+    if (st != 1) return st;
     // the key tile was written by cp.async (generic proxy): order it before
     // the tensor core's reads
     fence_proxy_async_smem();
     tc_fence_after();
-    mma_z(cx, 0, 0);
-    umma_commit_elect(&B->zfull[0]);
-    RTRACE(RV_MMA_Z, 0);
-    for (;;) {
-      int nflags = 0;
-      long long niq = iq;
-      // the dK MMA of tile g first: the dK warps wait for it
-      if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
-      if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
-      tc_fence_after();
-      mma_dk(cx, g, (int)(iq & 1));
-      umma_commit_elect(&B->dkfull[g & 1]);
-      RTRACE(RV_MMA_DK, g);
-      if (!(flags & F_END)) {
-        // then Z of tile g+1
-        const int g1 = g + 1;
-        if (!WAITW(&B->mfull[g1 % MST], (uint32_t)((g1 / MST) & 1))) goto drain;
-        nflags = cx.meta[g1 % MST].flags;
-        if (nflags & F_FIRST) {
-          niq = iq + 1;
-          if (!WAITW(&B->qfull[niq & 1], (uint32_t)((niq >> 1) & 1))) goto drain;
-        }
-        if (!WAITW(&B->kfull[g1 % KST], (uint32_t)((g1 / KST) & 1))) goto drain;
-        if (!WAITW(&B->zempty[g1 & 1], (uint32_t)(((g1 >> 1) & 1) ^ 1))) goto drain;
-        fence_proxy_async_smem();
-        tc_fence_after();
-        mma_z(cx, g1, (int)(niq & 1));
-        umma_commit_elect(&B->zfull[g1 & 1]);
-        RTRACE(RV_MMA_Z, g1);
-      }
-      if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
-      tc_fence_after();
-      mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
-      RTRACE(RV_MMA_DQ, g);
-      umma_commit_elect(&B->kempty[g % KST]);
-      umma_commit_elect(&B->dzempty[g & 1]);
-      if (flags & F_LAST) umma_commit_elect(&B->dqfull[iq & 1]);
-      if (flags & F_END) break;
-      ++g;
-      flags = nflags;
-      iq = niq;
-    }
+    mma_z(cx, g1, (int)(ni & 1));
+    umma_commit_elect(&B->zfull[g1 & 1]);
+    RTRACE(RV_MMA_Z, g1);
+    nflags = nf;
+    niq = ni;
+    zn = true;
+    return 1;
+  };
+  if (!WAITW(&B->mfull[0], 0)) goto drain;
+  flags = cx.meta[0].flags;
+  if (!WAITW(&B->qfull[0], 0) || !WAITW(&B->kfull[0], 0)) goto drain;
+  fence_proxy_async_smem();
+  tc_fence_after();
+  mma_z(cx, 0, 0);
+  umma_commit_elect(&B->zfull[0]);
+  RTRACE(RV_MMA_Z, 0);
+  for (;;) {
+    const bool more = !(flags & F_END);
+    if (more && try_z(false) < 0) goto drain;
+    if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
+    if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
+    tc_fence_after();
+    mma_dk(cx, g, (int)(iq & 1));
+    umma_commit_elect(&B->dkfull[g & 1]);
+    RTRACE(RV_MMA_DK, g);
+    if (more && !zn && try_z(false) < 0) goto drain;
+    if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
+    tc_fence_after();
+    mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
+    RTRACE(RV_MMA_DQ, g);
+    umma_commit_elect(&B->kempty[g % KST]);
+    umma_commit_elect(&B->dzempty[g & 1]);
+    if (flags & F_LAST) umma_commit_elect(&B->dqfull[iq & 1]);
+    if (!more) break;
+    if (!zn && try_z(true) < 0) goto drain;
+    ++g;
+    flags = nflags;
+    iq = niq;
+    zn = false;
   }
 drain:
   // every MMA issued so far completes before TMEM can be released
@@ -516,33 +620,9 @@ drain:
 
 // ------------------------------------------------------------ dz group ----
 // Group `hg` (0 or 1) owns heads 32*hg .. 32*hg+31 of every tile row.
-__device__ __forceinline__ void dq_epilogue(const KParams& p, const Ctx& cx, int hg, long long iq, int r, int c) {
-  const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-  if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return;
-  tc_fence_after();
-  const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + hg * 32;
-  const float sc = pow2f(-c);
-  const int d = qw * 32 + lane;  // TMEM lane = column of dQ
-  float* dst = p.dq + (long long)r * p.H * p.D + d;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float v[16];
-    tmem_ld16(ta + half * 16, v);
-    tmem_wait_ld_dep16(v);
-    if (half == 1) {
-      tc_fence_before();
-      mbar_arrive(&cx.bars->dqempty[iq & 1]);
-    }
-    if (d < p.D) {
-#pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const int hh = hg * 32 + half * 16 + h;
-        if (hh < p.H) dst[(long long)hh * p.D] = v[h] * sc;
-      }
-    }
-  }
-}
-
+// With kOneTile (every row one tile) the group also stores its 32 heads of
+// the previous row's dQ after each tile's dz, and of the last row at the end.
+template <bool kOneTile>
 __device__ void dz_role(const KParams& p, const Ctx& cx) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int s = qw * 32 + lane;  // tile row = TMEM lane
@@ -551,8 +631,8 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
   float acc[32];
 #pragma unroll
   for (int h = 0; h < 32; ++h) acc[h] = 0.f;
-  long long iq = -1, ep_iq = 0;
-  int ep_r = -1, ep_c = 0;
+  long long iq = -1;
+  int ep_r = -1, ep_c = 0;  // kOneTile: the row whose dQ is stored next
   bool ok = true;
   for (int g = 0;; ++g) {
     const int ms = g % MST;
@@ -606,10 +686,9 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
     if (tdz == 0) RTRACE(RV_DZ_DONE, g);
-    if ((flags & F_FIRST) && ep_r >= 0) {
-      dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
-      ep_r = -1;
-      if (tdz == 0) RTRACE(RV_EPI_DONE, g);
+    if (kOneTile && ep_r >= 0) {
+      if (!dq_epilogue<32>(p, cx, iq - 1, ep_r, ep_c, hg * 32)) { ok = false; break; }
+      if (tdz == 0) RTRACE(RV_EPI_DONE, g - 1);
     }
     if (flags & F_LAST) {
       // dW[t,h] = 2^-c sum over the 128 tile rows of acc[h]: a butterfly
@@ -636,13 +715,14 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
               (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
       }
       if (tdz == 0) RTRACE(RV_DW_DONE, g);
+    }
+    if (kOneTile) {
       ep_r = r;
       ep_c = c;
-      ep_iq = iq;
     }
     if (flags & F_END) break;
   }
-  if (ok && ep_r >= 0) dq_epilogue(p, cx, hg, ep_iq, ep_r, ep_c);
+  if (kOneTile && ok && ep_r >= 0) dq_epilogue<32>(p, cx, iq, ep_r, ep_c, hg * 32);
 }
 
 // ------------------------------------------------------------ dK group ----
@@ -679,6 +759,7 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
   }
 }
 
+template <bool kOneTile>
 __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -715,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
       mbar_init(&B->dkfull[i], 1);
       mbar_init(&B->dkempty[i], NDKT);
       mbar_init(&B->dqfull[i], 1);
-      mbar_init(&B->dqempty[i], NDZT);
+      mbar_init(&B->dqempty[i], kOneTile ? NDZT : NGT);  // the threads that store dQ
       mbar_init(&B->dwred[i], NDZT);
     }
     for (int i = 0; i < RQ; ++i) mbar_init(&B->rowid[i], 1);
@@ -737,7 +818,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
   if (!run) {
     // another kernel serves this call
   } else if (warp < W_SCAN) {
-    gather_role(p, cx);
+    gather_role<kOneTile>(p, cx);
   } else if (warp == W_SCAN) {
     scan_role(p, cx);
   } else if (warp == W_MMA) {
@@ -745,7 +826,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
   } else if (warp < W_DZ0) {
     q_role(p, cx);
   } else if (warp < W_DK0) {
-    dz_role(p, cx);
+    dz_role<kOneTile>(p, cx);
   } else {
     dk_role(p, cx);
   }
@@ -787,7 +868,9 @@ cudaError_t prepare_gemm_rows() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && g_attr_rows[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(gemm_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(gemm_rows_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attr_rows[dev].store(true, std::memory_order_release);
   return e;
 }
@@ -831,7 +914,9 @@ cudaError_t launch_gemm_rows_kernel(const GemmArgs& a, const __half* k16, unsign
              (uintptr_t)a.idx % 16 == 0;
   p.select = select;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
-  return launch_ex(gemm_rows_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
+  // rows of at most 128 slots are one tile each: the dz warps store their dQ
+  if (a.L <= kBM) return launch_ex(gemm_rows_kernel<true>, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
+  return launch_ex(gemm_rows_kernel<false>, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
 }
 
 #ifdef IBWD_TRACE

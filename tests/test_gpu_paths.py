@@ -25,6 +25,7 @@ CASES = [
     W("odd_shapes", 1, 7, 40, 131, 97, 53, "causal", 13),
     W("uniform_small", 1, 16, 64, 130, 512, 256, "uniform", 17),
     W("uniform_sparse", 1, 32, 128, 256, 4096, 128, "uniform", 18),
+    W("short_rows_b2", 2, 64, 128, 200, 300, 96, "causal", 19),  # rows of one tile, two batches
 ]
 
 
