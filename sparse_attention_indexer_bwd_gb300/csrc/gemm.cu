@@ -22,8 +22,8 @@
 // leaves TMEM transposed (lane = column d) for full-line reductions.
 //
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31):
-//   0-3   gather, and each row's dQ epilogue (the dz warps' when every row
-//   is one tile);  4 scan (row ids and dI
+//   0-3   gather, and each row's dQ epilogue (through a staging row and a
+//   bulk copy when every row is one tile);  4 scan (row ids and dI
 //   staged by bulk copies one row ahead, compaction into tile metadata);
 //   5 MMA issuer and TMEM owner;  6-7 Q loader (the row's q by one bulk
 //   copy, then fp16 conversion);  8-15 dz (two groups of four for heads
@@ -48,7 +48,6 @@ constexpr int NGT = 128;                  // gather threads
 constexpr int NQT = 64;                   // Q-loader threads
 constexpr int NDZT = 256;                 // dz threads (two groups of 128)
 constexpr int NDKT = 256;                 // dK threads (two groups of 128)
-constexpr uint32_t ROW_BYTES = 16384;     // one staged row: idx | dI
 
 constexpr uint32_t KTILE_BYTES = kBM * kDP * 2;   // 32 KB
 constexpr uint32_t KHALF_BYTES = kBM * 64 * 2;    // one 64-column half of a K tile
@@ -78,24 +77,34 @@ struct Bars {
   uint64_t dqfull[2], dqempty[2];
   uint64_t dwred[2];
   uint64_t rowid[RQ];
+  uint64_t dqst_free, dqst_full;  // one-tile rows: the dQ staging row
   uint64_t drain;
 };
 
-constexpr uint32_t OFF_K = 0;
-constexpr uint32_t OFF_Q = OFF_K + KST * KTILE_BYTES;
-constexpr uint32_t OFF_DZ = OFF_Q + 2 * QTILE_BYTES;
-constexpr uint32_t OFF_QRAW = OFF_DZ + 2 * DZTILE_BYTES;  // two rows of q as they are (bf16 [H][D])
-constexpr uint32_t OFF_ROW = OFF_QRAW + 2 * QTILE_BYTES;
-constexpr uint32_t OFF_META = OFF_ROW + 2 * ROW_BYTES;
-constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
-constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
-constexpr uint32_t OFF_BARS = OFF_RED + 2 * 4 * kHP * 4;  // [2][4 warps][64 heads]
-constexpr uint32_t OFF_ROWQ = OFF_BARS + sizeof(Bars);  // int[RQ]: rows in this CTA's order, -1 = end
-constexpr uint32_t OFF_DKST = (OFF_ROWQ + RQ * 4 + 15) & ~15u;  // dK transpose stages, 2 KB per dK warp
-constexpr uint32_t OFF_MISC = OFF_DKST + (NDKT / 32) * 16 * 32 * 4;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-static_assert(OFF_BARS % 8 == 0 && OFF_ROW % 16 == 0, "alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// Shared-memory layout.  With rows of one tile (kOneTile: L <= 128) a
+// staged row takes 1 KB instead of 16 KB, and the room holds a row of dQ
+// (fp32 [H][D]) on its way out by one bulk copy.
+template <bool kOneTile>
+struct Geo {
+  static constexpr uint32_t ROW_BYTES = kOneTile ? 1024 : 16384;  // one staged row: idx | dI
+  static constexpr uint32_t DQST_BYTES = kOneTile ? kHP * kDP * 4 : 0;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_Q = OFF_K + KST * KTILE_BYTES;
+  static constexpr uint32_t OFF_DZ = OFF_Q + 2 * QTILE_BYTES;
+  static constexpr uint32_t OFF_QRAW = OFF_DZ + 2 * DZTILE_BYTES;  // two rows of q as they are (bf16 [H][D])
+  static constexpr uint32_t OFF_ROW = OFF_QRAW + 2 * QTILE_BYTES;
+  static constexpr uint32_t OFF_DQST = OFF_ROW + 2 * ROW_BYTES;
+  static constexpr uint32_t OFF_META = OFF_DQST + DQST_BYTES;
+  static constexpr uint32_t OFF_W = OFF_META + MST * sizeof(TileMeta);
+  static constexpr uint32_t OFF_RED = OFF_W + 2 * kHP * 4;
+  static constexpr uint32_t OFF_BARS = OFF_RED + 2 * 4 * kHP * 4;  // [2][4 warps][64 heads]
+  static constexpr uint32_t OFF_ROWQ = OFF_BARS + sizeof(Bars);  // int[RQ]: rows in this CTA's order, -1 = end
+  static constexpr uint32_t OFF_DKST = (OFF_ROWQ + RQ * 4 + 15) & ~15u;  // dK transpose stages, 2 KB per dK warp
+  static constexpr uint32_t OFF_MISC = OFF_DKST + (NDKT / 32) * 16 * 32 * 4;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static_assert(OFF_BARS % 8 == 0 && OFF_ROW % 16 == 0, "alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 struct KParams {
   const uint16_t* q;
@@ -163,7 +172,9 @@ __device__ unsigned long long g_rtrace[RTRACE_CTAS][RV_COUNT][RTRACE_TILES];
 // buffer, issued a row ahead; the loader threads then convert it into the
 // fp16, 128-byte-swizzled Q operand once that buffer is free.  The copy's
 // latency stays off the MMA chain.
+template <bool kOneTile>
 __device__ void q_role(const KParams& p, const Ctx& cx) {
+  using G = Geo<kOneTile>;
   const int tid = threadIdx.x - W_Q0 * 32;  // 0..63
   const uint32_t rowq_bytes = (uint32_t)(p.H * p.D * 2);
   long long issued = -1, landed = -1;  // last rows whose raw copy was issued / waited for
@@ -171,7 +182,7 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
     if (tid == 0) {
       const int b = (int)(i & 1);
       mbar_arrive_expect_tx(&cx.bars->qraw[b], rowq_bytes);
-      bulk_g2s(cx.sbase + OFF_QRAW + b * QTILE_BYTES, p.q + r * p.H * p.D, rowq_bytes, &cx.bars->qraw[b]);
+      bulk_g2s(cx.sbase + G::OFF_QRAW + b * QTILE_BYTES, p.q + r * p.H * p.D, rowq_bytes, &cx.bars->qraw[b]);
     }
     issued = i;
   };
@@ -200,8 +211,8 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
     // once that row's dQ accumulator is complete
     if (i >= 2 && !WAIT(&cx.bars->dqfull[qb], (uint32_t)(((i - 2) >> 1) & 1))) return drain();
     if (tid == 0) RTRACE(RV_Q_FREE, (int)i);
-    const uint8_t* raw = cx.smem + OFF_QRAW + qb * QTILE_BYTES;
-    const uint32_t qs = cx.sbase + OFF_Q + qb * QTILE_BYTES;
+    const uint8_t* raw = cx.smem + G::OFF_QRAW + qb * QTILE_BYTES;
+    const uint32_t qs = cx.sbase + G::OFF_Q + qb * QTILE_BYTES;
     bool bad = false;
 #pragma unroll 4
     for (int it = 0; it < 16; ++it) {
@@ -225,10 +236,12 @@ __device__ void q_role(const KParams& p, const Ctx& cx) {
 }
 
 // ----------------------------------------------------------------- scan ---
+template <bool kOneTile>
 __device__ void scan_role(const KParams& p, const Ctx& cx) {
+  using G = Geo<kOneTile>;
   const int lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  uint8_t* rowbuf = cx.smem + OFF_ROW;
+  uint8_t* rowbuf = cx.smem + G::OFF_ROW;
   long long staged_wait = -1;  // last row whose bulk copy was issued but not yet waited for
   // The CTA's first row is blockIdx.x (the grid never exceeds the row
   // count); later rows are claimed from the shared counter, so CTAs that run
@@ -257,7 +270,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
     if (lane == 0) {
       // this thread's earlier generic reads of the buffer precede the async writes
       fence_proxy_async_smem();
-      const uint32_t dst = smem_u32(rowbuf + buf * ROW_BYTES);
+      const uint32_t dst = smem_u32(rowbuf + buf * G::ROW_BYTES);
       const uint32_t stride = (uint32_t)p.L * 4;  // packed: idx | dI
       mbar_arrive_expect_tx(&cx.bars->rowfull[buf], 2 * stride);
       bulk_g2s(dst, p.idx + r * p.L, stride, &cx.bars->rowfull[buf]);
@@ -284,7 +297,7 @@ __device__ void scan_role(const KParams& p, const Ctx& cx) {
       if (!WAIT(&cx.bars->rowfull[buf], (uint32_t)((i >> 1) & 1))) goto done;
       staged_wait = -1;
       __syncwarp();
-      const uint8_t* rb = rowbuf + buf * ROW_BYTES;
+      const uint8_t* rb = rowbuf + buf * G::ROW_BYTES;
       idx = reinterpret_cast<const int32_t*>(rb);
       dI = reinterpret_cast<const float*>(rb + (uint32_t)p.L * 4);
     } else {
@@ -387,39 +400,30 @@ done:
 
 // ------------------------------------------------------- dQ epilogue ----
 // Row `iq` of this CTA (query row r, scale 2^c) leaves its dQ accumulator:
-// a group of four warps (warp w reads TMEM lanes 32w .. 32w+31, the columns
-// d of dQ) stores heads h0 .. h0 + NH - 1 as dQ[r, h, d] = acc * 2^-c, one
-// 128-byte line per head and warp: the four gather warps all 64 heads (NH =
-// 64, in loads of 32 columns), or each of the two dz groups its 32 (NH = 32,
-// in loads of 16).
-template <int NH>
-__device__ __forceinline__ bool dq_epilogue(const KParams& p, const Ctx& cx, long long iq, int r, int c, int h0) {
-  constexpr int NL = NH / 2;  // columns per TMEM load
+// warp w of the four gather warps reads TMEM lanes 32w .. 32w+31 (the
+// columns d of dQ), all 64 heads, and stores dQ[r, h, d] = acc * 2^-c, one
+// 128-byte line per head and warp.
+__device__ __forceinline__ bool dq_epilogue(const KParams& p, const Ctx& cx, long long iq, int r, int c) {
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return false;
   tc_fence_after();
-  const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64 + h0;
+  const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64;
   const float sc = pow2f(-c);
   const int d = qw * 32 + lane;  // TMEM lane = column of dQ
   float* dst = p.dq + (long long)r * p.H * p.D + d;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    float v[NL];
-    if constexpr (NL == 32) {
-      tmem_ld32(ta + half * NL, v);
-      tmem_wait_ld_dep(v);
-    } else {
-      tmem_ld16(ta + half * NL, v);
-      tmem_wait_ld_dep16(v);
-    }
+    float v[32];
+    tmem_ld32(ta + half * 32, v);
+    tmem_wait_ld_dep(v);
     if (half == 1) {
       tc_fence_before();
       mbar_arrive(&cx.bars->dqempty[iq & 1]);
     }
     if (d < p.D) {
 #pragma unroll
-      for (int h = 0; h < NL; ++h) {
-        const int hh = h0 + half * NL + h;
+      for (int h = 0; h < 32; ++h) {
+        const int hh = half * 32 + h;
         if (hh < p.H) dst[(long long)hh * p.D] = v[h] * sc;
       }
     }
@@ -427,17 +431,70 @@ __device__ __forceinline__ bool dq_epilogue(const KParams& p, const Ctx& cx, lon
   return true;
 }
 
+// The same for one-tile rows: the four warps write the row, scaled, into a
+// staging row laid out as dQ[r] is ([H][D] fp32), and one thread sends it
+// out by one bulk copy (dq is 16-byte aligned and D a multiple of 8 at every
+// entry point, so each row is 16-byte aligned and H*D*4 a multiple of 16).
+// `ne` counts this CTA's staged rows (the staging barriers' phases).
+template <bool kOneTile>
+__device__ __forceinline__ bool dq_epilogue_staged(const KParams& p, const Ctx& cx, long long iq, int r, int c,
+                                                   long long ne) {
+  using G = Geo<kOneTile>;
+  const int x = threadIdx.x - W_GATHER0 * 32, qw = x >> 5, lane = x & 31;
+  if (!WAIT(&cx.bars->dqfull[iq & 1], (uint32_t)((iq >> 1) & 1))) return false;
+  // the staging row is free once the previous row's bulk copy has read it
+  if (x == 0) {
+    bulk_wait_read<0>();
+    mbar_arrive(&cx.bars->dqst_free);
+  }
+  if (!WAIT(&cx.bars->dqst_free, (uint32_t)(ne & 1))) return false;
+  tc_fence_after();
+  const uint32_t ta = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_DQ + (uint32_t)(iq & 1) * 64;
+  const float sc = pow2f(-c);
+  const int d = qw * 32 + lane;  // TMEM lane = column of dQ
+  float* st = reinterpret_cast<float*>(cx.smem + G::OFF_DQST) + d;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float v[32];
+    tmem_ld32(ta + half * 32, v);
+    tmem_wait_ld_dep(v);
+    if (half == 1) {
+      tc_fence_before();
+      mbar_arrive(&cx.bars->dqempty[iq & 1]);
+    }
+    if (d < p.D) {
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        const int hh = half * 32 + h;
+        if (hh < p.H) st[hh * p.D] = v[h] * sc;
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  mbar_arrive(&cx.bars->dqst_full);
+  bool ok = true;
+  if (x == 0) {
+    ok = mbar_wait(&cx.bars->dqst_full, (uint32_t)(ne & 1), cx.abort, p.status, p.wait_ns);
+    if (ok) {
+      bulk_s2g(p.dq + (long long)r * p.H * p.D, cx.sbase + G::OFF_DQST, (uint32_t)(p.H * p.D * 4));
+      bulk_commit();
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0);
+}
+
 // --------------------------------------------------------------- gather ---
 // Thread x copies chunk (x % 16) of rows (x / 16) + 8i, i = 0..15: every warp
 // instruction moves two whole 256-byte key rows.  Row r of the tile lands in
 // the 128-byte-swizzle layout: half (chunk / 8), XOR (chunk % 8) ^ (r % 8).
 // Each thread's copies arrive on the stage barrier when they land.
-// Unless every row is one tile (kOneTile: the dz warps store dQ then), the
-// same warps store each row's dQ: once tile g's K stage is free again, the dQ
-// MMA of tile g - KST has completed, and if that tile ended its row the row's
-// accumulator is complete; its store overlaps tile g's copies.
+// The same warps store each row's dQ (through the staging row when every
+// row is one tile): once tile g's K stage is free
+// again, the dQ MMA of tile g - KST has completed, and if that tile ended its
+// row the row's accumulator is complete; its store overlaps tile g's copies.
 template <bool kOneTile>
 __device__ void gather_role(const KParams& p, const Ctx& cx) {
+  using G = Geo<kOneTile>;
   const int x = threadIdx.x - W_GATHER0 * 32;  // 0..127
   const int rsub = x >> 4, ch = x & 15;
   const uint32_t dst_off = (ch >> 3) * KHALF_BYTES + rsub * 128 + (((ch & 7) ^ rsub) << 4);
@@ -448,9 +505,14 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
   long long hiq[KST];
 #pragma unroll
   for (int i = 0; i < KST; ++i) hlast[i] = false;
-  long long iq = -1;
+  long long iq = -1, ne = 0;
   bool ok = true;
   int g = 0;
+  // the row's dQ: staged (counting the staged rows) or stored directly
+  auto epilogue = [&](long long eiq, int er, int ec) -> bool {
+    if constexpr (kOneTile) return dq_epilogue_staged<kOneTile>(p, cx, eiq, er, ec, ne++);
+    return dq_epilogue(p, cx, eiq, er, ec);
+  };
   for (;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) { ok = false; break; }
@@ -460,7 +522,7 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
     if (flags & F_FIRST) ++iq;
     const int st = g % KST;
     if (!WAIT(&cx.bars->kempty[st], (uint32_t)(((g / KST) & 1) ^ 1))) { ok = false; break; }
-    const uint32_t kbase = cx.sbase + OFF_K + st * KTILE_BYTES + dst_off;
+    const uint32_t kbase = cx.sbase + G::OFF_K + st * KTILE_BYTES + dst_off;
     const __half* kb = p.k16 + b * (p.S_k + 1) * kDP + ch * 8;
     int key[kBM / 8];
 #pragma unroll
@@ -474,8 +536,8 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
     if (x == 0) RTRACE(RV_GATHER, g);
     // tile g - KST: its row's dQ, if it ended the row (the history is a
     // shift register, so that it stays in registers)
-    if (!kOneTile && hlast[0]) {
-      if (!dq_epilogue<64>(p, cx, hiq[0], hr[0], hc[0], 0)) { ok = false; break; }
+    if (hlast[0]) {
+      if (!epilogue(hiq[0], hr[0], hc[0])) { ok = false; break; }
       if (x == 0) RTRACE(RV_EPI_DONE, g - KST);
     }
 #pragma unroll
@@ -492,13 +554,14 @@ __device__ void gather_role(const KParams& p, const Ctx& cx) {
     if (flags & F_END) break;
   }
   // the rows of the last KST tiles, in order
-  if (!kOneTile && ok) {
+  if (ok) {
 #pragma unroll
     for (int i = 0; i < KST; ++i)
-      if (hlast[i] && !dq_epilogue<64>(p, cx, hiq[i], hr[i], hc[i], 0)) break;
+      if (hlast[i] && !epilogue(hiq[i], hr[i], hc[i])) break;
   }
-  // copies in flight must land before the CTA can exit
+  // copies in flight must land (or leave) before the CTA can exit
   cp_async_wait_all();
+  if (kOneTile && x == 0) bulk_wait<0>();
 }
 
 // ------------------------------------------------------------------ MMA ---
@@ -506,9 +569,11 @@ constexpr uint32_t ID_Z = idesc_f16_f32(128, 64, 0, 0);    // Z^T = K . Q^T
 constexpr uint32_t ID_DKT = idesc_f16_f32(128, 128, 1, 0);  // dK^T = Q^T . dz^T (Q as MN-major A)
 constexpr uint32_t ID_DQ = idesc_f16_f32(128, 64, 1, 1);   // dQ^T = K^T . dz (both MN-major)
 
+template <bool kOneTile>
 __device__ __forceinline__ void mma_z(const Ctx& cx, int g, int qb) {
-  const uint64_t a0 = sw128_desc(cx.sbase + OFF_K + (g % KST) * KTILE_BYTES, 16, 1024);
-  const uint64_t b0 = sw128_desc(cx.sbase + OFF_Q + qb * QTILE_BYTES, 16, 1024);
+  using G = Geo<kOneTile>;
+  const uint64_t a0 = sw128_desc(cx.sbase + G::OFF_K + (g % KST) * KTILE_BYTES, 16, 1024);
+  const uint64_t b0 = sw128_desc(cx.sbase + G::OFF_Q + qb * QTILE_BYTES, 16, 1024);
   const uint32_t d = cx.tmem + TM_Z + (g & 1) * 64;
 #pragma unroll
   for (int k = 0; k < 8; ++k)  // K = D = 128 in steps of 16
@@ -516,18 +581,22 @@ __device__ __forceinline__ void mma_z(const Ctx& cx, int g, int qb) {
                    b0 + (((k >> 2) * QHALF_BYTES + (k & 3) * 32) >> 4), ID_Z, k > 0);
 }
 
+template <bool kOneTile>
 __device__ __forceinline__ void mma_dk(const Ctx& cx, int g, int qb) {
-  const uint64_t a0 = sw128_desc(cx.sbase + OFF_Q + qb * QTILE_BYTES, QHALF_BYTES, 1024);  // Q^T: M = d, MN-major
-  const uint64_t b0 = sw128_desc(cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES, 16, 1024);    // dz^T: N = s, K-major
+  using G = Geo<kOneTile>;
+  const uint64_t a0 = sw128_desc(cx.sbase + G::OFF_Q + qb * QTILE_BYTES, QHALF_BYTES, 1024);  // Q^T: M = d, MN-major
+  const uint64_t b0 = sw128_desc(cx.sbase + G::OFF_DZ + (g & 1) * DZTILE_BYTES, 16, 1024);    // dz^T: N = s, K-major
   const uint32_t d = cx.tmem + TM_DK + (g & 1) * 128;
 #pragma unroll
   for (int k = 0; k < 4; ++k)  // K = H = 64 in steps of 16
     umma_f16_elect(d, a0 + ((k * 2048) >> 4), b0 + ((k * 32) >> 4), ID_DKT, k > 0);
 }
 
+template <bool kOneTile>
 __device__ __forceinline__ void mma_dq(const Ctx& cx, int g, int qd, bool first) {
-  const uint64_t a0 = sw128_desc(cx.sbase + OFF_K + (g % KST) * KTILE_BYTES, KHALF_BYTES, 1024);
-  const uint64_t b0 = sw128_desc(cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES, DZTILE_BYTES, 1024);
+  using G = Geo<kOneTile>;
+  const uint64_t a0 = sw128_desc(cx.sbase + G::OFF_K + (g % KST) * KTILE_BYTES, KHALF_BYTES, 1024);
+  const uint64_t b0 = sw128_desc(cx.sbase + G::OFF_DZ + (g & 1) * DZTILE_BYTES, DZTILE_BYTES, 1024);
   const uint32_t d = cx.tmem + TM_DQ + qd * 64;
 #pragma unroll
   for (int k = 0; k < 8; ++k)  // K = 128 keys in steps of 16
@@ -541,7 +610,9 @@ __device__ __forceinline__ void mma_dq(const Ctx& cx, int g, int qd, bool first)
 // dQ.  So tile g's dQ, and the release of its K stage, dz tile and (for the
 // row's last tile) Q buffer behind it, never wait on the next tile's inputs:
 // with one-tile rows those inputs are what that release makes room for.
+template <bool kOneTile>
 __device__ void mma_role(const KParams& p, const Ctx& cx) {
+  using G = Geo<kOneTile>;
   Bars* B = cx.bars;
   int g = 0;
   long long iq = 0;
@@ -571,7 +642,7 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
     // the tensor core's reads
     fence_proxy_async_smem();
     tc_fence_after();
-    mma_z(cx, g1, (int)(ni & 1));
+    mma_z<kOneTile>(cx, g1, (int)(ni & 1));
     umma_commit_elect(&B->zfull[g1 & 1]);
     RTRACE(RV_MMA_Z, g1);
     nflags = nf;
@@ -584,7 +655,7 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
   if (!WAITW(&B->qfull[0], 0) || !WAITW(&B->kfull[0], 0)) goto drain;
   fence_proxy_async_smem();
   tc_fence_after();
-  mma_z(cx, 0, 0);
+  mma_z<kOneTile>(cx, 0, 0);
   umma_commit_elect(&B->zfull[0]);
   RTRACE(RV_MMA_Z, 0);
   for (;;) {
@@ -593,13 +664,13 @@ __device__ void mma_role(const KParams& p, const Ctx& cx) {
     if (!WAITW(&B->dzfull[g & 1], (uint32_t)((g >> 1) & 1))) goto drain;
     if (!WAITW(&B->dkempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) goto drain;
     tc_fence_after();
-    mma_dk(cx, g, (int)(iq & 1));
+    mma_dk<kOneTile>(cx, g, (int)(iq & 1));
     umma_commit_elect(&B->dkfull[g & 1]);
     RTRACE(RV_MMA_DK, g);
     if (more && !zn && try_z(false) < 0) goto drain;
     if ((flags & F_FIRST) && !WAITW(&B->dqempty[iq & 1], (uint32_t)(((iq >> 1) & 1) ^ 1))) goto drain;
     tc_fence_after();
-    mma_dq(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
+    mma_dq<kOneTile>(cx, g, (int)(iq & 1), (flags & F_FIRST) != 0);
     RTRACE(RV_MMA_DQ, g);
     umma_commit_elect(&B->kempty[g % KST]);
     umma_commit_elect(&B->dzempty[g & 1]);
@@ -620,10 +691,9 @@ drain:
 
 // ------------------------------------------------------------ dz group ----
 // Group `hg` (0 or 1) owns heads 32*hg .. 32*hg+31 of every tile row.
-// With kOneTile (every row one tile) the group also stores its 32 heads of
-// the previous row's dQ after each tile's dz, and of the last row at the end.
 template <bool kOneTile>
 __device__ void dz_role(const KParams& p, const Ctx& cx) {
+  using G = Geo<kOneTile>;
   const int qw = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const int s = qw * 32 + lane;  // tile row = TMEM lane
   const int tdz = threadIdx.x - W_DZ0 * 32;  // 0..255
@@ -632,29 +702,27 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
 #pragma unroll
   for (int h = 0; h < 32; ++h) acc[h] = 0.f;
   long long iq = -1;
-  int ep_r = -1, ep_c = 0;  // kOneTile: the row whose dQ is stored next
-  bool ok = true;
   for (int g = 0;; ++g) {
     const int ms = g % MST;
-    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) { ok = false; break; }
+    if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) break;
     const TileMeta& M = cx.meta[ms];
     const int flags = M.flags, count = M.count, c = M.c, r = M.r;
     if (flags & F_FIRST) {
       ++iq;
 #pragma unroll
       for (int h = 0; h < 32; ++h) acc[h] = 0.f;
-      if (!WAIT(&cx.bars->qfull[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
+      if (!WAIT(&cx.bars->qfull[iq & 1], (uint32_t)((iq >> 1) & 1))) break;
     }
     const float dis = s < count ? M.dis[s] : 0.f;
     // dI 2^c w for this row's 32 heads, as fp32 pairs
     const uint64_t* w2 = reinterpret_cast<const uint64_t*>(cx.w_s + (iq & 1) * kHP + hg * 32);
     const uint64_t dis2 = pack2(__float_as_uint(dis), __float_as_uint(dis));
-    if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) { ok = false; break; }
-    if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
+    if (!WAIT(&cx.bars->zfull[g & 1], (uint32_t)((g >> 1) & 1))) break;
+    if (!WAIT(&cx.bars->dzempty[g & 1], (uint32_t)(((g >> 1) & 1) ^ 1))) break;
     tc_fence_after();
     if (tdz == 0) RTRACE(RV_DZ_START, g);
     const uint32_t za = cx.tmem + ((uint32_t)(qw * 32) << 16) + TM_Z + (uint32_t)(g & 1) * 64 + hg * 32;
-    const uint32_t dzrow = cx.sbase + OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
+    const uint32_t dzrow = cx.sbase + G::OFF_DZ + (g & 1) * DZTILE_BYTES + s * 128;
 #pragma unroll
     for (int zh = 0; zh < 2; ++zh) {
       float z[16];
@@ -686,10 +754,6 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
     fence_proxy_async_smem();
     mbar_arrive(&cx.bars->dzfull[g & 1]);
     if (tdz == 0) RTRACE(RV_DZ_DONE, g);
-    if (kOneTile && ep_r >= 0) {
-      if (!dq_epilogue<32>(p, cx, iq - 1, ep_r, ep_c, hg * 32)) { ok = false; break; }
-      if (tdz == 0) RTRACE(RV_EPI_DONE, g - 1);
-    }
     if (flags & F_LAST) {
       // dW[t,h] = 2^-c sum over the 128 tile rows of acc[h]: a butterfly
       // leaves head 32*hg + lane summed over the warp, then the four warps'
@@ -709,29 +773,26 @@ __device__ void dz_role(const KParams& p, const Ctx& cx) {
       red[qw * kHP + hg * 32 + lane] = acc[0];
       mbar_arrive(&cx.bars->dwred[iq & 1]);
       if (tdz < kHP) {
-        if (!WAIT(&cx.bars->dwred[iq & 1], (uint32_t)((iq >> 1) & 1))) { ok = false; break; }
+        if (!WAIT(&cx.bars->dwred[iq & 1], (uint32_t)((iq >> 1) & 1))) break;
         if (tdz < p.H)
           p.dw[(long long)r * p.H + tdz] =
               (((red[tdz] + red[kHP + tdz]) + red[2 * kHP + tdz]) + red[3 * kHP + tdz]) * pow2f(-c);
       }
       if (tdz == 0) RTRACE(RV_DW_DONE, g);
     }
-    if (kOneTile) {
-      ep_r = r;
-      ep_c = c;
-    }
     if (flags & F_END) break;
   }
-  if (kOneTile && ok && ep_r >= 0) dq_epilogue<32>(p, cx, iq, ep_r, ep_c, hg * 32);
 }
 
 // ------------------------------------------------------------ dK group ----
 // TMEM holds dK^T: lane = column d, TMEM column = tile row.  Group kg owns
 // tile rows 64*kg .. 64*kg+63 in two chunks of 32.
+template <bool kOneTile>
 __device__ void dk_role(const KParams& p, const Ctx& cx) {
+  using G = Geo<kOneTile>;
   const int qw = (threadIdx.x >> 5) & 3;
   const int kg = (threadIdx.x - W_DK0 * 32) >> 7;
-  float* stage = reinterpret_cast<float*>(cx.smem + OFF_DKST) + ((threadIdx.x >> 5) - W_DK0) * (16 * 32);
+  float* stage = reinterpret_cast<float*>(cx.smem + G::OFF_DKST) + ((threadIdx.x >> 5) - W_DK0) * (16 * 32);
   for (int g = 0;; ++g) {
     const int ms = g % MST;
     if (!WAIT(&cx.bars->mfull[ms], (uint32_t)((g / MST) & 1))) return;
@@ -761,18 +822,19 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
 
 template <bool kOneTile>
 __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p) {
+  using G = Geo<kOneTile>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctx cx;
   cx.smem = smem;
   cx.sbase = smem_u32(smem);
-  cx.meta = reinterpret_cast<TileMeta*>(smem + OFF_META);
-  cx.w_s = reinterpret_cast<float*>(smem + OFF_W);
-  cx.red_s = reinterpret_cast<float*>(smem + OFF_RED);
-  cx.bars = reinterpret_cast<Bars*>(smem + OFF_BARS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  cx.abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  cx.rowq = reinterpret_cast<int*>(smem + OFF_ROWQ);
+  cx.meta = reinterpret_cast<TileMeta*>(smem + G::OFF_META);
+  cx.w_s = reinterpret_cast<float*>(smem + G::OFF_W);
+  cx.red_s = reinterpret_cast<float*>(smem + G::OFF_RED);
+  cx.bars = reinterpret_cast<Bars*>(smem + G::OFF_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::OFF_MISC);
+  cx.abort = reinterpret_cast<volatile int*>(smem + G::OFF_MISC + 4);
+  cx.rowq = reinterpret_cast<int*>(smem + G::OFF_ROWQ);
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
@@ -796,10 +858,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
       mbar_init(&B->dkfull[i], 1);
       mbar_init(&B->dkempty[i], NDKT);
       mbar_init(&B->dqfull[i], 1);
-      mbar_init(&B->dqempty[i], kOneTile ? NDZT : NGT);  // the threads that store dQ
+      mbar_init(&B->dqempty[i], NGT);
       mbar_init(&B->dwred[i], NDZT);
     }
     for (int i = 0; i < RQ; ++i) mbar_init(&B->rowid[i], 1);
+    mbar_init(&B->dqst_free, 1);
+    mbar_init(&B->dqst_full, NGT);
     mbar_init(&B->drain, 1);
     *cx.abort = 0;
     fence_barrier_init();
@@ -820,15 +884,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
   } else if (warp < W_SCAN) {
     gather_role<kOneTile>(p, cx);
   } else if (warp == W_SCAN) {
-    scan_role(p, cx);
+    scan_role<kOneTile>(p, cx);
   } else if (warp == W_MMA) {
-    mma_role(p, cx);  // the whole warp runs the loop; one elected lane issues
+    mma_role<kOneTile>(p, cx);  // the whole warp runs the loop; one elected lane issues
   } else if (warp < W_DZ0) {
-    q_role(p, cx);
+    q_role<kOneTile>(p, cx);
   } else if (warp < W_DK0) {
     dz_role<kOneTile>(p, cx);
   } else {
-    dk_role(p, cx);
+    dk_role<kOneTile>(p, cx);
   }
 
   tc_fence_before();
@@ -868,9 +932,10 @@ cudaError_t prepare_gemm_rows() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && g_attr_rows[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_rows_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(gemm_rows_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Geo<false>::SMEM_BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(gemm_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<true>::SMEM_BYTES);
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attr_rows[dev].store(true, std::memory_order_release);
   return e;
 }
@@ -910,13 +975,16 @@ cudaError_t launch_gemm_rows_kernel(const GemmArgs& a, const __half* k16, unsign
   p.D = a.D;
   p.L = a.L;
   // rows are staged in shared memory when they fit and are 16-byte aligned
-  p.staged = 2 * (size_t)a.L * 4 <= ROW_BYTES && a.L % 4 == 0 && (uintptr_t)a.dI % 16 == 0 &&
+  const bool one_tile = a.L <= kBM;
+  p.staged = 2 * (size_t)a.L * 4 <= (one_tile ? Geo<true>::ROW_BYTES : Geo<false>::ROW_BYTES) && a.L % 4 == 0 &&
+             (uintptr_t)a.dI % 16 == 0 &&
              (uintptr_t)a.idx % 16 == 0;
   p.select = select;
   const int grid = (int)std::min<long long>(a.num_sms, p.rows);
   // rows of at most 128 slots are one tile each: the dz warps store their dQ
-  if (a.L <= kBM) return launch_ex(gemm_rows_kernel<true>, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
-  return launch_ex(gemm_rows_kernel<false>, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
+  if (one_tile)
+    return launch_ex(gemm_rows_kernel<true>, (unsigned)grid, (unsigned)NTHREADS, Geo<true>::SMEM_BYTES, st, true, p);
+  return launch_ex(gemm_rows_kernel<false>, (unsigned)grid, (unsigned)NTHREADS, Geo<false>::SMEM_BYTES, st, true, p);
 }
 
 #ifdef IBWD_TRACE
