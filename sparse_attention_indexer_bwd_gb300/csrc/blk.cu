@@ -291,11 +291,13 @@ __global__ void __launch_bounds__(UT, 4) union_kernel(const UParams p) {
     __syncthreads();
     // the union's entries of this window, in ascending key order: a warp
     // takes one bitmap word at a time and lane l its bit l, so the set lanes
-    // write consecutive entries
+    // write consecutive entries; empty words (about half of them for causal
+    // rows) are passed over at once
     // (every shared read of a word comes before its global stores, so the
     // reads overlap)
     for (int i = warp; i < WW; i += UT / 32) {
       const uint32_t m = bm[4 * WW + i];
+      if (m == 0u) continue;  // warp-uniform: one word for all lanes
       const bool on = (m >> lane) & 1u;
       const uint32_t below = (1u << lane) - 1u;
       const int pu = pf[4 * WW + i];
