@@ -50,8 +50,8 @@ GEMM_FILES = ("blk.cu", "blk.h", "blk_pipe.cuh", "blk_pipe.cu", "gemm.cu", "kcom
 SCORE_GRAD_FILES = ("score_grad.cu",)
 PROFILED_TRAFFIC = {
     # k_to_f16 + select + union + q_image + blk + (exiting) per-row kernels of one gemm-stage call
-    ("anchor", "atomic", "gemm_stage"): ("d9b218a80e2aeb4f3cdaed0265c702d1c38eabaee221e14d41b854c882879a98", 1.062e6 + 4.212e6 + 83.791e6 + 218.837e6 + 423.660e6 + 0.071e6),
-    ("anchor", "atomic", "score_grad"): ("32716e0bdb141dfa50987a5d3f34f07eb40acf8a602b202185531f24332fc497", 102.783e6),
+    ("anchor", "atomic", "gemm_stage"): ("6b6c5692434484f4cab0e9b49e8978b00489a5f0502fa5f5758f7fd670ef9824", 1.062e6 + 4.212e6 + 83.763e6 + 218.850e6 + 423.690e6 + 0.070e6),
+    ("anchor", "atomic", "score_grad"): ("32716e0bdb141dfa50987a5d3f34f07eb40acf8a602b202185531f24332fc497", 102.840e6),
 }
 
 

@@ -822,6 +822,13 @@ __device__ void dk_role(const KParams& p, const Ctx& cx) {
 
 template <bool kOneTile>
 __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p) {
+  if (p.select != nullptr) {
+    // the choice was made on the device: the blocked kernel before never
+    // lets this one launch early, so the wait costs nothing, and a call that
+    // kernel served leaves before any setup
+    griddep_wait();
+    if (__ldcg(p.select) != 1u) return;
+  }
   using G = Geo<kOneTile>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -877,11 +884,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_rows_kernel(const KParams p)
   tc_fence_after();
   cx.tmem = *tmem_slot;
   griddep_wait();  // the fp16 copy of k is written by the kernel before
-  const bool run = p.select == nullptr || __ldcg(p.select) == 1u;
 
-  if (!run) {
-    // another kernel serves this call
-  } else if (warp < W_SCAN) {
+  if (warp < W_SCAN) {
     gather_role<kOneTile>(p, cx);
   } else if (warp == W_SCAN) {
     scan_role<kOneTile>(p, cx);
