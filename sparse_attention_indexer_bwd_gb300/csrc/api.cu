@@ -17,7 +17,7 @@ struct DeviceInfo {
   // at the highest priority, so that the images (the later of the two to
   // finish otherwise) take the SMs first as the union pass's CTAs retire
   cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, sel = nullptr;
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -43,7 +43,8 @@ int device_info(DeviceInfo** out) {
       if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
           cudaStreamCreateWithPriority(&d.side, cudaStreamNonBlocking, greatest) != cudaSuccess ||
           cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess)
+          cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&d.sel, cudaEventDisableTiming) != cudaSuccess)
         return IBWD_ERR_CUDA;
     }
     d.ready = true;
@@ -184,7 +185,15 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.side = dv->side;
   a.ev_fork = dv->fork;
   a.ev_join = dv->join;
+  a.ev_sel = dv->sel;
   if (I) {
+    // the gemm stage's work that needs neither dI nor the score-grad's dK
+    // zeroing (k copy, kernel choice, q images) starts beside the score-grad
+    // on the side stream, after everything queued before this call
+    if (cudaEventRecord(dv->fork, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaStreamWaitEvent(dv->side, dv->fork, 0) != cudaSuccess)
+      return IBWD_ERR_CUDA;
+    a.early_side = 1;
     rc = score_grad_common(I, const_cast<float*>(dI), idx, need_idx, B, S_q, S_k, L, grad_scale,
                            mode == IBWD_DK_ATOMIC ? dk : nullptr, D, stream, a.ids_global);
     if (rc) return rc;

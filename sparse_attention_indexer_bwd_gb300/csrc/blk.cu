@@ -650,6 +650,21 @@ unsigned long long test_timeout_ns() {
   return ns < 1000 ? 1000 : (ns > 2000000000ull ? 2000000000ull : ns);
 }
 std::atomic<int> g_attr_union[64];
+std::atomic<int> g_attr_qimg[64];
+
+// The q image kernel asks for the largest shared-memory carveout although it
+// uses none: an SM whose carveout was set for it could not take the union
+// pass's CTAs (~53 KB each at the anchor) beside it until it drained.
+bool set_qimg_carveout() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && g_attr_qimg[dev].load(std::memory_order_acquire)) return true;
+  if (cudaFuncSetAttribute((const void*)q_image_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < 64) g_attr_qimg[dev].store(1, std::memory_order_release);
+  return true;
+}
 
 // Test of the pipeline's ordering: IBWD_TEST_SHALLOW_PIPELINE=1 in the
 // environment runs the gemm kernel built with one K-tile stage and two
@@ -750,23 +765,33 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   unsigned* qmax = a.deterministic ? reinterpret_cast<unsigned*>(ws + lay.qmax) : nullptr;
   // deterministic mode: the key counts and the q maxima (contiguous) start at zero
   const long long nzero = a.deterministic ? (hist ? lay.nchunks * a.S_k : 0LL) + lay.nblocks : 0LL;
-  cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, SCHED_ZERO, a.status, a.after_score_grad != 0,
-                                  a.num_sms, st, a.deterministic ? reinterpret_cast<int*>(ws + lay.hist) : nullptr,
-                                  nzero);
+  // the k copy, the choice and the q images: on the side stream already
+  // forked by a one-call entry point (beside its score-grad), else on the
+  // call's stream with the images forked after the choice
+  const cudaStream_t pre = a.early_side ? a.side : st;
+  cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, SCHED_ZERO, a.status,
+                                  a.after_score_grad != 0 && !a.early_side, a.num_sms, pre,
+                                  a.deterministic ? reinterpret_cast<int*>(ws + lay.hist) : nullptr, nzero);
   if (e != cudaSuccess) return e;
   if (choose) {
     const long long nsample = std::min<long long>(lay.nblocks, 256);
     const long long stride = lay.nblocks / nsample;
     const size_t sh = (size_t)((a.S_k + 31) / 32) * 4;
-    e = launch_ex(select_kernel, (unsigned)nsample, 128u, sh, st, true, static_cast<const int32_t*>(a.idx), a.S_q,
+    e = launch_ex(select_kernel, (unsigned)nsample, 128u, sh, pre, true, static_cast<const int32_t*>(a.idx), a.S_q,
                   a.S_k, a.L, lay.nbpb, stride, sched, forced);
     if (e != cudaSuccess) return e;
   }
   // the q images on the side stream: the union pass (or the dense scale
   // pass) is latency-bound and leaves the memory system mostly idle, so the
   // two overlap; the gemm kernel waits for both
-  e = cudaEventRecord(a.ev_fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(a.side, a.ev_fork, 0);
+  if (a.early_side) {
+    // the union pass reads the choice and the zeroed counters
+    e = cudaEventRecord(a.ev_sel, a.side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, a.ev_sel, 0);
+  } else {
+    e = cudaEventRecord(a.ev_fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(a.side, a.ev_fork, 0);
+  }
   if (e != cudaSuccess) return e;
   {
     const QImg qi{a.q, qimg, qmax, lay.nblocks, a.S_q, a.H, a.D, lay.nbpb};
@@ -774,6 +799,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     // four CTAs per SM: the union pass keeps three of its four while both run
     // (measured: 30 us faster than two CTAs per SM at the anchor)
     const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 4LL * a.num_sms));
+    if (!set_qimg_carveout()) return cudaErrorInvalidValue;
     q_image_kernel<<<blocks, 256, 0, a.side>>>(qi, a.status, select);
     e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaEventRecord(a.ev_join, a.side);

@@ -65,6 +65,12 @@ struct GemmArgs {
   float sm_scale;        // logit scale s (> 0; 0 reads as 1): dq, dw, dk are s times the unscaled results
   cudaStream_t side;     // a second stream of the device, forked from and joined to the call's stream
   cudaEvent_t ev_fork, ev_join;
+  // set by the one-call entry points, which fork the side stream before
+  // their score-grad: the k copy, the kernel choice and the q images then run
+  // on it beside the score-grad, and ev_sel (recorded after the choice) holds
+  // back the union pass until the choice is made
+  int early_side;
+  cudaEvent_t ev_sel;
 };
 
 // Workspace of the gemm stage (indexer_bwd_gemm and the one-call forms).
