@@ -430,11 +430,14 @@ cudaError_t launch_score_grad(const ScoreGradArgs& a, cudaStream_t st) {
   const bool aligned = (a.L % 4 == 0) && ((uintptr_t)a.index_score % 16 == 0) &&
                        ((uintptr_t)a.attn_score % 16 == 0) && (!a.idx || (uintptr_t)a.idx % 16 == 0) &&
                        (!a.dk_zero || (uintptr_t)a.dk_zero % 16 == 0);
-  // rows of 128..2048 slots (sparse) or 128..4096 (dense), a multiple of 128:
-  // the staged kernel (one float4 per thread per array; two beyond 2048 slots)
+  // rows of 256..2048 slots (sparse) or 256..4096 (dense), a multiple of 128:
+  // the staged kernel (one float4 per thread per array; two beyond 2048
+  // slots).  Shorter rows are packed eight to a CTA, one warp each, in
+  // registers (vec<1, 1>: 19 against 22 us for the staged kernel's one-warp
+  // CTAs at uniform top-128)
   const int lmax = a.idx ? 2048 : 4096;
   const int nv = a.L > 2048 ? 2 : 1;
-  if (aligned && a.L % (128 * nv) == 0 && a.L >= 128 && a.L <= lmax && a.status && a.num_sms > 0) {
+  if (aligned && a.L % (128 * nv) == 0 && a.L >= 256 && a.L <= lmax && a.status && a.num_sms > 0) {
     const int threads = a.L / (4 * nv);
     const size_t smem = (size_t)NSTG * (a.idx ? 12 : 8) * a.L;
     static std::atomic<bool> attr_done[64];  // per device; setting the attribute twice is harmless

@@ -22,6 +22,7 @@ SMALL = [
     W("dense_odd", 2, 5, 24, 77, 77, 0, "dense", 15),
     W("dense_256", 1, 8, 64, 256, 256, 0, "dense", 16),                # staged dense score-grad rows
     W("uniform_small", 1, 16, 64, 130, 512, 256, "uniform", 17),       # uniform lengths, 2 full tiles per row
+    W("rows128_b2", 2, 16, 64, 90, 300, 128, "causal", 20),            # 128-slot rows: packed score-grad rows
 ]
 
 
