@@ -50,8 +50,8 @@ GEMM_FILES = ("blk.cu", "blk.h", "blk_pipe.cuh", "blk_pipe.cu", "gemm.cu", "kcom
 SCORE_GRAD_FILES = ("score_grad.cu",)
 PROFILED_TRAFFIC = {
     # k_to_f16 + select + union + q_image + blk + (exiting) per-row kernels of one gemm-stage call
-    ("anchor", "atomic", "gemm_stage"): ("6b6c5692434484f4cab0e9b49e8978b00489a5f0502fa5f5758f7fd670ef9824", 1.062e6 + 4.212e6 + 83.763e6 + 218.850e6 + 423.690e6 + 0.070e6),
-    ("anchor", "atomic", "score_grad"): ("32716e0bdb141dfa50987a5d3f34f07eb40acf8a602b202185531f24332fc497", 102.840e6),
+    ("anchor", "atomic", "gemm_stage"): ("1ca899f01e28149162b43c529cb4544798420a264a4ffcb3b741a9f9a21e30fc", 1.063e6 + 4.211e6 + 83.701e6 + 219.202e6 + 423.594e6 + 0.068e6),
+    ("anchor", "atomic", "score_grad"): ("56e45ec7b1c5fb62867535e1ef1414916bef85b0738b22445c9f9c2b9e269420", 102.835e6),
 }
 
 
