@@ -7,6 +7,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include "blk.h"
 
 namespace ibwd {
@@ -474,60 +476,6 @@ __global__ void __launch_bounds__(128) select_kernel(const int32_t* __restrict__
   }
 }
 
-struct QImg {  // the Q operand images of every block
-  const uint16_t* q;
-  uint8_t* img;
-  unsigned* qmax;  // if set: per block, max |q| as bf16 bits (zeroed before)
-  long long nblocks;
-  int S_q, H, D, nbpb;
-};
-
-// Chunk x of the images (16 bytes; 4096 per block).
-__device__ __forceinline__ QChunk q_image_at(const QImg& qi, long long x) {
-  const long long blk = x / (NR * 16);
-  const int within = (int)(x % (NR * 16));
-  const int batch = (int)(blk / qi.nbpb), t0 = (int)(blk % qi.nbpb) * R;
-  return q_image_chunk(qi.q, qi.img + blk * QIMG_BYTES, (long long)batch * qi.S_q + t0, min(R, qi.S_q - t0), qi.H,
-                       qi.D, within >> 4, within & 15);
-}
-
-// The q images, on the side stream beside the union pass (or the dense
-// scale pass).  A thread loads QIMG_ILP chunks before it stores any: the
-// stores could alias q as far as the compiler knows, so loads interleaved
-// with stores would be issued one at a time.
-constexpr int QIMG_ILP = 4;
-__global__ void q_image_kernel(const QImg qi, unsigned* __restrict__ status, const unsigned* __restrict__ select) {
-  if (select && __ldcg(select) != 0u) return;  // the per-row kernel serves this call
-  const long long nq = qi.nblocks * (NR * 16);
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  bool bad = false;
-  for (long long x = blockIdx.x * (long long)blockDim.x + threadIdx.x; x < nq; x += QIMG_ILP * stride) {
-    QChunk ch[QIMG_ILP];
-    uint4 v[QIMG_ILP];
-#pragma unroll
-    for (int k = 0; k < QIMG_ILP; ++k) {
-      const long long y = x + k * stride;
-      ch[k] = y < nq ? q_image_at(qi, y) : QChunk{nullptr, nullptr};
-    }
-#pragma unroll
-    for (int k = 0; k < QIMG_ILP; ++k) v[k] = ch[k].src ? __ldg(ch[k].src) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int k = 0; k < QIMG_ILP; ++k)
-      if (ch[k].dst) bad |= q_image_put(ch[k].dst, v[k]);
-    if (qi.qmax) {
-      // a warp's 32 chunks are consecutive and lie in one block (4096 chunks
-      // per block, 32-aligned): one maximum per warp and chunk step
-#pragma unroll
-      for (int k = 0; k < QIMG_ILP; ++k) {
-        const unsigned m = __reduce_max_sync(0xffffffffu, bf16x8_abs_max(v[k]));
-        const long long y = x + k * stride;
-        if ((threadIdx.x & 31) == 0 && y < nq && m != 0u) atomicMax(qi.qmax + y / (NR * 16), m);
-      }
-    }
-  }
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, DEV_FP16_RANGE);
-}
-
 // Dense blocks: block b holds keys [0, t0 + Rb); its dz scale exponent from
 // max |dI| over each row's causal keys and max |w|, written to binfo (the
 // gemm kernel's scan reads it).  One CTA of four warps per block, warp r on
@@ -650,20 +598,36 @@ unsigned long long test_timeout_ns() {
   return ns < 1000 ? 1000 : (ns > 2000000000ull ? 2000000000ull : ns);
 }
 std::atomic<int> g_attr_union[64];
-std::atomic<int> g_attr_qimg[64];
 
-// The q image kernel asks for the largest shared-memory carveout although it
-// uses none: an SM whose carveout was set for it could not take the union
-// pass's CTAs (~53 KB each at the anchor) beside it until it drained.
-bool set_qimg_carveout() {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && g_attr_qimg[dev].load(std::memory_order_acquire)) return true;
-  if (cudaFuncSetAttribute((const void*)q_image_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-    return false;
-  if (dev >= 0 && dev < 64) g_attr_qimg[dev].store(1, std::memory_order_release);
-  return true;
+// q as the gemm kernel's TMA source: a 4-d bf16 tensor [B][S_q][H][D] (D
+// innermost), boxes of 4 rows x 64 heads x 64 columns, the 128-byte swizzle;
+// elements past S_q, H or D read as zero.  The encoder is the driver's,
+// reached through the runtime (no link against the driver library).
+bool encode_q_map(CUtensorMap* m, const uint16_t* q, int B, int S_q, int H, int D) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::atomic<int> state{0};  // 0 not looked up, 1 found, 2 missing
+  int st = state.load(std::memory_order_acquire);
+  if (st == 0) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult res{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &res) ==
+            cudaSuccess &&
+        res == cudaDriverEntryPointSuccess && fn) {
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      st = 1;
+    } else {
+      st = 2;
+    }
+    state.store(st, std::memory_order_release);
+  }
+  if (st != 1) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S_q, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S_q * H * D * 2};
+  const cuuint32_t box[4] = {64, 64, (cuuint32_t)R, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(q), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Test of the pipeline's ordering: IBWD_TEST_SHALLOW_PIPELINE=1 in the
@@ -707,8 +671,6 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
   off = up(off + 256);
   w.k16 = off;
   off = up(off + (size_t)B * (S_k + 1) * kDP * 2);
-  w.qimg = off;
-  off = up(off + (size_t)w.nblocks * QIMG_BYTES);
   w.binfo = off;
   off = up(off + (size_t)w.nblocks * 16);
   if (!dense) {
@@ -732,11 +694,8 @@ WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int
     }
     w.u = off;
     off = up(off + (size_t)w.entries_cap * u_row_bytes(D));
-    // the key counts and the q maxima are contiguous: one zeroing covers both
     w.hist = off;
-    if (!dense) off += (size_t)w.nchunks * S_k * 4;
-    w.qmax = off;
-    off = up(off + (size_t)w.nblocks * 4);
+    if (!dense) off = up(off + (size_t)w.nchunks * S_k * 4);
     w.key_start = off;
     off = up(off + ((size_t)B * S_k + 1) * 4);
   }
@@ -750,7 +709,6 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   char* ws = static_cast<char*>(a.ws);
   __half* k16 = reinterpret_cast<__half*>(ws + lay.k16);
   unsigned* sched = reinterpret_cast<unsigned*>(ws + lay.sched);
-  uint8_t* qimg = reinterpret_cast<uint8_t*>(ws + lay.qimg);
   int4* binfo = reinterpret_cast<int4*>(ws + lay.binfo);
   // The per-row kernel can serve atomic sparse calls without options (and
   // keys that fit select_kernel's bitmap); select_kernel chooses on the
@@ -762,12 +720,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   // programmatic only right after this library's score-grad kernel: the
   // kernel reads k before it waits for its predecessor
   int* hist = (a.deterministic && !dense) ? reinterpret_cast<int*>(ws + lay.hist) : nullptr;
-  unsigned* qmax = a.deterministic ? reinterpret_cast<unsigned*>(ws + lay.qmax) : nullptr;
-  // deterministic mode: the key counts and the q maxima (contiguous) start at zero
-  const long long nzero = a.deterministic ? (hist ? lay.nchunks * a.S_k : 0LL) + lay.nblocks : 0LL;
-  // the k copy, the choice and the q images: on the side stream already
-  // forked by a one-call entry point (beside its score-grad), else on the
-  // call's stream with the images forked after the choice
+  // deterministic sparse mode: the key counts start at zero
+  const long long nzero = hist ? lay.nchunks * a.S_k : 0LL;
+  // the k copy and the choice: on the side stream already forked by a
+  // one-call entry point (beside its score-grad), else on the call's stream
   const cudaStream_t pre = a.early_side ? a.side : st;
   cudaError_t e = launch_k_to_f16(a.k, k16, a.B, a.S_k, a.D, sched, SCHED_ZERO, a.status,
                                   a.after_score_grad != 0 && !a.early_side, a.num_sms, pre,
@@ -781,28 +737,10 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
                   a.S_k, a.L, lay.nbpb, stride, sched, forced);
     if (e != cudaSuccess) return e;
   }
-  // the q images on the side stream: the union pass (or the dense scale
-  // pass) is latency-bound and leaves the memory system mostly idle, so the
-  // two overlap; the gemm kernel waits for both
   if (a.early_side) {
     // the union pass reads the choice and the zeroed counters
     e = cudaEventRecord(a.ev_sel, a.side);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, a.ev_sel, 0);
-  } else {
-    e = cudaEventRecord(a.ev_fork, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(a.side, a.ev_fork, 0);
-  }
-  if (e != cudaSuccess) return e;
-  {
-    const QImg qi{a.q, qimg, qmax, lay.nblocks, a.S_q, a.H, a.D, lay.nbpb};
-    const long long n = lay.nblocks * (NR * 16);
-    // four CTAs per SM: the union pass keeps three of its four while both run
-    // (measured: 30 us faster than two CTAs per SM at the anchor)
-    const int blocks = (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, 4LL * a.num_sms));
-    if (!set_qimg_carveout()) return cudaErrorInvalidValue;
-    q_image_kernel<<<blocks, 256, 0, a.side>>>(qi, a.status, select);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) e = cudaEventRecord(a.ev_join, a.side);
     if (e != cudaSuccess) return e;
   }
   if (!dense) {
@@ -841,12 +779,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     e = launch_det_sort(a, lay, st);
     if (e != cudaSuccess) return e;
   }
-  e = cudaStreamWaitEvent(st, a.ev_join, 0);
-  if (e != cudaSuccess) return e;
+  CUtensorMap qmap;
+  if (!encode_q_map(&qmap, a.q, a.B, a.S_q, a.H, a.D)) return cudaErrorInvalidValue;
   BParams p{};
   p.q = a.q;
   p.k16 = k16;
-  p.qimg = qimg;
   p.w = a.w;
   p.dI = a.dI;
   p.rec = dense ? nullptr : ws + lay.rec;
@@ -856,7 +793,6 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.dw = a.dw;
   p.dk = a.dk;
   p.u = a.deterministic ? ws + lay.u : nullptr;
-  p.qmax = qmax;
   p.dq16 = a.dq16;
   p.dw16 = a.dw16;
   p.sched = sched;
@@ -880,7 +816,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
   p.rstride = lay.rstride;
   p.dense_batch_entries = (dense && a.deterministic) ? lay.entries_cap / a.B : 0;
   const int grid = (int)std::min<long long>(a.num_sms, lay.nblocks);
-  e = test_shallow_pipeline() ? launch_blk_pipe<1, 2>(p, grid, st) : launch_blk_pipe<2, 4>(p, grid, st);
+  e = test_shallow_pipeline() ? launch_blk_pipe<1, 2>(p, qmap, grid, st) : launch_blk_pipe<2, 4>(p, qmap, grid, st);
   if (e != cudaSuccess) return e;
   if (choose) {
     // the per-row kernel: runs only if chosen (then the blocked kernel has

@@ -28,6 +28,8 @@
 #pragma once
 #include <atomic>
 
+#include <cuda.h>  // CUtensorMap
+
 #include "kcommon.cuh"
 
 namespace ibwd {
@@ -44,40 +46,16 @@ constexpr uint32_t REC_BYTES = 3072;
 // A block's q rows as the gemm kernel's Q operand: fp16, [d-half][(r,h) =
 // 64r + h][128 B], each 128-byte row's 16-byte chunks in the 128-byte swizzle
 // (chunk c of row n at (c ^ n % 8) * 16); rows past the block, heads past H
-// and columns past D zero.  Built once per call, copied as it is.
+// and columns past D zero.  Two TMA tile loads of q (bf16) land in exactly
+// this layout; the kernel converts them to fp16 in place.
 constexpr uint32_t QIMG_HALF = NR * 128;  // one 64-column half: 32 KB
 constexpr uint32_t QIMG_BYTES = 2 * QIMG_HALF;
-
-// One 16-byte chunk of a block's image: chunk c (0..15, 8 columns each) of
-// (r,h) row n (0..255) of the block whose first q row is global row row0
-// (Rb rows).  Its source in q (nullptr: a zero chunk) and its place in img.
-struct QChunk {
-  const uint4* src;
-  uint4* dst;
-};
-__device__ __forceinline__ QChunk q_image_chunk(const uint16_t* q, uint8_t* img, long long row0, int Rb, int H, int D,
-                                                int n, int c) {
-  const int r = n >> 6, h = n & 63;
-  QChunk o;
-  o.src = (r < Rb && h < H && c * 8 < D) ? reinterpret_cast<const uint4*>(q + ((row0 + r) * H + h) * D + c * 8)
-                                         : nullptr;
-  o.dst = reinterpret_cast<uint4*>(img + (c >> 3) * QIMG_HALF + n * 128 + (((c & 7) ^ (n & 7)) << 4));
-  return o;
-}
-
-// Writes the fp16 form of eight bf16 values; returns whether one lies
-// outside the fp16 range.
-__device__ __forceinline__ bool q_image_put(uint4* dst, uint4 v) {
-  *dst = make_uint4(bf16x2_to_half2(v.x), bf16x2_to_half2(v.y), bf16x2_to_half2(v.z), bf16x2_to_half2(v.w));
-  return bf16x2_out_of_fp16(v.x) || bf16x2_out_of_fp16(v.y) || bf16x2_out_of_fp16(v.z) || bf16x2_out_of_fp16(v.w);
-}
 
 struct BParams {
   const uint16_t* q;   // bf16 [rows, H, D]
   const __half* k16;   // [B][S_k + 1][128]; row S_k of each batch is zero
   const float* w;      // [rows, H]
   const float* dI;     // dense: [rows, S] (sparse blocks read their tile records instead)
-  const uint8_t* qimg; // per block: the Q operand image
   const char* rec;     // sparse: tile records
   const int4* binfo;   // per block {tiles, c, entries, 0}
   const int* border;   // sparse: processing order of the blocks
@@ -85,7 +63,6 @@ struct BParams {
   float* dw;
   float* dk;           // [B, S_k, D] (atomic mode)
   char* u;             // deterministic: per-entry dK rows in key order (u_row_bytes(D) each), or nullptr
-  const unsigned* qmax;  // deterministic: per block, max |q| as bf16 bits
   uint16_t* dq16;      // bf16 outputs instead of dq / dw when set
   uint16_t* dw16;
   unsigned* sched;     // block counter, zeroed by the k conversion kernel
@@ -120,11 +97,13 @@ inline bool set_smem_attr(const void* fn, size_t bytes, std::atomic<int>* done) 
 // tile-record slots.  <2, 4> is the one the library runs (blk_pipe.cu);
 // <1, 2> (blk_pipe_shallow.cu) exists to test that the results do not depend
 // on the depths.
+// qmap: q as a 4-d bf16 tensor [B][S_q][H][D] with boxes of 4 rows x 64
+// heads x 64 columns and the 128-byte swizzle (one block's Q operand half).
 template <int KST, int MST>
-cudaError_t launch_blk_pipe(const blk::BParams& p, int grid, cudaStream_t st);
+cudaError_t launch_blk_pipe(const blk::BParams& p, const CUtensorMap& qmap, int grid, cudaStream_t st);
 template <>
-cudaError_t launch_blk_pipe<2, 4>(const blk::BParams& p, int grid, cudaStream_t st);
+cudaError_t launch_blk_pipe<2, 4>(const blk::BParams& p, const CUtensorMap& qmap, int grid, cudaStream_t st);
 template <>
-cudaError_t launch_blk_pipe<1, 2>(const blk::BParams& p, int grid, cudaStream_t st);
+cudaError_t launch_blk_pipe<1, 2>(const blk::BParams& p, const CUtensorMap& qmap, int grid, cudaStream_t st);
 
 }  // namespace ibwd

@@ -27,8 +27,8 @@
 //         (bulk copy; dense blocks: builds it from dI), publishes the block
 //   3     Z MMA issuer (one elected lane) and TMEM owner
 //   4     dQ / dK MMA issuer
-//   5-7   Q loader: the block's q rows by cp.async, converted to fp16 in
-//         place; w
+//   5-7   Q loader: the block's q rows by two TMA tile loads (bf16, landing
+//         in the operand's swizzled layout), converted to fp16 in place; w
 //   8-23  dz: Z -> mask, dW partial, fp16 dz tile; at block end dW and the
 //         dQ epilogue (TMEM -> fp32)
 //   24-31 dK: dK^T tile from TMEM -> fp32 red.global.add (one 128-byte line
@@ -77,7 +77,7 @@ struct Bars {
   uint64_t kfull[KST], kempty[KST];
   uint64_t mfull[MST], mempty[MST];
   uint64_t bfull[BQ], bempty[BQ];
-  uint64_t qfull, qempty;
+  uint64_t qfull[2], qempty, qraw;  // qfull[h]: (r,h) rows 128h .. 128h+127 of Q converted
   uint64_t zfull, zempty;
   uint64_t dzfull, dzempty;
   uint64_t dkfull, dkempty;
@@ -196,13 +196,14 @@ __device__ void scan_role(const BParams& p, const Ctx& cx) {
     // dense scale pass)
     const int4 bi = __ldg(p.binfo + b);
     const int ntiles = bi.x, c = bi.y, U = bi.z;
-    const int qe = p.qmax ? q_exponent(__ldcg(p.qmax + b)) : 0;
+    const int qe = 0;  // deterministic rows take the block's q exponent from the Q loader
     // publish the block to the Q loader; warm L2 with its q rows
     if (!WAIT(&B->bempty[i % BQ], ((i / BQ) & 1) ^ 1)) return drain_records();
     if (lane == 0) {
       bq[i % BQ] = make_int4(row0, Rb, (int)b, 0);
       mbar_arrive(&B->bfull[i % BQ]);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.qimg + b * QIMG_BYTES), "r"(QIMG_BYTES)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.q + (long long)row0 * p.H * p.D),
+                   "r"((uint32_t)(Rb * p.H * p.D * 2))
                    : "memory");
     }
     unsigned pend = 0;
@@ -303,24 +304,28 @@ __device__ void gather_role(const BParams& p, const Ctx& cx) {
 }
 
 // ------------------------------------------------------------- Q loader ---
-// The block's Q operand image (fp16, already swizzled: built by the union
-// pass or the k conversion kernel) arrives by one bulk copy once the previous
-// block's last MMA that reads Q is complete; the loader warps meanwhile put
-// the block's w in shared memory.
-__device__ void q_role(const BParams& p, const Ctx& cx) {
+// Once the previous block's last MMA that reads Q is complete, the block's q
+// rows arrive as two TMA tile loads (the two 64-column halves: 4 rows x 64
+// heads x 64 columns of bf16 each, rows past S_q, heads past H and columns
+// past D zero), already in the Q operand's swizzled layout; the loader warps
+// then convert them to fp16 in place (the range check and, in deterministic
+// mode, the block's largest |q| on the way) and put the block's w in shared
+// memory.
+__device__ void q_role(const BParams& p, const Ctx& cx, const CUtensorMap* qmap) {
   const int tid = threadIdx.x - W_Q0 * 32;  // 0..95
   Bars* B = cx.bars;
   const int4* bq = reinterpret_cast<const int4*>(cx.smem + OFF_BQ);
   float* w_s = reinterpret_cast<float*>(cx.smem + OFF_W);
-  long long issued = -1;  // the last block whose image copy was issued
-  // before the role returns: that copy has landed (its phase completes once
-  // every loader thread has arrived and the bytes are in)
+  unsigned* qmax_s = reinterpret_cast<unsigned*>(cx.smem + OFF_MISC + 8);  // [2]: by block parity
+  long long issued = -1, landed = -1;  // the last blocks whose loads were issued / waited for
+  // before the role returns: loads in flight have landed
   auto drain = [&]() {
-    if (issued >= 0) drain_wait(&B->qfull, (uint32_t)(issued & 1), p.status, p.drain_ns);
+    if (tid == 0 && issued > landed) drain_wait(&B->qraw, (uint32_t)(issued & 1), p.status, p.drain_ns);
   };
+  constexpr int ILP = 4;                       // chunks loaded before any is stored
   for (long long i = 0;; ++i) {
     if (!WAIT(&B->bfull[i % BQ], (i / BQ) & 1)) return drain();
-    const int row0 = bq[i % BQ].x, Rb = bq[i % BQ].y, blk = bq[i % BQ].z;
+    const int row0 = bq[i % BQ].x, Rb = bq[i % BQ].y;
     mbar_arrive(&B->bempty[i % BQ]);
     if (row0 < 0) return drain();
     float wv[(NR + NQT - 1) / NQT];  // w of the block
@@ -331,16 +336,56 @@ __device__ void q_role(const BParams& p, const Ctx& cx) {
     }
     // the previous block's last MMAs that read Q (and its w) are complete
     if (!WAIT(&B->qempty, (i & 1) ^ 1)) return drain();
-    issued = i;
     if (tid == 0) {
       TRACE(EV_Q_START, (int)i);
-      mbar_expect_tx(&B->qfull, QIMG_BYTES);
-      bulk_g2s(cx.sbase + OFF_Q, p.qimg + (long long)blk * QIMG_BYTES, QIMG_BYTES, &B->qfull);
+      if (p.u) qmax_s[i & 1] = 0u;
+      const int batch = row0 / p.S_q, t0 = row0 - batch * p.S_q;
+      mbar_arrive_expect_tx(&B->qraw, QIMG_BYTES);
+      tma_load_4d(cx.sbase + OFF_Q, qmap, 0, 0, t0, batch, &B->qraw);
+      tma_load_4d(cx.sbase + OFF_Q + QDH, qmap, 64, 0, t0, batch, &B->qraw);
     }
+    issued = i;
 #pragma unroll
     for (int k = 0; k < (NR + NQT - 1) / NQT; ++k)
       if (tid + NQT * k < NR) w_s[tid + NQT * k] = wv[k];
-    mbar_arrive(&B->qfull);  // the phase completes when the copy has landed too
+    if (!WAIT(&B->qraw, i & 1)) return drain();
+    landed = i;
+    // rows 0-1 first ((r,h) 0..127 of both 64-column halves: the first Z
+    // MMA of the block needs only them), then rows 2-3
+    unsigned mx = 0u;  // largest |q| as bf16 bits (above 0x477F: outside the fp16 range)
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      constexpr int HCH = (int)(QIMG_BYTES / 32);  // chunks of one pair of rows: 2048
+      const uint32_t base = cx.sbase + OFF_Q + (uint32_t)hf * (QDH / 2);
+#pragma unroll 1
+      for (int y0 = tid; y0 < HCH; y0 += ILP * NQT) {
+        uint4 v[ILP];
+        uint32_t at[ILP];
+#pragma unroll
+        for (int k = 0; k < ILP; ++k) {
+          const int y = y0 + k * NQT;  // chunk y & 1023 of 64-column half y >> 10
+          at[k] = base + (uint32_t)(y >> 10) * QDH + (uint32_t)(y & 1023) * 16;
+          v[k] = y < HCH ? ld_shared_v4(at[k]) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < ILP; ++k) {
+          if (y0 + k * NQT >= HCH) break;
+          mx = max(mx, bf16x8_abs_max(v[k]));
+          st_shared_v4(at[k], bf16x2_to_half2(v[k].x), bf16x2_to_half2(v[k].y), bf16x2_to_half2(v[k].z),
+                       bf16x2_to_half2(v[k].w));
+        }
+      }
+      if (hf == 1) {
+        if (__any_sync(FULL, mx > 0x477Fu) && (tid & 31) == 0) atomicOr(p.status, DEV_FP16_RANGE);
+        if (p.u) {
+          const unsigned m = __reduce_max_sync(FULL, mx);
+          if ((tid & 31) == 0 && m != 0u) atomicMax(&qmax_s[i & 1], m);
+        }
+      }
+      // the generic-proxy writes precede the tensor core's reads
+      fence_proxy_async_smem();
+      mbar_arrive(&B->qfull[hf]);
+    }
     if (tid == 0) TRACE(EV_Q_DONE, (int)i);
   }
 }
@@ -397,12 +442,12 @@ __device__ void zmma_role(const BParams& p, const Ctx& cx) {
     const int ms = (int)(g % MST), st = (int)(g % KST);
     if (!WAITW(&B->mfull[ms], (g / MST) & 1)) break;
     const int flags = cx.hdr[ms].flags;
-    if ((flags & F_FIRST) && !WAITW(&B->qfull, i & 1)) break;
     if (!WAITW(&B->kfull[st], (g / KST) & 1)) break;
     bool ok = true;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-      if (!WAITW(&B->zempty, (zi & 1) ^ 1)) {
+      // a block's first Z of each pair of rows waits for those rows' q
+      if (((flags & F_FIRST) && !WAITW(&B->qfull[half], i & 1)) || !WAITW(&B->zempty, (zi & 1) ^ 1)) {
         ok = false;
         break;
       }
@@ -550,7 +595,7 @@ __device__ void dz_role(const BParams& p, const Ctx& cx) {
     const int flags = cx.hdr[ms].flags, c = cx.hdr[ms].c;
     if (flags & F_FIRST) {
       ++i;
-      if (!WAIT(&B->qfull, i & 1)) return;
+      if (!WAIT(&B->qfull[0], i & 1)) return;  // and w
       wv0 = w_s[nrow];
       wv1 = w_s[128 + nrow];
       acc0 = acc1 = 0.f;
@@ -634,11 +679,16 @@ __device__ void dk_role(const BParams& p, const Ctx& cx) {
   const int idmax = p.u ? (int)(p.dense ? (long long)p.B * p.dense_batch_entries - 1
                                         : p.nblocks * min((long long)p.S_k, (long long)R * p.L) - 1)
                         : p.S_k - 1;
+  unsigned nb = 0;  // blocks before this tile's (its parity is what is used)
   for (long long g = 0;; ++g) {
     const int ms = (int)(g % MST);
     if (!WAIT(&B->mfull[ms], (g / MST) & 1)) return;
     const int flags = cx.hdr[ms].flags, c = cx.hdr[ms].c, count = cx.hdr[ms].count, batch = cx.hdr[ms].batch;
-    const int qe = cx.hdr[ms].qe;
+    // deterministic: the Q loader's maximum of this block, complete once its
+    // q is (the next phase of qfull needs this block's last dK MMA, which
+    // needs this role)
+    if (p.u && (flags & F_FIRST) && !WAIT(&B->qfull[1], nb & 1)) return;
+    const int qe = p.u ? q_exponent(reinterpret_cast<const unsigned*>(cx.smem + OFF_MISC + 8)[nb & 1]) : 0;
     float* base = p.dk + (long long)batch * p.S_k * p.D;
     const int* ids = p.u ? rec_pos(cx, ms) : rec_key(cx, ms);
     if (!WAIT(&B->dkfull, g & 1)) return;
@@ -665,11 +715,12 @@ __device__ void dk_role(const BParams& p, const Ctx& cx) {
     mbar_arrive(&B->dkempty);
     mbar_arrive(&B->mempty[ms]);
     if (threadIdx.x == W_DK0 * 32) TRACE(EV_DK_DONE, (int)g);
+    if (flags & F_LAST) ++nb;
     if (flags & F_END) return;
   }
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctx cx;
@@ -695,8 +746,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
       mbar_init(&B->bfull[i], 1);
       mbar_init(&B->bempty[i], NQT);
     }
-    mbar_init(&B->qfull, NQT);
+    mbar_init(&B->qfull[0], NQT);
+    mbar_init(&B->qfull[1], NQT);
     mbar_init(&B->qempty, 1);
+    mbar_init(&B->qraw, 1);
     mbar_init(&B->zfull, 1);
     mbar_init(&B->zempty, NDZT);
     mbar_init(&B->dzfull, NDZT);
@@ -735,7 +788,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) blk_kernel(const BParams p) {
   } else if (warp == W_GMMA) {
     gmma_role(p, cx);
   } else if (warp < W_DZ0) {
-    q_role(p, cx);
+    q_role(p, cx, &qmap);
   } else if (warp < W_DK0) {
     dz_role(p, cx);
   } else {
@@ -754,9 +807,9 @@ std::atomic<int> g_attr_pipe[64];
 }  // namespace
 
 template <>
-cudaError_t launch_blk_pipe<KST, MST>(const blk::BParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_blk_pipe<KST, MST>(const blk::BParams& p, const CUtensorMap& qmap, int grid, cudaStream_t st) {
   if (!set_smem_attr((const void*)blk_kernel, SMEM_BYTES, g_attr_pipe)) return cudaErrorInvalidValue;
-  return launch_ex(blk_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p);
+  return launch_ex(blk_kernel, (unsigned)grid, (unsigned)NTHREADS, SMEM_BYTES, st, true, p, qmap);
 }
 
 #if IBWD_PIPE_PRIMARY

@@ -84,13 +84,11 @@ struct GemmArgs {
 struct WsLayout {
   size_t sched;      // 256 bytes: [0] the gemm kernel's block counter, [1] the union pass's CTA counter
   size_t k16;        // fp16 copy of k, [B, S_k + 1, 128]
-  size_t qimg;       // per block: its q rows as the gemm kernel's fp16 Q operand image (64 KB)
   size_t binfo;      // int4 per block {tiles, dz scale exponent, entries, 0}
   size_t border;     // sparse: the blocks in descending tile count (processing order)
   size_t rec;        // sparse: tile records [nblocks][tcap][rstride bytes]
   size_t u;          // deterministic: per-entry dK rows [entries_cap][u_row_bytes(D)], in key order
   size_t hist;       // deterministic sparse: per-chunk key counts [nchunks, S_k] int32
-  size_t qmax;       // deterministic: per block, max |q| as bf16 bits (right after hist: zeroed with it)
   size_t key_start;  // deterministic: CSR offsets into u [B*S_k + 1] int32
   size_t total;
   long long nblocks;      // B * nbpb

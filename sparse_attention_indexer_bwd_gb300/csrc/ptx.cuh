@@ -339,6 +339,26 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Tiled 4-d load by the TMA engine through a tensor map (a __grid_constant__
+// kernel parameter): the box at element coordinates (c0, c1, c2, c3), c0
+// innermost, lands in shared memory as the map lays it out (swizzle
+// included), elements outside the tensor read as zero; completes the box's
+// bytes on `bar`.  c0 times the element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 // Bulk shared->global copy by the TMA engine (async proxy), in this thread's
 // current bulk group.  Both addresses 16-byte aligned, bytes % 16 == 0; the
 // shared source must be made visible to the async proxy first.

@@ -49,23 +49,22 @@ def test_status_strings(lib):
 def test_workspace_sizes(lib):
     a = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_ATOMIC)
     nb, tcap = 8192 // 4, 4096 // 128       # blocks of four query rows; records per block (min(S_k, 4*topk) keys)
-    qimg = nb * 65536                        # per block: its q rows as the fp16 Q operand image
-    # counters + fp16 copy of k (+ a zero row) + q images + per-block info and order + the tile records
-    assert a == 256 + 4097 * 128 * 2 + qimg + nb * 16 + nb * 4 + nb * tcap * 2560
+    # counters + fp16 copy of k (+ a zero row) + per-block info and order + the tile records
+    assert a == 256 + 4097 * 128 * 2 + nb * 16 + nb * 4 + nb * tcap * 2560
     d = ibwd.indexer_bwd_gemm_workspace_size(1, 8192, 4096, 64, 128, 1024, ibwd.IBWD_DK_DETERMINISTIC)
     ent = nb * 4096                          # (block, key) entries at most
     u = ent * (128 * 2 + 32)                 # per entry a scaled fp16 dK row and a sector with its factor
     keyoff = ((4096 + 1) * 4 + 255) // 256 * 256
-    # key counts per two blocks and the blocks' q maxima share one padded part
-    sort = ((nb // 2) * 4096 * 4 + nb * 4 + 255) // 256 * 256
+    # key counts per two blocks
+    sort = ((nb // 2) * 4096 * 4 + 255) // 256 * 256
     assert d == a + nb * tcap * 512 + u + sort + keyoff
     dnb = 4096 // 4
-    dense = 256 + 4097 * 128 * 2 + dnb * 65536 + dnb * 16
+    dense = 256 + 4097 * 128 * 2 + dnb * 16
     assert ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 0) == dense
     # dense deterministic: block j holds keys [0, 4j + 4): sum over j of 4(j + 1) dK rows
     dd = ibwd.indexer_bwd_dense_gemm_workspace_size(1, 4096, 64, 128, 1)
     dent = 4 * (1024 * 1025 // 2)
-    assert dd == dense + dent * (128 * 2 + 32) + dnb * 4 + keyoff
+    assert dd == dense + dent * (128 * 2 + 32) + keyoff
     # unsupported shapes report 0
     assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 65, 128, 4, 0) == 0
     assert ibwd.indexer_bwd_gemm_workspace_size(1, 8, 8, 4, 12, 4, 0) == 0
