@@ -12,12 +12,12 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   unsigned* status = nullptr;  // one device word, allocated once
-  // a second stream for work that runs beside the caller's stream within one
-  // call (the gemm stage's q images), and the events that fork and join it;
-  // at the highest priority, so that the images (the later of the two to
-  // finish otherwise) take the SMs first as the union pass's CTAs retire
+  // a second stream for work that runs beside the caller's stream within a
+  // one-call step (the k copy and the kernel choice, beside the score-grad),
+  // at the highest priority; the event that forks it and the one that joins
+  // the union pass to the choice
   cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr, sel = nullptr;
+  cudaEvent_t fork = nullptr, sel = nullptr;
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -43,7 +43,6 @@ int device_info(DeviceInfo** out) {
       if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
           cudaStreamCreateWithPriority(&d.side, cudaStreamNonBlocking, greatest) != cudaSuccess ||
           cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&d.sel, cudaEventDisableTiming) != cudaSuccess)
         return IBWD_ERR_CUDA;
     }
@@ -184,11 +183,10 @@ int gemm_common(const uint16_t* q, const uint16_t* k, const float* w, const floa
   a.num_sms = dv->num_sms;
   a.side = dv->side;
   a.ev_fork = dv->fork;
-  a.ev_join = dv->join;
   a.ev_sel = dv->sel;
   if (I) {
     // the gemm stage's work that needs neither dI nor the score-grad's dK
-    // zeroing (k copy, kernel choice, q images) starts beside the score-grad
+    // zeroing (k copy, kernel choice) starts beside the score-grad
     // on the side stream, after everything queued before this call
     if (cudaEventRecord(dv->fork, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
         cudaStreamWaitEvent(dv->side, dv->fork, 0) != cudaSuccess)

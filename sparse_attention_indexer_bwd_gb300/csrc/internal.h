@@ -63,11 +63,11 @@ struct GemmArgs {
   uint16_t* dw16;        // if set: dw likewise
   uint16_t* dk16;        // if set: bf16 copy of the final dk, written after it
   float sm_scale;        // logit scale s (> 0; 0 reads as 1): dq, dw, dk are s times the unscaled results
-  cudaStream_t side;     // a second stream of the device, forked from and joined to the call's stream
-  cudaEvent_t ev_fork, ev_join;
+  cudaStream_t side;     // a second stream of the device
+  cudaEvent_t ev_fork;
   // set by the one-call entry points, which fork the side stream before
-  // their score-grad: the k copy, the kernel choice and the q images then run
-  // on it beside the score-grad, and ev_sel (recorded after the choice) holds
+  // their score-grad (ev_fork): the k copy and the kernel choice then run on
+  // it beside the score-grad, and ev_sel (recorded after the choice) holds
   // back the union pass until the choice is made
   int early_side;
   cudaEvent_t ev_sel;
@@ -100,9 +100,9 @@ struct WsLayout {
 };
 WsLayout gemm_workspace_layout(int B, int S_q, int S_k, int H, int D, int L, int deterministic, int dense);
 
-// The blocked gemm stage (blk.cu): fp16 copy of k, the q images, the union
-// pass (sparse) or the scale pass (dense), the deterministic sort (det.cu),
-// the gemm kernel, the segment sum.
+// The blocked gemm stage (blk.cu): fp16 copy of k, the union pass (sparse)
+// or the scale pass (dense), the deterministic sort (det.cu), the gemm
+// kernel (q by TMA, converted in place), the segment sum.
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st);
 
 // Deterministic mode (det.cu): the key sort of the blocks' entries (sparse) or

@@ -117,7 +117,7 @@ __device__ __forceinline__ void dk_chunk_tmem(float* base, const int* ids, uint3
 }
 
 // Exponent qe with max |q| < 2^qe, from the largest |q| of a block as bf16
-// bits (the q images hold fp16, where magnitudes below 2^-25 are zero, so
+// bits (the Q operand holds fp16, where magnitudes below 2^-25 are zero, so
 // qe >= -24 covers every nonzero operand; non-finite q raises the range
 // status and takes the top value).
 __device__ __forceinline__ int q_exponent(unsigned bits) {
