@@ -352,7 +352,7 @@ __device__ void q_role(const BParams& p, const Ctx& cx, const CUtensorMap* qmap)
     landed = i;
     // rows 0-1 first ((r,h) 0..127 of both 64-column halves: the first Z
     // MMA of the block needs only them), then rows 2-3
-    unsigned mx = 0u;  // largest |q| as bf16 bits (above 0x477F: outside the fp16 range)
+    uint32_t mx2 = 0u;  // largest |q| as bf16 bits, per 16-bit lane of a word
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
       constexpr int HCH = (int)(QIMG_BYTES / 32);  // chunks of one pair of rows: 2048
@@ -370,12 +370,15 @@ __device__ void q_role(const BParams& p, const Ctx& cx, const CUtensorMap* qmap)
 #pragma unroll
         for (int k = 0; k < ILP; ++k) {
           if (y0 + k * NQT >= HCH) break;
-          mx = max(mx, bf16x8_abs_max(v[k]));
+          mx2 = max_u16x2(mx2, max_u16x2(max_u16x2(v[k].x & 0x7FFF7FFFu, v[k].y & 0x7FFF7FFFu),
+                                         max_u16x2(v[k].z & 0x7FFF7FFFu, v[k].w & 0x7FFF7FFFu)));
           st_shared_v4(at[k], bf16x2_to_half2(v[k].x), bf16x2_to_half2(v[k].y), bf16x2_to_half2(v[k].z),
                        bf16x2_to_half2(v[k].w));
         }
       }
       if (hf == 1) {
+        // above 0x477F: outside the fp16 range
+        const unsigned mx = max(mx2 & 0xFFFFu, mx2 >> 16);
         if (__any_sync(FULL, mx > 0x477Fu) && (tid & 31) == 0) atomicOr(p.status, DEV_FP16_RANGE);
         if (p.u) {
           const unsigned m = __reduce_max_sync(FULL, mx);

@@ -431,6 +431,12 @@ __device__ __forceinline__ bool bf16x2_out_of_fp16(uint32_t v) {
 
 // The largest magnitude among eight bf16 (a uint4), as bf16 bits: for
 // finite values the bits of |x| order as the magnitudes do.
+// Lane-wise maximum of two pairs of unsigned 16-bit values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ unsigned bf16x8_abs_max(uint4 v) {
   auto m2 = [](uint32_t x) { return max(x & 0x7FFFu, (x >> 16) & 0x7FFFu); };
   return max(max(m2(v.x), m2(v.y)), max(m2(v.z), m2(v.w)));
